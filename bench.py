@@ -1,0 +1,503 @@
+#!/usr/bin/env python
+"""Throughput of libq4mm on GB300: decode weight-GB/s and prefill TFLOP/s, as fractions of
+the measured HBM and dense-bf16 rooflines.
+
+Headline workload (one "step"): the INT4 group-32 affine decode GEMV at every shape of the
+decode configuration -- M in {1, 4, 16} x (K, N) in {(4096, 14336), (14336, 4096),
+(4096, 4096)} -- one q4_gemv call per shape, each on a weight replica that is not in L2.
+value = algorithmic bytes of a step / device time of a step (GB/s).  The prefill GEMM,
+LUT4 and Q4_0 MoE paths are timed in the same run and reported beside it.
+
+Timing: inputs resident in HBM; steps are CUDA-graph replays timed with CUDA events on the
+launching stream; weights rotate through a ring of replicas whose total is >= 4x L2, so
+every call reads its weights from HBM.  nvidia-smi clocks are sampled during the timed
+region.  `--impl reference` times the CPU oracle on the host cores instead (a deliberately
+slow baseline on a bounded sample of the same workload).
+
+Multi-GPU: the path does not shard (replicas only); under torchrun every rank runs the same
+workload on its own GPU, and value = units of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "int4 qmm decode weight-GB/s & prefill TFLOP/s, % of GB300 roofline"
+DECODE_KN = [(4096, 14336), (14336, 4096), (4096, 4096)]
+DECODE_M = [1, 4, 16]
+PREFILL_KN = [(4096, 14336), (14336, 4096), (4096, 6144)]
+PREFILL_M = [512, 2048, 8192]
+HEADLINE = (1, 4096, 14336)   # (M, K, N) of the kernel whose roofline is reported
+
+
+def decode_shapes():
+    return [(M, K, N) for (K, N) in DECODE_KN for M in DECODE_M]
+
+
+def int4_bytes(M, K, N):
+    """Algorithmic bytes of one INT4 matmul call: codes + scales/biases + x + y."""
+    return N * K // 2 + N * (K // 32) * 4 + 2 * M * K + 2 * M * N
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------------------------------------------
+# clocks
+# ------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(mx)) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import weight_only_bit_int4_gb300 as q
+    from weight_only_bit_int4_gb300 import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    pk = peaks()
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        view = {np.dtype(np.uint16): np.int16, np.dtype(np.uint32): np.int32}.get(a.dtype, a.dtype)
+        return torch.from_numpy(a.view(view)).to(dev)
+
+    def ring_of(tensors, nbytes):
+        """Replicas of `tensors` so that the ring holds >= 4x L2."""
+        R = max(2, math.ceil(4 * l2 / nbytes))
+        return [tensors] + [tuple(t.clone() for t in tensors) for _ in range(R - 1)]
+
+    def time_graph(build_calls, launches_per_replay, replays, warmup=3):
+        """Capture build_calls() into a graph; return (seconds per replay)."""
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            build_calls(0)       # eager warm-up outside capture (first-call set-up)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            build_calls(1)
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(replays):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / replays
+
+    # ---------------- decode workload ----------------
+    rings = {}
+    for i, (K, N) in enumerate(DECODE_KN):
+        w, s, b = synth.int4_weights(1000 + i, N, K)
+        rings[(K, N)] = ring_of((to_dev(w), to_dev(s), to_dev(b)), N * K * 9 // 16)
+    xs, ys = {}, {}
+    for j, (M, K, N) in enumerate(decode_shapes()):
+        xs[(M, K, N)] = to_dev(synth.activations_bf16(1100 + j, M, K))
+        ys[(M, K, N)] = torch.empty((M, N), dtype=torch.int16, device=dev)
+    P = max(len(r) for r in rings.values())
+    step_bytes = sum(int4_bytes(*shp) for shp in decode_shapes())
+
+    # eager warm-up of every shape (first-call attribute set-up happens outside capture)
+    for shp in decode_shapes():
+        M, K, N = shp
+        q.q4_gemv(xs[shp], *rings[(K, N)][0], ys[shp])
+    torch.cuda.synchronize()
+
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graphs = []
+    with torch.cuda.stream(cap):
+        for p in range(P):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                for shp in decode_shapes():
+                    M, K, N = shp
+                    r = rings[(K, N)]
+                    q.q4_gemv(xs[shp], *r[p % len(r)], ys[shp])
+            graphs.append(g)
+    torch.cuda.synchronize()
+    launches_per_step = len(decode_shapes())
+
+    for i in range(max(3, args.warmup)):
+        graphs[i % P].replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        graphs[i % P].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    elapsed = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        torch.distributed.barrier()
+        t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed = float(t.item())
+    # per-shape and headline-kernel timings (same run, same clock sampling)
+    shape_rows = []
+    headline = None
+    for shp in decode_shapes():
+        M, K, N = shp
+        r = rings[(K, N)]
+        L = 2 * len(r)
+        def calls(_, shp=shp, r=r, L=L):
+            for l in range(L):
+                q.q4_gemv(xs[shp], *r[l % len(r)], ys[shp])
+        t = time_graph(calls, L, replays=max(5, args.steps // 10)) / L
+        by = int4_bytes(M, K, N)
+        row = {"M": M, "K": K, "N": N, "us": round(t * 1e6, 3), "GB_s": round(by / t / 1e9, 1),
+               "frac_hbm": round(by / t / 1e9 / pk["hbm_gbs"], 3)}
+        shape_rows.append(row)
+        if shp == HEADLINE:
+            headline = (t, by)
+    clocks = sampler.stop()
+
+    value = step_bytes * args.steps * world / elapsed / 1e9
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(elapsed / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "INT4 g32 affine decode GEMV, M in {1,4,16} x (K,N) in "
+                               "{(4096,14336),(14336,4096),(4096,4096)}, one call per shape per step",
+                   "l2": f"weights rotate through replicas totalling >= 4x L2 ({l2 >> 20} MiB)",
+                   "timing": "CUDA-graph replays, CUDA events on the launching stream",
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "decode_shapes": shape_rows,
+    }
+    t_h, by_h = headline
+    out["roofline"] = {"bound": "hbm", "kernel": "gemv_kernel (q4_gemv)",
+                       "shape": {"M": HEADLINE[0], "K": HEADLINE[1], "N": HEADLINE[2]},
+                       "achieved": round(by_h / t_h / 1e9, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                       "frac": round(by_h / t_h / 1e9 / pk["hbm_gbs"], 3),
+                       "frac_vs_8TBs": round(by_h / t_h / 8e12, 3),
+                       "peak_source": pk["source"] + " (hbm_gbs, burst copy)",
+                       "traffic": None}
+
+    # ---------------- e2e through the public API with host buffers ----------------
+    out["e2e"] = e2e_decode(args, q, synth, rings, dev)
+
+    if not args.quick:
+        out["prefill"] = bench_prefill(args, q, synth, to_dev, time_graph, dev, pk)
+        out["lut4"] = bench_lut4(args, q, synth, to_dev, ring_of, time_graph, dev, pk)
+        out["moe"] = bench_moe(args, q, synth, to_dev, ring_of, time_graph, dev, pk)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+    return out
+
+
+def e2e_decode(args, q, synth, rings, dev):
+    import torch
+    shapes = decode_shapes()
+    xh = {s: torch.from_numpy(synth.activations_bf16(1100 + j, s[0], s[1]).view(np.int16)).pin_memory()
+          for j, s in enumerate(shapes)}
+    yh = {s: torch.empty((s[0], s[2]), dtype=torch.int16).pin_memory() for s in shapes}
+    xd = {s: torch.empty((s[0], s[1]), dtype=torch.int16, device=dev) for s in shapes}
+    yd = {s: torch.empty((s[0], s[2]), dtype=torch.int16, device=dev) for s in shapes}
+    steps = max(3, min(args.steps, 50))
+    def one(i):
+        for s in shapes:
+            M, K, N = s
+            r = rings[(K, N)]
+            xd[s].copy_(xh[s], non_blocking=True)
+            q.q4_gemv(xd[s], *r[i % len(r)], yd[s])
+            yh[s].copy_(yd[s], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        one(i)
+    t = (time.perf_counter() - t0) / steps
+    by = sum(int4_bytes(*s) for s in shapes)
+    return {"value": round(by / t / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": sum(2 * s[0] * s[1] for s in shapes),
+            "d2h_bytes_per_step": sum(2 * s[0] * s[2] for s in shapes),
+            "ms_per_step": round(t * 1e3, 3),
+            "note": "python calls through the C ABI, pinned host x in / y out every call, weights resident"}
+
+
+def bench_prefill(args, q, synth, to_dev, time_graph, dev, pk):
+    import torch
+    rows = []
+    gen = torch.Generator(device=dev)
+    for i, (K, N) in enumerate(PREFILL_KN):
+        w, s, b = synth.int4_weights(2000 + i, N, K)
+        W = (to_dev(w), to_dev(s), to_dev(b))
+        gen.manual_seed(2100 + i)
+        xmax = torch.randn((max(PREFILL_M), K), generator=gen, device=dev, dtype=torch.float32)
+        out_cols = torch.randperm(K, generator=gen, device=dev)[: max(1, round(0.01 * K))]
+        xmax[:, out_cols] *= 20.0
+        xmax = xmax.to(torch.bfloat16).view(torch.int16)
+        for M in PREFILL_M:
+            x = xmax[:M]
+            y = torch.empty((M, N), dtype=torch.int16, device=dev)
+            flops = 2.0 * M * N * K
+            L = 2 if M == 8192 else 4
+            t = time_graph(lambda _: [q.q4_gemm(x, *W, y) for _ in range(L)], L,
+                           replays=3 if M == 8192 else 5) / L
+            tf = flops / t / 1e12
+            rows.append({"M": M, "K": K, "N": N, "us": round(t * 1e6, 2), "TFLOP_s": round(tf, 1),
+                         "frac_bf16_burst": round(tf / pk["bf16_tflops"], 3),
+                         "tokens_s": round(M / t, 0)})
+        del xmax
+        torch.cuda.empty_cache()
+    tot_f = sum(2.0 * r["M"] * r["K"] * r["N"] for r in rows)
+    tot_t = sum(r["us"] for r in rows) / 1e6
+    return {"kernel": "qgemm_tc_kernel (q4_gemm, tcgen05)", "shapes": rows,
+            "aggregate_TFLOP_s": round(tot_f / tot_t / 1e12, 1),
+            "aggregate_frac_bf16_burst": round(tot_f / tot_t / 1e12 / pk["bf16_tflops"], 3),
+            "x": "bf16 N(0,1), 1% columns x20, seeded torch generator on device"}
+
+
+def bench_lut4(args, q, synth, to_dev, ring_of, time_graph, dev, pk):
+    import torch
+    N = K = 4096
+    packed, scales, book = synth.lut4_weights(3000, N, K, 64)
+    ring = ring_of((to_dev(packed), to_dev(scales)), packed.nbytes + scales.nbytes)
+    rows = []
+    for M in (1, 512):
+        x = to_dev(synth.activations_bf16(3100 + M, M, K))
+        y = torch.empty((M, N), dtype=torch.int16, device=dev)
+        L = 2 * len(ring)
+        t = time_graph(lambda _: [q.lut4_matmul(x, *ring[l % len(ring)], book, y, N, K, 64, 1)
+                                  for l in range(L)], L, replays=10) / L
+        by = packed.nbytes + scales.nbytes + 64 + 2 * M * K + 2 * M * N
+        fl = 2.0 * M * N * K
+        rows.append({"M": M, "K": K, "N": N, "us": round(t * 1e6, 3), "GB_s": round(by / t / 1e9, 1),
+                     "frac_hbm": round(by / t / 1e9 / pk["hbm_gbs"], 3),
+                     "TFLOP_s": round(fl / t / 1e12, 2),
+                     "frac_bf16_burst": round(fl / t / 1e12 / pk["bf16_tflops"], 3)})
+    return {"shapes": rows}
+
+
+def bench_moe(args, q, synth, to_dev, ring_of, time_graph, dev, pk):
+    import torch
+    E, top_k, N, K = 64, 8, 1408, 2048
+    w, stride = synth.q4_0_experts(4000, E, N, K)
+    ring = ring_of((to_dev(w),), w.nbytes)
+    rows = []
+    for n_tokens in (1, 512):
+        ids = synth.routing_ids(4100 + n_tokens, n_tokens, top_k, E)
+        x = to_dev(synth.activations_f32(4200 + n_tokens, n_tokens, K))
+        idd = to_dev(ids.view(np.int32))
+        out = torch.empty((n_tokens * top_k, N), dtype=torch.float32, device=dev)
+        ws = torch.empty(q.q4_0_matmul_id_workspace_size(n_tokens, top_k, N, K, E), dtype=torch.uint8,
+                         device=dev)
+        touched = len(np.unique(ids))
+        by = touched * N * (K // 32) * 18 + x.numel() * 4 + out.numel() * 4 + ids.nbytes
+        fl = 2.0 * n_tokens * top_k * N * K
+        for mode in ((1,) if n_tokens == 1 else (2,)):
+            L = 2 * len(ring)
+            t = time_graph(lambda _: [q.q4_0_matmul_id(x, ring[l % len(ring)][0], idd, out, top_k, N, K, E,
+                                                       stride, mode=mode, workspace=ws)
+                                      for l in range(L)], L, replays=5) / L
+            rows.append({"n_tokens": n_tokens, "mode": {1: "mv", 2: "mm"}[mode], "us": round(t * 1e6, 2),
+                         "GB_s": round(by / t / 1e9, 1), "frac_hbm": round(by / t / 1e9 / pk["hbm_gbs"], 3),
+                         "TFLOP_s": round(fl / t / 1e12, 2)})
+    return {"experts": E, "top_k": top_k, "N": N, "K": K, "shapes": rows}
+
+
+# ------------------------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline leg and the reference arm)
+# ------------------------------------------------------------------------------------------
+def _oracle_sample_rows(seconds: float):
+    """Rows of every decode shape to run so that one pass takes about `seconds`."""
+    import oracle
+    from weight_only_bit_int4_gb300 import synth
+    K, N = 4096, 64
+    w, s, b = synth.int4_weights(1000, N, K)
+    x = synth.activations_bf16(1100, 16, K)
+    t0 = time.perf_counter()
+    oracle.q4_matmul(x, w, s, b, 16, N, K)
+    per_mac = (time.perf_counter() - t0) / (16 * N * K)
+    macs_per_row = sum(M * K for (M, K, N) in decode_shapes())
+    return max(8, int(seconds / (per_mac * macs_per_row)))
+
+
+def oracle_pass(n_rows: int, cache: dict):
+    """One pass of the decode workload on the oracle, restricted to the first n_rows weight
+    rows of every shape.  Returns (seconds, algorithmic bytes of the sampled work)."""
+    import oracle
+    from weight_only_bit_int4_gb300 import synth
+    t = 0.0
+    by = 0
+    for j, (M, K, N) in enumerate(decode_shapes()):
+        key = (M, K, N)
+        if key not in cache:
+            i = DECODE_KN.index((K, N))
+            w, s, b = synth.int4_weights(1000 + i, N, K)
+            rows = min(n_rows, N)
+            cache[key] = (synth.activations_bf16(1100 + j, M, K), w[:rows].copy(), s[:rows].copy(),
+                          b[:rows].copy(), rows)
+        x, w, s, b, rows = cache[key]
+        t0 = time.perf_counter()
+        oracle.q4_matmul(x, w, s, b, M, rows, K)
+        t += time.perf_counter() - t0
+        by += int4_bytes(M, K, rows)
+    return t, by
+
+
+def cpu_baseline(seconds: float = 15.0):
+    n_rows = _oracle_sample_rows(seconds)
+    t, by = oracle_pass(n_rows, {})
+    return {"value": round(by / t / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"decode workload, first {n_rows} weight rows of each of the 9 shapes "
+                      f"(all M tokens, full K), one pass, {t:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    budget = 120.0
+    n_rows = _oracle_sample_rows(budget / max(1, args.steps + args.warmup))
+    cache = {}
+    for _ in range(args.warmup):
+        oracle_pass(n_rows, cache)
+    t_tot, by_tot = 0.0, 0
+    for _ in range(args.steps):
+        t, by = oracle_pass(n_rows, cache)
+        t_tot += t
+        by_tot += by
+    value = by_tot / t_tot / 1e9
+    sample = (f"decode workload, first {n_rows} weight rows of each of the 9 shapes per step "
+              f"(all M tokens, full K)")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t_tot / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "INT4 g32 affine decode GEMV, M in {1,4,16} x (K,N) in "
+                                   "{(4096,14336),(14336,4096),(4096,4096)} (bounded row sample)",
+                       "parallelism": "cpu oracle, 1 thread"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--quick", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    out = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

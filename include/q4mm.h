@@ -1,0 +1,174 @@
+/*
+ * q4mm.h -- C ABI of libq4mm: weight-only 4-bit quantized matrix multiplies
+ *           y = x . dequant(W)^T on one NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Pointers named as device data (x, w, scales, biases, y, out, ids, workspace, ...) are
+ *    device pointers in the current CUDA device's address space.  The only host pointers
+ *    are the LUT4 codebook (`book`, copied by value into the launch) and output arguments
+ *    named `out_*` of the query calls.
+ *  - Ownership: the caller owns every buffer, including workspaces.  No call allocates,
+ *    frees, or synchronises; every kernel is enqueued on `stream` in call order (a NULL
+ *    stream is the legacy default stream).  Calls on one stream see each other's results.
+ *  - Layouts are row-major and dense (no strides).  "bf16" arguments are uint16_t bit
+ *    patterns of bfloat16 values; "fp16" are IEEE binary16 bit patterns.
+ *  - Errors: arguments are checked on the host before anything is enqueued; a failed check
+ *    returns a status and launches nothing.  M == 0 (or n_tokens == 0) returns Q4MM_OK
+ *    with nothing enqueued.  After enqueueing, a launch failure reported by the CUDA runtime
+ *    is returned as Q4MM_ERR_CUDA.  No call falls back to another path or to the CPU.
+ *  - Device-side faults are never raised on purpose: bounded waits that give up, and
+ *    routed ids outside [0, n_experts), are recorded in a device error word readable
+ *    with q4mm_device_errors().
+ *
+ * Sources (page title, section) of the operations:
+ *   quant_fastkernel.rs  -- onnxruntime-ep-mlx 0.27.4, src/ops/quant_fastkernel.rs: the INT4
+ *                           group-32 affine MatMulNBits prefill kernel (module doc "Algorithm",
+ *                           kernel source, `eligible`, `try_apply`).
+ *   lut4.rs              -- onnxruntime-ep-mlx 0.31.1, src/ops/lut4.rs: `LookupMatMul`, the
+ *                           lookup4 kernel source, `execute` and the lookup4 decode kernel.
+ *   quantized_matmul_id_ggml.rs -- mlx-native 0.9.0: module doc (routed-matmul definition),
+ *                           `quantized_matmul_id_ggml`, `IdMmScratch`, `dispatch_id_mv`,
+ *                           `dispatch_id_mm_for_test` (map0 + mm_id stages).
+ */
+#ifndef Q4MM_H
+#define Q4MM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *q4mm_stream_t;
+
+typedef enum q4mm_status {
+    Q4MM_OK = 0,
+    Q4MM_ERR_INVALID_ARG = 1,  /* null pointer, bad size, size out of range            */
+    Q4MM_ERR_UNSUPPORTED = 2,  /* valid request this build does not serve (alignment)   */
+    Q4MM_ERR_WORKSPACE = 3,    /* workspace missing or smaller than the size query says */
+    Q4MM_ERR_CUDA = 4,         /* the CUDA runtime reported an error                     */
+    Q4MM_ERR_DEVICE = 5        /* current device is not compute capability 10.3         */
+} q4mm_status;
+
+typedef enum q4mm_dtype { Q4MM_F32 = 0, Q4MM_BF16 = 1, Q4MM_F16 = 2 } q4mm_dtype;
+
+/* Bits of the device error word. */
+#define Q4MM_DEVERR_WAIT_TIMEOUT 0x1u  /* a pipeline wait gave up; that output is invalid */
+#define Q4MM_DEVERR_BAD_EXPERT 0x2u    /* an id >= n_experts was routed (its row is zero) */
+
+/* Static string for a status code (never NULL). */
+const char *q4mm_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int q4mm_version(void);
+
+/* Reads the current device's error word into *out_flags (host pointer) and, if clear != 0,
+ * resets it.  Synchronises the device (diagnostics only, not for hot loops). */
+q4mm_status q4mm_device_errors(uint32_t *out_flags, int clear);
+
+/* ======================================================================================
+ * INT4 group-32 affine MatMulNBits  (quant_fastkernel.rs)
+ *   w       uint32 [N, K/8]: element k of row n is bits 4*(k%8)..4*(k%8)+3 of word
+ *           w[n][k/8] (low nibble first), an unsigned code q in 0..15.
+ *   scales  bf16 [N, K/32], biases bf16 [N, K/32]; bias = -zero_point * scale.
+ *   value   W[n][k] = fmaf(q, scales[n][k/32], biases[n][k/32])   (fp32, one rounding)
+ *   x       bf16 [M, K];   y bf16 [M, N],  y[m][n] = sum_k x[m][k] * W[n][k].
+ * Requirements: N >= 1, K >= 32, K % 32 == 0; w, scales, biases, x, y 16-byte aligned
+ * (Q4MM_ERR_UNSUPPORTED otherwise).  Float outputs are fp32-accumulated and rounded to
+ * bf16 (nearest even) once.
+ * ====================================================================================*/
+
+/* Standalone dequant (the decode-then-GEMM pattern of lut4.rs `decoded_gemm`, for the
+ * INT4 format).  out: [N, K] of out_dtype (Q4MM_F32 / Q4MM_BF16 / Q4MM_F16); F32 output is
+ * the fmaf value bit for bit, BF16/F16 are that value rounded to nearest even. */
+q4mm_status q4_dequant(const uint32_t *w, const uint16_t *scales, const uint16_t *biases,
+                       int64_t N, int64_t K, void *out, int out_dtype, q4mm_stream_t stream);
+
+/* Decode matmul, 1 <= M <= 16 (tokens).  Streams W once from HBM; split-K partial sums
+ * are combined inside a thread-block cluster in a fixed order (deterministic).  Needs no
+ * workspace. */
+q4mm_status q4_gemv(const uint16_t *x, const uint32_t *w, const uint16_t *scales,
+                    const uint16_t *biases, uint16_t *y, int64_t M, int64_t N, int64_t K,
+                    q4mm_stream_t stream);
+
+/* Prefill matmul (meant for M > 16; any M >= 1 is served).  Fifth-generation tensor
+ * cores: W tiles are dequantised to bf16 in shared memory, x tiles arrive by TMA,
+ * fp32 accumulators live in tensor memory. */
+q4mm_status q4_gemm(const uint16_t *x, const uint32_t *w, const uint16_t *scales,
+                    const uint16_t *biases, uint16_t *y, int64_t M, int64_t N, int64_t K,
+                    q4mm_stream_t stream);
+
+/* ======================================================================================
+ * LUT4: frozen 16-entry codebook, blocked 4-bit  (lut4.rs)
+ *   The stored matrix has `rows` x `cols` codes; flat index f = r*cols + c; byte f/2 of
+ *   `packed` holds code f: the HIGH nibble for even f, the LOW nibble for odd f.
+ *   scales  f32 [ceil(rows*cols / block)], one per `block` consecutive flat elements.
+ *   value   W = fl32(book[code] * scales[f / block])  (one fp32 product)
+ *   transpose = 1: stored [rows = N, cols = K], W[n][k] at f = n*K + k  (the [N, K/2] layout)
+ *   transpose = 0: stored [rows = K, cols = N], W[n][k] at f = k*N + n
+ *   book    HOST pointer to 16 floats, copied into the launch.
+ *   x bf16 [M, K]  ->  y bf16 [M, N], y[m][n] = sum_k x[m][k] * W[n][k].
+ * Requirements: M >= 0, N, K >= 1, block > 0 and even; packed holds ceil(rows*cols/2) bytes;
+ * x, y 2-byte aligned, scales 4-byte aligned.  The fast kernels serve transpose = 1 with K % 32 == 0,
+ * block % 32 == 0, K % block == 0 and 16-byte aligned x/packed; any other valid layout runs
+ * on a general (slower) kernel with the same results.
+ * ====================================================================================*/
+q4mm_status lut4_matmul(const uint16_t *x, const uint8_t *packed, const float *scales,
+                        const float *book, uint16_t *y, int64_t M, int64_t N, int64_t K,
+                        int64_t block, int transpose, q4mm_stream_t stream);
+
+/* Standalone LUT4 decode (lut4.rs lookup4 decode kernel): out [rows, cols] of out_dtype,
+ * out[f] = fl32(book[code(f)] * scales[f / block]) (F32 bit for bit; BF16/F16 rounded to
+ * nearest even). */
+q4mm_status lut4_dequant(const uint8_t *packed, const float *scales, const float *book,
+                         int64_t rows, int64_t cols, int64_t block, void *out, int out_dtype,
+                         q4mm_stream_t stream);
+
+/* ======================================================================================
+ * GGML Q4_0 expert-routed matmul  (quantized_matmul_id_ggml.rs)
+ *   x    f32 [n_tokens, K]; one row per token, shared by all of its top_k slots.
+ *   w    stacked experts: expert e starts at byte e*expert_stride; within it row n is
+ *        K/32 consecutive 18-byte blocks.  Block: fp16 d (little endian), then 16 bytes qs;
+ *        element j < 16 is (qs[j] & 15) - 8, element 16+j is (qs[j] >> 4) - 8;
+ *        value = (q - 8) * d.
+ *   ids  uint32 [n_tokens * top_k]; routed row r = token*top_k + slot uses expert ids[r].
+ *   out  f32 [n_tokens * top_k, N]; out[r][n] = sum_k x[r / top_k][k] * W[ids[r]][n][k].
+ *        A row whose id is >= n_experts is written as zeros and sets
+ *        Q4MM_DEVERR_BAD_EXPERT.
+ * ====================================================================================*/
+
+/* Per-expert routed lists (the map0 stage of dispatch_id_mm_for_test).
+ *   htpe  uint32 [n_experts]: htpe[e] = number of rows r < n_rows with ids[r] == e.
+ *   hids  int32 [n_rows]: expert 0's rows, then expert 1's, ..., each list ascending in r;
+ *         expert e's list starts at sum_{e'<e} htpe[e'].  Entries past the total are
+ *         left unchanged.
+ *   n_invalid  uint32 [1] (device, may be NULL): rows whose id is >= n_experts.
+ * Requirements: 1 <= n_rows <= 2^24, 1 <= n_experts <= 1024.  Deterministic. */
+q4mm_status q4_0_route(const uint32_t *ids, int64_t n_rows, int64_t n_experts, uint32_t *htpe,
+                       int32_t *hids, uint32_t *n_invalid, q4mm_stream_t stream);
+
+/* Bytes of workspace q4_0_matmul_id needs in mat-mat mode (0 in mat-vec mode). */
+size_t q4_0_matmul_id_workspace_size(int64_t n_tokens, int64_t top_k, int64_t N, int64_t K,
+                                     int64_t n_experts);
+
+/* Mode: 0 = automatic (mat-mat when n_tokens > Q4MM_MM_ID_THRESHOLD, else mat-vec),
+ *       1 = mat-vec (each routed row reads its expert's rows; no workspace),
+ *       2 = mat-mat (route, gather each expert's rows, stream each expert's weights once
+ *           per 128-row tile through the tensor cores; needs the workspace).
+ * Requirements: n_tokens, top_k, N, K, n_experts >= 1; K % 32 == 0; expert_stride >=
+ * N*(K/32)*18; x, out 16-byte aligned; workspace (mat-mat) 256-byte aligned and at least
+ * q4_0_matmul_id_workspace_size(...) bytes. */
+#define Q4MM_MM_ID_THRESHOLD 32
+q4mm_status q4_0_matmul_id(const float *x, const void *w, const uint32_t *ids, float *out,
+                           int64_t n_tokens, int64_t top_k, int64_t N, int64_t K,
+                           int64_t n_experts, uint64_t expert_stride, int mode,
+                           void *workspace, size_t workspace_bytes, q4mm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4MM_H */

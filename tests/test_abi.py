@@ -1,0 +1,80 @@
+"""CPU-side checks of the C ABI: the library loads, exports every function include/q4mm.h
+declares, and rejects bad arguments on the host before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from weight_only_bit_int4_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q4mm.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_0-9]+)\s*\([^;{]*\)\s*;", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    return _lib.lib()
+
+
+def test_header_declares_the_hot_path():
+    names = _declared_functions()
+    for n in ["q4_dequant", "q4_gemv", "q4_gemm", "lut4_matmul", "lut4_dequant", "q4_0_route",
+              "q4_0_matmul_id", "q4_0_matmul_id_workspace_size", "q4mm_status_string"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+    assert set(_declared_functions()) <= set(_lib.SIGNATURES)
+
+
+def test_status_strings(L):
+    assert L.q4mm_status_string(0) == b"ok"
+    assert L.q4mm_status_string(3).startswith(b"workspace")
+    assert L.q4mm_version() >= 100
+
+
+FAKE = 1 << 20   # an aligned non-null address; never dereferenced: the checks fail first
+
+
+def test_int4_argument_checks(L):
+    # null pointers, K not a multiple of 32, M out of range -> INVALID_ARG, nothing launched
+    assert L.q4_gemv(None, FAKE, FAKE, FAKE, FAKE, 1, 64, 64, None) == 1
+    assert L.q4_gemv(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 48, None) == 1
+    assert L.q4_gemv(FAKE, FAKE, FAKE, FAKE, FAKE, 17, 64, 64, None) == 1
+    assert L.q4_gemm(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 64, 64, None) == 1
+    assert L.q4_dequant(FAKE, FAKE, FAKE, 4, 64, FAKE, 7, None) == 1
+    # misaligned operand -> UNSUPPORTED
+    assert L.q4_gemv(FAKE + 2, FAKE, FAKE, FAKE, FAKE, 1, 64, 64, None) == 2
+    # zero tokens -> OK with nothing enqueued
+    assert L.q4_gemv(None, None, None, None, None, 0, 64, 64, None) == 0
+    assert L.q4_gemm(None, None, None, None, None, 0, 64, 64, None) == 0
+
+
+def test_lut4_argument_checks(L):
+    book = (ctypes.c_float * 16)()
+    assert L.lut4_matmul(FAKE, FAKE, FAKE, book, FAKE, 1, 4, 4, 3, 1, None) == 1      # odd block
+    assert L.lut4_matmul(FAKE, FAKE, FAKE, None, FAKE, 1, 4, 4, 4, 1, None) == 1      # no book
+    assert L.lut4_matmul(FAKE, FAKE, FAKE, book, FAKE, 1, 4, 4, 4, 2, None) == 1      # bad transpose flag
+
+
+def test_moe_argument_checks(L):
+    # expert_stride smaller than one expert -> INVALID_ARG
+    assert L.q4_0_matmul_id(FAKE, FAKE, FAKE, FAKE, 2, 8, 64, 64, 16, 64 * 2 * 18 - 1, 1, None, 0, None) == 1
+    # K not a multiple of 32
+    assert L.q4_0_matmul_id(FAKE, FAKE, FAKE, FAKE, 2, 8, 64, 48, 16, 1 << 20, 1, None, 0, None) == 1
+    # mat-mat mode without workspace -> WORKSPACE
+    assert L.q4_0_matmul_id(FAKE, FAKE, FAKE, FAKE, 64, 8, 64, 64, 16, 64 * 2 * 18, 2, None, 0, None) == 3
+    need = L.q4_0_matmul_id_workspace_size(64, 8, 64, 64, 16)
+    assert need > 0
+    assert L.q4_0_matmul_id(FAKE, FAKE, FAKE, FAKE, 64, 8, 64, 64, 16, 64 * 2 * 18, 2, FAKE, need - 1, None) == 3
+    # routing: too many experts
+    assert L.q4_0_route(FAKE, 8, 2000, FAKE, FAKE, None, None) == 1

@@ -1,0 +1,87 @@
+"""LUT4 (frozen codebook, blocked scales): CUDA path against the CPU oracle."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import weight_only_bit_int4_gb300 as q
+from weight_only_bit_int4_gb300 import synth
+
+from gpu_util import DEV, assert_within_tolerance, bf16_out, dev, poisoned_bf16
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _case(seed, M, N, K, block=64, transpose=1):
+    rows, cols = (N, K) if transpose else (K, N)
+    packed, scales, book = synth.lut4_weights(seed, rows, cols, block)
+    x = synth.activations_bf16(seed + 1, M, K)
+    return x, packed, scales, book
+
+
+@pytest.mark.parametrize("M,N,K,block", [(1, 256, 512, 64), (16, 200, 96, 32), (5, 130, 1024, 128),
+                                         (512, 256, 512, 64), (40, 300, 640, 64), (129, 128, 256, 64)])
+def test_lut4_fast_paths(M, N, K, block):
+    x, packed, scales, book = _case(60 + M, M, N, K, block)
+    ref = oracle.lut4_matmul(x, packed, scales, book, M, N, K, block, 1)
+    y = poisoned_bf16(M, N)
+    q.lut4_matmul(dev(x), dev(packed), dev(scales), book, y, N, K, block, 1)
+    assert_within_tolerance(bf16_out(y), ref, f"lut4 M={M} N={N} K={K} block={block}")
+
+
+@pytest.mark.parametrize("M,N,K,block,transpose", [(3, 5, 7, 4, 0), (20, 33, 70, 6, 1), (2, 64, 96, 10, 0),
+                                                   (17, 40, 50, 2, 1)])
+def test_lut4_general_layouts(M, N, K, block, transpose):
+    x, packed, scales, book = _case(70 + M, M, N, K, block, transpose)
+    ref = oracle.lut4_matmul(x, packed, scales, book, M, N, K, block, transpose)
+    y = poisoned_bf16(M, N)
+    q.lut4_matmul(dev(x), dev(packed), dev(scales), book, y, N, K, block, transpose)
+    assert_within_tolerance(bf16_out(y), ref, f"lut4 general transpose={transpose}")
+
+
+def test_lut4_worked_example_on_gpu():
+    book = np.array([i * i / 32.0 for i in range(16)], np.float32)
+    with open(os.path.join(GOLDEN, "lut4_worked_example.txt")) as f:
+        lines = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    for parts in lines:
+        byte, scale, transpose = int(parts[0], 16), float(parts[1]), int(parts[2])
+        expected = [float(v) for v in parts[3:]]
+        K, N = (5, 3) if transpose else (3, 5)
+        x = synth.to_bf16_bits(np.full((2, K), 0.25, np.float32))
+        y = poisoned_bf16(2, N)
+        q.lut4_matmul(dev(x), dev(np.full(32, byte, np.uint8)), dev(np.array([scale], np.float32)),
+                      book, y, N, K, 64, transpose)
+        got = bf16_out(y)
+        # the exact results are dyadic with few bits: bf16 holds them exactly
+        np.testing.assert_array_equal(got, np.array([expected, expected]))
+
+
+@pytest.mark.parametrize("rows,cols,block", [(64, 128, 64), (3, 5, 4), (33, 70, 6)])
+def test_lut4_dequant_bit_exact(rows, cols, block):
+    packed, scales, book = synth.lut4_weights(80, rows, cols, block)
+    ref = oracle.lut4_dequant(packed, scales, book, rows, cols, block)
+    for dt, conv in ((torch.float32, None), (torch.bfloat16, oracle.f32_to_bf16), (torch.float16, oracle.f32_to_f16)):
+        out = torch.empty((rows, cols), dtype=dt, device=DEV)
+        q.lut4_dequant(dev(packed), dev(scales), book, rows, cols, block, out)
+        if conv is None:
+            np.testing.assert_array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+        else:
+            np.testing.assert_array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), conv(ref))
+
+
+@pytest.mark.parametrize("M", [1, 512])
+def test_lut4_full_size_sampled(M):
+    N = K = 4096
+    x, packed, scales, book = _case(3000 + M, M, N, K)
+    y = poisoned_bf16(M, N)
+    q.lut4_matmul(dev(x), dev(packed), dev(scales), book, y, N, K, 64, 1)
+    got = bf16_out(y)
+    assert np.all(np.isfinite(got))
+    rng = np.random.default_rng(M)
+    mi = rng.integers(0, M, 600)
+    ni = rng.integers(0, N, 600)
+    ref = oracle.lut4_matmul_at(x, packed, scales, book, N, K, 64, 1, mi, ni)
+    assert_within_tolerance(got[mi, ni], ref, f"lut4 full M={M}")

@@ -1,0 +1,113 @@
+"""libq4mm: weight-only 4-bit quantized matmuls, y = x . dequant(W)^T, for one GB300.
+
+Every function here has the name of a C-ABI entry point in include/q4mm.h and does
+argument marshalling only (tensor -> device pointer, shape -> sizes, current CUDA stream);
+every step of the computation runs in the library's own CUDA kernels.  A non-OK status
+raises Q4MMError.  There is no CPU path.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._lib import lib
+
+Q4MM_OK = 0
+Q4MM_F32, Q4MM_BF16, Q4MM_F16 = 0, 1, 2
+MM_ID_THRESHOLD = 32
+_DTYPES = {torch.float32: Q4MM_F32, torch.bfloat16: Q4MM_BF16, torch.float16: Q4MM_F16}
+
+
+class Q4MMError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {lib().q4mm_status_string(status).decode()} (status {status})")
+
+
+def _check(fn: str, status: int) -> None:
+    if status != Q4MM_OK:
+        raise Q4MMError(fn, status)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def version() -> int:
+    return lib().q4mm_version()
+
+
+def device_errors(clear: bool = True) -> int:
+    v = ctypes.c_uint32(0)
+    _check("q4mm_device_errors", lib().q4mm_device_errors(ctypes.byref(v), int(clear)))
+    return v.value
+
+
+def q4_dequant(w, scales, biases, out, stream=None) -> None:
+    """out[N, K] (float32/bfloat16/float16) = fmaf(code, scale, bias), codes low nibble first."""
+    N, K = w.shape[0], w.shape[1] * 8
+    _check("q4_dequant", lib().q4_dequant(_ptr(w), _ptr(scales), _ptr(biases), N, K, _ptr(out),
+                                          _DTYPES[out.dtype], _stream(stream)))
+
+
+def q4_gemv(x, w, scales, biases, y, stream=None) -> None:
+    """y[M, N] = x[M, K] . W^T for 1 <= M <= 16 (bf16 in/out)."""
+    M, K = x.shape
+    N = w.shape[0]
+    _check("q4_gemv", lib().q4_gemv(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(y), M, N, K,
+                                    _stream(stream)))
+
+
+def q4_gemm(x, w, scales, biases, y, stream=None) -> None:
+    """y[M, N] = x[M, K] . W^T on the tensor cores (bf16 in/out)."""
+    M, K = x.shape
+    N = w.shape[0]
+    _check("q4_gemm", lib().q4_gemm(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(y), M, N, K,
+                                    _stream(stream)))
+
+
+def _book_ptr(book):
+    arr = (ctypes.c_float * 16)(*[float(v) for v in book])
+    return arr, ctypes.cast(arr, ctypes.c_void_p)
+
+
+def lut4_matmul(x, packed, scales, book, y, N: int, K: int, block: int, transpose: int,
+                stream=None) -> None:
+    """y[M, N] = x[M, K] . W^T with W[n][k] = fl32(book[code] * scale) (see q4mm.h)."""
+    M = x.shape[0]
+    keep, bp = _book_ptr(book)
+    _check("lut4_matmul", lib().lut4_matmul(_ptr(x), _ptr(packed), _ptr(scales), bp, _ptr(y), M, N,
+                                            K, block, int(transpose), _stream(stream)))
+    del keep
+
+
+def lut4_dequant(packed, scales, book, rows: int, cols: int, block: int, out, stream=None) -> None:
+    keep, bp = _book_ptr(book)
+    _check("lut4_dequant", lib().lut4_dequant(_ptr(packed), _ptr(scales), bp, rows, cols, block,
+                                              _ptr(out), _DTYPES[out.dtype], _stream(stream)))
+    del keep
+
+
+def q4_0_route(ids, n_experts: int, htpe, hids, n_invalid=None, stream=None) -> None:
+    _check("q4_0_route", lib().q4_0_route(_ptr(ids), ids.numel(), n_experts, _ptr(htpe), _ptr(hids),
+                                          _ptr(n_invalid), _stream(stream)))
+
+
+def q4_0_matmul_id_workspace_size(n_tokens: int, top_k: int, N: int, K: int, n_experts: int) -> int:
+    return int(lib().q4_0_matmul_id_workspace_size(n_tokens, top_k, N, K, n_experts))
+
+
+def q4_0_matmul_id(x, w, ids, out, top_k: int, N: int, K: int, n_experts: int,
+                   expert_stride: int, mode: int = 0, workspace=None, stream=None) -> None:
+    """out[n_tokens*top_k, N] f32: row r = x[r // top_k] . dequant_q4_0(W[ids[r]])^T."""
+    n_tokens = x.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("q4_0_matmul_id", lib().q4_0_matmul_id(
+        _ptr(x), _ptr(w), _ptr(ids), _ptr(out), n_tokens, top_k, N, K, n_experts, expert_stride,
+        mode, _ptr(workspace), ws_bytes, _stream(stream)))

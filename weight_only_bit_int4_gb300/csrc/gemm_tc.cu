@@ -1,0 +1,336 @@
+// gemm_tc.cu -- prefill matmul (M > 16) on the fifth-generation tensor cores:
+// q4_gemm (INT4 group-32 affine) and the fused LUT4 path of lut4_matmul.
+//
+// What it computes: y[m][n] = sum_k x[m][k] * W[n][k], W dequantised as in
+// quant_fastkernel.rs (nibble*scale + bias, low nibble first; module doc "Algorithm":
+// per K chunk, dequantise the W tile into shared memory, then tensor-core MMA with fp32
+// accumulation, then store bf16) or as in lut4.rs (fl32(book[code] * scale), high nibble
+// for even flat index).  The Metal design on those pages (BM=64/BN=32 threadgroup tiles,
+// simdgroup 8x8 MMA, a half-precision transposed W tile) is prior art only; this is the
+// GB300 design:
+//
+//  * Weights are the MMA's M side: a CTA owns 128 weight rows x 256 tokens.  The fp32
+//    accumulator tile (128 lanes x 256 columns) lives in tensor memory.
+//  * Warp 0, one lane: TMA loads x tiles [256 tokens x 64 k] (bf16, 128-byte swizzle).
+//  * Warps 2-5 (128 threads, one weight row each): load the raw codes for the next K
+//    block from global memory (two 16-byte loads per row per 64 k, prefetched two
+//    blocks ahead), dequantise them in registers (INT4: magic-number bf16 conversion +
+//    one bf16x2 FMA per pair, so each value is code*s+b rounded once; LUT4: codebook
+//    lookup in shared memory, one fp32 product, rounded to bf16), and write the bf16 row
+//    into the 128-byte-swizzled K-major tile the MMA reads.
+//  * Warp 1, one lane: issues tcgen05.mma (M=128, N=256, K=16) x4 per 64-wide K block and
+//    commits each stage back to the producers.
+//  * Epilogue (warps 2-5): tcgen05.ld 32 columns at a time, round to bf16, store y.
+//  * Four-stage mbarrier pipeline; every wait is bounded (a timeout sets the device error
+//    word and unwinds the CTA; tensor memory is always released).
+#include "tc_common.cuh"
+
+#include <cudaTypedefs.h>
+
+namespace q4mm {
+
+Q4MM_DEFINE_ERROR_READER(read_errors_gemm)
+
+namespace {
+
+constexpr int kTileW = 128;     // weight rows per CTA (MMA M)
+constexpr int kTileT = 256;     // tokens per CTA (MMA N)
+constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle row)
+constexpr int kStages = 4;
+constexpr int kThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 producers + epilogue
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kABytes = kTileW * kBK * 2;   // 16 KB
+constexpr uint32_t kBBytes = kTileT * kBK * 2;   // 32 KB
+
+struct TcGemmParams {
+  const uint8_t *w;        // row n at w + n*(K/2)
+  const void *scales;      // INT4: bf16 [N, K/32]; LUT4: f32 [N * K/block]
+  const uint16_t *biases;  // INT4 only
+  uint16_t *y;             // bf16 [M, N]
+  int M, N, K;
+  int lut_blocks_per_row;  // LUT4: K / block
+  int lut_kb_per_block;    // LUT4: block / 64
+  float book[16];
+};
+
+struct SmemLayout {
+  static constexpr uint32_t a = 0;
+  static constexpr uint32_t b = a + kStages * kABytes;
+  static constexpr uint32_t bars = b + kStages * kBBytes;          // full_a, full_b, empty, accum
+  static constexpr uint32_t misc = bars + (3 * kStages + 1) * 8;
+  static constexpr uint32_t book = misc + 16;
+  static constexpr uint32_t total = book + 16 * 4;
+};
+constexpr size_t kSmemBytes = SmemLayout::total + 1024;   // + alignment slack
+
+// Raw operand of one weight row for one 64-wide K block.
+struct RawKb {
+  uint4 q0, q1;      // 64 codes
+  uint32_t s, b;     // INT4: bf16 scale/bias of groups (2kb, 2kb+1) in low/high half; LUT4: f32 scale
+};
+
+template <bool LUT>
+__device__ __forceinline__ void load_kb(RawKb &r, const TcGemmParams &p, int row, int kb) {
+  r.q0 = make_uint4(0, 0, 0, 0);
+  r.q1 = make_uint4(0, 0, 0, 0);
+  r.s = 0;
+  r.b = 0;
+  if (row >= p.N) return;
+  const int k0 = kb * kBK;
+  const uint8_t *src = p.w + (size_t)row * (size_t)(p.K / 2) + (size_t)k0 / 2;
+  const bool second = k0 + 32 < p.K;
+  r.q0 = ldg_stream_v4(src);
+  if (second) r.q1 = ldg_stream_v4(src + 16);
+  if constexpr (LUT) {
+    const float *sc = static_cast<const float *>(p.scales);
+    r.s = __float_as_uint(__ldg(sc + (size_t)row * p.lut_blocks_per_row + kb / p.lut_kb_per_block));
+  } else {
+    const int G = p.K / 32;
+    const size_t gi = (size_t)row * G + 2 * kb;
+    const uint16_t *sc = static_cast<const uint16_t *>(p.scales);
+    uint32_t s0 = ldg_u16(sc + gi), b0 = ldg_u16(p.biases + gi), s1 = 0, b1 = 0;
+    if (second) {
+      s1 = ldg_u16(sc + gi + 1);
+      b1 = ldg_u16(p.biases + gi + 1);
+    }
+    r.s = s0 | (s1 << 16);
+    r.b = b0 | (b1 << 16);
+  }
+}
+
+// Eight consecutive k values (word c of the block) as four natural-order bf16 pairs.
+template <bool LUT>
+__device__ __forceinline__ uint4 decode_chunk(uint32_t word, int c, const RawKb &r, const float *book) {
+  if constexpr (LUT) {
+    const float s = __uint_as_float(r.s);
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t hi = (word >> (8 * j + 4)) & 0xFu;   // even k
+      const uint32_t lo = (word >> (8 * j)) & 0xFu;       // odd k
+      o[j] = pack_bf16x2(book[hi] * s, book[lo] * s);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  } else {
+    const uint32_t sh = c < 4 ? 0u : 16u;                 // words 0-3: group 2kb, 4-7: 2kb+1
+    const uint32_t sv = (r.s >> sh) & 0xFFFFu, bv = (r.b >> sh) & 0xFFFFu;
+    const Int4Pairs P = int4_word_to_bf16_pairs(word, sv | (sv << 16), bv | (bv << 16));
+    // P[i] = (k=i, k=i+4)  ->  (0,1) (2,3) (4,5) (6,7)
+    return make_uint4(prmt(P.p[0], P.p[1], 0x5410), prmt(P.p[2], P.p[3], 0x5410),
+                      prmt(P.p[0], P.p[1], 0x7632), prmt(P.p[2], P.p[3], 0x7632));
+  }
+}
+
+template <bool LUT>
+__global__ void __launch_bounds__(kThreads, 1)
+    qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ TcGemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - raw_base);
+
+  const uint32_t sA = base + SmemLayout::a;
+  const uint32_t sB = base + SmemLayout::b;
+  const uint32_t bar_full_a = base + SmemLayout::bars;
+  const uint32_t bar_full_b = bar_full_a + kStages * 8;
+  const uint32_t bar_empty = bar_full_b + kStages * 8;
+  const uint32_t bar_accum = bar_empty + kStages * 8;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SmemLayout::misc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SmemLayout::misc + 4);
+  float *book = reinterpret_cast<float *>(smem + SmemLayout::book);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int n0 = blockIdx.x * kTileW;
+  const int m0 = blockIdx.y * kTileT;
+  const int KB = (p.K + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(bar_full_a + 8 * s, 128);
+      tc::mbar_init(bar_full_b + 8 * s, 1);
+      tc::mbar_init(bar_empty + 8 * s, 1);
+    }
+    tc::mbar_init(bar_accum, 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+    tc::tma_prefetch_desc(&tmap_x);
+  }
+  if (LUT && threadIdx.x < 16) book[threadIdx.x] = p.book[threadIdx.x];
+  if (warp == 1) {
+    tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer: x tiles ----------------
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int s = kb % kStages;
+        const uint32_t ph = (kb / kStages) & 1;
+        if (!tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag)) break;
+        tc::mbar_arrive_expect_tx(bar_full_b + 8 * s, kBBytes);
+        tc::tma_load_2d(sB + s * kBBytes, &tmap_x, kb * kBK, m0, bar_full_b + 8 * s);
+        ++issued;
+      }
+      if (*abort_flag) {
+        // drain our own copies still in flight before the CTA can exit
+        for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb) {
+          const int s = kb % kStages;
+          const uint32_t ph = (kb / kStages) & 1;
+          volatile int dummy = 0;
+          tc::mbar_wait(bar_full_b + 8 * s, ph, &dummy);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kTileW, kTileT);
+      bool ok = true;
+      for (int kb = 0; kb < KB && ok; ++kb) {
+        const int s = kb % kStages;
+        const uint32_t ph = (kb / kStages) & 1;
+        ok = tc::mbar_wait(bar_full_a + 8 * s, ph, abort_flag) && tc::mbar_wait(bar_full_b + 8 * s, ph, abort_flag);
+        if (!ok) break;
+        tc::tc_fence_after();
+        const uint64_t ad = tc::smem_desc_sw128(sA + s * kABytes);
+        const uint64_t bd = tc::smem_desc_sw128(sB + s * kBBytes);
+#pragma unroll
+        for (int j = 0; j < kBK / 16; ++j)
+          tc::mma_bf16(tmem, ad + 2 * j, bd + 2 * j, idesc, (kb | j) != 0);
+        tc::mma_commit(bar_empty + 8 * s);
+      }
+      if (ok) tc::mma_commit(bar_accum);
+    }
+  } else {
+    // ---------------- dequant producers (one weight row per thread) ----------------
+    const int tp = threadIdx.x - 64;          // 0..127
+    const int row = n0 + tp;
+    RawKb r0, r1, r2;
+    load_kb<LUT>(r0, p, row, 0);
+    if (KB > 1) load_kb<LUT>(r1, p, row, 1);
+    bool ok = true;
+    for (int kb = 0; kb < KB; ++kb) {
+      if (kb + 2 < KB) load_kb<LUT>(r2, p, row, kb + 2);
+      const int s = kb % kStages;
+      const uint32_t ph = (kb / kStages) & 1;
+      if (!tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag)) { ok = false; break; }
+      uint8_t *a_tile = smem + SmemLayout::a + s * kABytes;
+      const uint32_t words[8] = {r0.q0.x, r0.q0.y, r0.q0.z, r0.q0.w, r0.q1.x, r0.q1.y, r0.q1.z, r0.q1.w};
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4 *>(a_tile + tc::sw128_offset((uint32_t)tp, (uint32_t)c)) =
+            decode_chunk<LUT>(words[c], c, r0, book);
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(bar_full_a + 8 * s);
+      r0 = r1;
+      r1 = r2;
+    }
+    // ---------------- epilogue ----------------
+    if (ok && tc::mbar_wait(bar_accum, 0, abort_flag)) {
+      tc::tc_fence_after();
+      const int quarter = warp & 3;
+      const int n = n0 + quarter * 32 + lane;
+      for (int c0 = 0; c0 < kTileT; c0 += 32) {
+        if (m0 + c0 >= p.M) break;
+        uint32_t v[32];
+        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+        tc::tmem_ld_wait();
+        if (n < p.N) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int m = m0 + c0 + j;
+            if (m < p.M) {
+              __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(v[j]));
+              p.y[(size_t)m * p.N + n] = *reinterpret_cast<uint16_t *>(&h);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// x [rows, K] bf16 row-major, box [box_rows x 64], 128-byte swizzle, zero fill out of bounds.
+cudaError_t make_x_map(CUtensorMap *map, const void *x, int rows, int K, int box_rows) {
+  auto enc = get_encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <bool LUT>
+cudaError_t launch_tc(const TcGemmParams &p, const void *x, cudaStream_t s) {
+  CUtensorMap map;
+  cudaError_t e = make_x_map(&map, x, p.M, p.K, kTileT);
+  if (e != cudaSuccess) return e;
+  auto kern = qgemm_tc_kernel<LUT>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((p.N + kTileW - 1) / kTileW), (unsigned)((p.M + kTileT - 1) / kTileT), 1);
+  kern<<<grid, kThreads, kSmemBytes, s>>>(map, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_q4_gemm(const uint16_t *x, const uint32_t *w, const uint16_t *scales,
+                           const uint16_t *biases, uint16_t *y, int M, int N, int K,
+                           cudaStream_t s) {
+  TcGemmParams p{};
+  p.w = reinterpret_cast<const uint8_t *>(w);
+  p.scales = scales;
+  p.biases = biases;
+  p.y = y;
+  p.M = M; p.N = N; p.K = K;
+  return launch_tc<false>(p, x, s);
+}
+
+cudaError_t launch_lut4_gemm(const uint16_t *x, const uint8_t *packed, const float *scales,
+                             const float *book, uint16_t *y, int M, int N, int K, int block,
+                             cudaStream_t s) {
+  if (K % kBK != 0 || block % kBK != 0 || K % block != 0) return cudaErrorNotSupported;
+  TcGemmParams p{};
+  p.w = packed;
+  p.scales = scales;
+  p.biases = nullptr;
+  p.y = y;
+  p.M = M; p.N = N; p.K = K;
+  p.lut_blocks_per_row = K / block;
+  p.lut_kb_per_block = block / kBK;
+  for (int i = 0; i < 16; ++i) p.book[i] = book[i];
+  return launch_tc<true>(p, x, s);
+}
+
+}  // namespace q4mm

@@ -112,10 +112,9 @@ def lut4_book(seed: int) -> np.ndarray:
 
 
 def lut4_weights(seed: int, rows: int, cols: int, block: int = 64):
-    """(packed uint8 [rows*cols/2], scales f32 [ceil(rows*cols/block)], book f32[16])."""
+    """(packed uint8 [ceil(rows*cols/2)], scales f32 [ceil(rows*cols/block)], book f32[16])."""
     total = rows * cols
-    assert total % 2 == 0
-    packed = (u64(seed, 7, total // 2) >> np.uint64(56)).astype(np.uint8)
+    packed = (u64(seed, 7, (total + 1) // 2) >> np.uint64(56)).astype(np.uint8)
     nblk = -(-total // block)
     scales = (0.01 + 0.04 * uniform(seed, 8, nblk)).astype(np.float32)
     return packed, scales, lut4_book(seed)
