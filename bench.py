@@ -122,6 +122,24 @@ class ClockSampler:
 # ------------------------------------------------------------------------------------------
 # our arm
 # ------------------------------------------------------------------------------------------
+def under_profiler() -> bool:
+    """Nsight Compute injects itself into the target (it sets the NV_NSIGHT_INJECTION_*
+    variables); kernel nodes of CUDA graphs do not replay under it, so the same command
+    then issues every launch eagerly (timings taken that way are never bench values)."""
+    return any(k.startswith("NV_NSIGHT_INJECTION") for k in os.environ) or \
+        bool(os.environ.get("CUDA_INJECTION64_PATH"))
+
+
+class EagerGraph:
+    """Stand-in for torch.cuda.CUDAGraph that re-issues the captured calls on replay()."""
+
+    def __init__(self, fn):
+        self.fn = fn
+
+    def replay(self):
+        self.fn()
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -144,8 +162,19 @@ def run_ours(args, rank, world, local_rank):
         R = max(2, math.ceil(4 * l2 / nbytes))
         return [tensors] + [tuple(t.clone() for t in tensors) for _ in range(R - 1)]
 
+    eager = under_profiler()
+
     def time_graph(build_calls, launches_per_replay, replays, warmup=3):
         """Capture build_calls() into a graph; return (seconds per replay)."""
+        if eager:
+            replays, warmup = 1, 1
+            for _ in range(warmup):
+                build_calls(0)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            build_calls(0)
+            torch.cuda.synchronize()
+            return (time.perf_counter() - t0) / replays
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
@@ -183,18 +212,24 @@ def run_ours(args, rank, world, local_rank):
         q.q4_gemv(xs[shp], *rings[(K, N)][0], ys[shp])
     torch.cuda.synchronize()
 
-    cap = torch.cuda.Stream()
-    cap.wait_stream(torch.cuda.current_stream())
+    def step_calls(p):
+        for shp in decode_shapes():
+            M, K, N = shp
+            r = rings[(K, N)]
+            q.q4_gemv(xs[shp], *r[p % len(r)], ys[shp])
+
     graphs = []
-    with torch.cuda.stream(cap):
-        for p in range(P):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=cap):
-                for shp in decode_shapes():
-                    M, K, N = shp
-                    r = rings[(K, N)]
-                    q.q4_gemv(xs[shp], *r[p % len(r)], ys[shp])
-            graphs.append(g)
+    if eager:
+        graphs = [EagerGraph(lambda p=p: step_calls(p)) for p in range(P)]
+    else:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap):
+            for p in range(P):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap):
+                    step_calls(p)
+                graphs.append(g)
     torch.cuda.synchronize()
     launches_per_step = len(decode_shapes())
 
@@ -465,6 +500,68 @@ def run_reference(args, rank, world):
             "gpu_launches": 0}
 
 
+CASES = {
+    "gemv_m1": "q4_gemv M=1 K=4096 N=14336",
+    "gemv_m16": "q4_gemv M=16 K=14336 N=4096",
+    "gemm_m2048": "q4_gemm M=2048 K=4096 N=14336",
+    "lut4_m1": "lut4_matmul M=1 K=N=4096",
+    "lut4_m512": "lut4_matmul M=512 K=N=4096",
+    "moe_n1": "q4_0_matmul_id n_tokens=1 (mat-vec)",
+    "moe_n512": "q4_0_matmul_id n_tokens=512 (mat-mat)",
+}
+
+
+def run_case(name: str, launches: int = 3):
+    """One named small workload, `launches` eager calls: the unit that profiler captures use.
+    Prints a wall-clock figure for orientation only (never a bench value)."""
+    import torch
+
+    import weight_only_bit_int4_gb300 as q
+    from weight_only_bit_int4_gb300 import synth
+    dev = torch.device("cuda", 0)
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        view = {np.dtype(np.uint16): np.int16, np.dtype(np.uint32): np.int32}.get(a.dtype, a.dtype)
+        return torch.from_numpy(a.view(view)).to(dev)
+
+    if name.startswith("gemv") or name.startswith("gemm"):
+        M, K, N = {"gemv_m1": (1, 4096, 14336), "gemv_m16": (16, 14336, 4096),
+                   "gemm_m2048": (2048, 4096, 14336)}[name]
+        w, s, b = synth.int4_weights(1000, N, K)
+        x = to_dev(synth.activations_bf16(1100, M, K, outlier_frac=0.01 if M > 16 else 0.0))
+        W = (to_dev(w), to_dev(s), to_dev(b))
+        y = torch.empty((M, N), dtype=torch.int16, device=dev)
+        fn = (lambda: q.q4_gemv(x, *W, y)) if name.startswith("gemv") else (lambda: q.q4_gemm(x, *W, y))
+    elif name.startswith("lut4"):
+        M = 1 if name == "lut4_m1" else 512
+        N = K = 4096
+        packed, scales, book = synth.lut4_weights(3000, N, K, 64)
+        x = to_dev(synth.activations_bf16(3100 + M, M, K))
+        P, S = to_dev(packed), to_dev(scales)
+        y = torch.empty((M, N), dtype=torch.int16, device=dev)
+        fn = lambda: q.lut4_matmul(x, P, S, book, y, N, K, 64, 1)
+    else:
+        n_tokens = 1 if name == "moe_n1" else 512
+        E, top_k, N, K = 64, 8, 1408, 2048
+        w, stride = synth.q4_0_experts(4000, E, N, K)
+        ids = synth.routing_ids(4100 + n_tokens, n_tokens, top_k, E)
+        x = to_dev(synth.activations_f32(4200 + n_tokens, n_tokens, K))
+        Wd, idd = to_dev(w), to_dev(ids.view(np.int32))
+        out = torch.empty((n_tokens * top_k, N), dtype=torch.float32, device=dev)
+        ws = torch.empty(q.q4_0_matmul_id_workspace_size(n_tokens, top_k, N, K, E), dtype=torch.uint8,
+                         device=dev)
+        mode = 1 if n_tokens == 1 else 2
+        fn = lambda: q.q4_0_matmul_id(x, Wd, idd, out, top_k, N, K, E, stride, mode=mode, workspace=ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(launches):
+        fn()
+    torch.cuda.synchronize()
+    print(json.dumps({"case": name, "what": CASES[name], "launches": launches,
+                      "wall_ms_per_call_orientation_only": round((time.perf_counter() - t0) / launches * 1e3, 3)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -474,7 +571,11 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--case", choices=sorted(CASES), help="run one small named workload (profiling)")
     args = ap.parse_args()
+    if args.case:
+        run_case(args.case)
+        return
     args.warmup = max(3, args.warmup)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -51,19 +51,40 @@ struct Raw {
   uint32_t b;   // INT4: bf16x2 (b, b)
 };
 
+// Per-lane streaming cursor of one weight row: the lane reads group 4*chunk + t.
+struct RowCursor {
+  const uint8_t *w;       // codes of group t of chunk 0 of this row (nullptr: row >= N)
+  const uint16_t *s, *b;  // INT4 scale / bias of group t (LUT4: s unused)
+  const float *ls;        // LUT4 scale row
+};
+
 template <bool LUT>
-__device__ __forceinline__ void load_raw(Raw &r, const GemvParams &p, int row, int grp) {
-  const int G = p.K / 32;
-  if (row < p.N && grp < G) {
-    r.q = ldg_stream_v4(p.w + (size_t)row * (size_t)(p.K / 2) + (size_t)grp * 16);
+__device__ __forceinline__ RowCursor make_cursor(const GemvParams &p, int row, int t) {
+  RowCursor c{};
+  if (row < p.N) {
+    c.w = p.w + (size_t)row * (size_t)(p.K / 2) + (size_t)t * 16;
     if constexpr (LUT) {
-      const float *sc = static_cast<const float *>(p.scales);
-      r.s = __float_as_uint(__ldg(sc + (size_t)row * p.lut_blocks_per_row + grp / p.lut_block_shift_div));
+      c.ls = static_cast<const float *>(p.scales) + (size_t)row * p.lut_blocks_per_row;
+    } else {
+      const size_t gi = (size_t)row * (p.K / 32) + t;
+      c.s = static_cast<const uint16_t *>(p.scales) + gi;
+      c.b = p.biases + gi;
+    }
+  }
+  return c;
+}
+
+template <bool LUT>
+__device__ __forceinline__ void load_raw(Raw &r, const GemvParams &p, const RowCursor &cur, int chunk, int t) {
+  const int grp = chunk * 4 + t;
+  if (cur.w != nullptr && grp < p.K / 32) {
+    r.q = ldg_stream_v4(cur.w + (size_t)chunk * 64);
+    if constexpr (LUT) {
+      r.s = __float_as_uint(__ldg(cur.ls + grp / p.lut_block_shift_div));
       r.b = 0;
     } else {
-      const size_t gi = (size_t)row * G + grp;
-      const uint32_t s = ldg_u16(static_cast<const uint16_t *>(p.scales) + gi);
-      const uint32_t b = ldg_u16(p.biases + gi);
+      const uint32_t s = ldg_u16(cur.s + chunk * 4);
+      const uint32_t b = ldg_u16(cur.b + chunk * 4);
       r.s = s | (s << 16);
       r.b = b | (b << 16);
     }
@@ -102,17 +123,18 @@ __device__ __forceinline__ void decode_word(uint32_t word, const Raw &r, const f
 __device__ __forceinline__ int x_row_stride(int max_chunks) { return max_chunks * 256 + 64; }
 
 template <bool LUT>
-__device__ void stage_x(const GemvParams &p, uint8_t *xs, int tokens, int c_begin, int nch) {
+__device__ void stage_x(const GemvParams &p, uint8_t *xs, int c_begin, int nch,
+                        uint16_t *xsum = nullptr) {
   const int TS = x_row_stride(p.max_chunks_per_cta);
   const int G = p.K / 32;
-  const int items = tokens * nch * 4;
+  const int items = p.M * nch * 4;   // tokens >= M are never read (their B fragments are zero)
   for (int it = threadIdx.x; it < items; it += kThreads) {
     const int tok = it / (nch * 4);
     const int gl = it % (nch * 4);          // group within this CTA's slice
     const int c = gl / 4, t = gl % 4;
     const int grp = (c_begin + c) * 4 + t;  // group within the row
     uint32_t X[16];
-    if (tok < p.M && grp < G) {
+    if (grp < G) {
       const uint4 *src = reinterpret_cast<const uint4 *>(p.x + (size_t)tok * p.K + (size_t)grp * 32);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -145,89 +167,25 @@ __device__ void stage_x(const GemvParams &p, uint8_t *xs, int tokens, int c_begi
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       *reinterpret_cast<uint4 *>(dst + j * 64) = make_uint4(e[4 * j], e[4 * j + 1], e[4 * j + 2], e[4 * j + 3]);
+    if (xsum != nullptr) {   // sum of the group's 32 x values (fp32, fixed order) as bf16
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        sum += __uint_as_float(X[i] << 16) + __uint_as_float(X[i] & 0xFFFF0000u);
+      __nv_bfloat16 hb = __float2bfloat16_rn(sum);
+      xsum[tok * (p.max_chunks_per_cta * 4) + gl] = *reinterpret_cast<uint16_t *>(&hb);
+    }
   }
 }
 
-template <int MT, int RT, bool LUT>
-__global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ GemvParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
+// Partial tile -> shared memory (token-major red[tok][row]) -> sum over the cluster's
+// K splits in rank order through distributed shared memory -> bf16 y.
+template <int MT, int RT>
+__device__ __forceinline__ void cluster_reduce_store(const GemvParams &p, float *red,
+                                                     const float (&acc)[RT][MT][4], int warp,
+                                                     int g, int t) {
   constexpr int kRowsCta = kWarps * 16 * RT;
-  constexpr int kTok = 8 * MT;
-  const int TS = x_row_stride(p.max_chunks_per_cta);
-  uint8_t *xs = smem;
-  float *red = reinterpret_cast<float *>(smem + (size_t)kTok * TS);   // [kTok][kRowsCta]
-  float *book = red + kTok * kRowsCta;                                  // [16]
-
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int g = lane / 4, t = lane % 4;
   const int S = gridDim.y;
-  const int split = blockIdx.y;
-  const int c_begin = (int)(((long long)split * p.chunks) / S);
-  const int c_end = (int)(((long long)(split + 1) * p.chunks) / S);
-  const int nch = c_end - c_begin;
-
-  if constexpr (LUT) {
-    if (threadIdx.x < 16) book[threadIdx.x] = p.book[threadIdx.x];
-  }
-  stage_x<LUT>(p, xs, kTok, c_begin, nch);
-  __syncthreads();
-
-  const int row0 = blockIdx.x * kRowsCta + warp * 16 * RT;
-  float acc[RT][MT][4];
-#pragma unroll
-  for (int rt = 0; rt < RT; ++rt)
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[rt][mt][i] = 0.f;
-
-  Raw cur[RT][2], nxt[RT][2];
-  if (nch > 0) {
-#pragma unroll
-    for (int rt = 0; rt < RT; ++rt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        load_raw<LUT>(cur[rt][h], p, row0 + rt * 16 + g + 8 * h, c_begin * 4 + t);
-  }
-  const uint8_t *xlane = xs + (size_t)g * TS + t * 16;
-
-  for (int c = 0; c < nch; ++c) {
-    if (c + 1 < nch) {
-#pragma unroll
-      for (int rt = 0; rt < RT; ++rt)
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          load_raw<LUT>(nxt[rt][h], p, row0 + rt * 16 + g + 8 * h, (c_begin + c + 1) * 4 + t);
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 xb[MT];
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-        xb[mt] = *reinterpret_cast<const uint4 *>(xlane + (size_t)(8 * mt) * TS + c * 256 + q * 64);
-#pragma unroll
-      for (int rt = 0; rt < RT; ++rt) {
-        const uint32_t w0 = q == 0 ? cur[rt][0].q.x : q == 1 ? cur[rt][0].q.y : q == 2 ? cur[rt][0].q.z : cur[rt][0].q.w;
-        const uint32_t w1 = q == 0 ? cur[rt][1].q.x : q == 1 ? cur[rt][1].q.y : q == 2 ? cur[rt][1].q.z : cur[rt][1].q.w;
-        uint32_t pg[4], pg8[4];
-        decode_word<LUT>(w0, cur[rt][0], book, pg);
-        decode_word<LUT>(w1, cur[rt][1], book, pg8);
-        const uint32_t a0[4] = {pg[0], pg8[0], pg[1], pg8[1]};
-        const uint32_t a1[4] = {pg[2], pg8[2], pg[3], pg8[3]};
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          mma_bf16_16816(acc[rt][mt], a0, xb[mt].x, xb[mt].y);
-          mma_bf16_16816(acc[rt][mt], a1, xb[mt].z, xb[mt].w);
-        }
-      }
-    }
-#pragma unroll
-    for (int rt = 0; rt < RT; ++rt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) cur[rt][h] = nxt[rt][h];
-  }
-
-  // Partial tile -> shared memory, token-major: red[tok][row].
 #pragma unroll
   for (int rt = 0; rt < RT; ++rt)
 #pragma unroll
@@ -272,6 +230,319 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
   cluster_sync_all();   // keep every CTA's shared memory alive until all ranks have read it
 }
 
+template <int MT, int RT, bool LUT>
+__global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ GemvParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int kRowsCta = kWarps * 16 * RT;
+  constexpr int kTok = 8 * MT;
+  const int TS = x_row_stride(p.max_chunks_per_cta);
+  uint8_t *xs = smem;
+  float *red = reinterpret_cast<float *>(smem + (size_t)kTok * TS);   // [kTok][kRowsCta]
+  float *book = red + kTok * kRowsCta;                                  // [16]
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int g = lane / 4, t = lane % 4;
+  const int S = gridDim.y;
+  const int split = blockIdx.y;
+  const int c_begin = (int)(((long long)split * p.chunks) / S);
+  const int c_end = (int)(((long long)(split + 1) * p.chunks) / S);
+  const int nch = c_end - c_begin;
+  const int row0 = blockIdx.x * kRowsCta + warp * 16 * RT;
+
+  // Start streaming weights first: three chunks in flight per row pair before x is staged.
+  RowCursor cur[RT][2];
+#pragma unroll
+  for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) cur[rt][h] = make_cursor<LUT>(p, row0 + rt * 16 + g + 8 * h, t);
+  Raw b0[RT][2], b1[RT][2], b2[RT][2];
+  auto load = [&](Raw (&b)[RT][2], int c) {
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) load_raw<LUT>(b[rt][h], p, cur[rt][h], c_begin + c, t);
+  };
+  if (nch > 0) load(b0, 0);
+  if (nch > 1) load(b1, 1);
+  if (nch > 2) load(b2, 2);
+
+  if constexpr (LUT) {
+    if (threadIdx.x < 16) book[threadIdx.x] = p.book[threadIdx.x];
+  }
+  stage_x<LUT>(p, xs, c_begin, nch);
+  __syncthreads();
+
+  float acc[RT][MT][4];
+#pragma unroll
+  for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[rt][mt][i] = 0.f;
+
+  const uint8_t *xlane = xs + (size_t)g * TS + t * 16;
+  bool tok_live[MT];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) tok_live[mt] = g + 8 * mt < p.M;
+
+  auto compute = [&](const Raw (&b)[RT][2], int c) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 xb[MT];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+        xb[mt] = tok_live[mt] ? *reinterpret_cast<const uint4 *>(xlane + (size_t)(8 * mt) * TS + c * 256 + q * 64)
+                              : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int rt = 0; rt < RT; ++rt) {
+        const uint32_t w0 = q == 0 ? b[rt][0].q.x : q == 1 ? b[rt][0].q.y : q == 2 ? b[rt][0].q.z : b[rt][0].q.w;
+        const uint32_t w1 = q == 0 ? b[rt][1].q.x : q == 1 ? b[rt][1].q.y : q == 2 ? b[rt][1].q.z : b[rt][1].q.w;
+        uint32_t pg[4], pg8[4];
+        decode_word<LUT>(w0, b[rt][0], book, pg);
+        decode_word<LUT>(w1, b[rt][1], book, pg8);
+        const uint32_t a0[4] = {pg[0], pg8[0], pg[1], pg8[1]};
+        const uint32_t a1[4] = {pg[2], pg8[2], pg[3], pg8[3]};
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          mma_bf16_16816(acc[rt][mt], a0, xb[mt].x, xb[mt].y);
+          mma_bf16_16816(acc[rt][mt], a1, xb[mt].z, xb[mt].w);
+        }
+      }
+    }
+  };
+
+  // Three statically rotated buffers: consume one, refill it three chunks ahead.
+  for (int c = 0; c < nch; c += 3) {
+    compute(b0, c);
+    if (c + 3 < nch) load(b0, c + 3);
+    if (c + 1 < nch) {
+      compute(b1, c + 1);
+      if (c + 4 < nch) load(b1, c + 4);
+    }
+    if (c + 2 < nch) {
+      compute(b2, c + 2);
+      if (c + 5 < nch) load(b2, c + 5);
+    }
+  }
+
+  cluster_reduce_store<MT, RT>(p, red, acc, warp, g, t);
+}
+
+// ---------------------------------------------------------------------------------------
+// Streaming variant for K % 128 == 0: each warp owns a private shared-memory ring of
+// kDepth chunk stages filled with cp.async (16-byte code vectors and 8-byte scale/bias
+// runs), so about kDepth chunks per warp are in flight without holding registers.
+// Stage layout (per warp): [row half h][lane][16 B codes] then [h][quad g][scales 8 B |
+// biases 8 B] (LUT4: [h][quad g][up to four f32 block scales]).
+// ---------------------------------------------------------------------------------------
+constexpr int kDepth = 8;
+constexpr int kStageBytes = 2 * 512 + 2 * 128;
+
+__device__ __forceinline__ void cp_async(uint32_t dst, const void *src, int bytes, uint32_t src_bytes) {
+  if (bytes == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+  else if (bytes == 8)
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// INT4 weights enter the MMA as fma(128 + q, s, c_hi) in bf16, where c = b - 128 s (exact
+// in fp32) splits as c_hi + c_lo, c_hi = bf16(c): the rounded value is that of q*s + b - c_lo,
+// a number of the weight's own size, so one rounding per weight as in the plain dequant.
+// The remainder sum_g c_lo[n][g] * sum_{k in g} x[m][k] is added by one extra MMA per chunk
+// whose k-slot 2t carries (c_lo of lane t's group, that group's x sum).
+template <int MT, int RT, bool LUT>
+__global__ void __launch_bounds__(kThreads) gemv_async_kernel(const __grid_constant__ GemvParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int kRowsCta = kWarps * 16 * RT;
+  constexpr int kTok = 8 * MT;
+  constexpr int kStage = RT * kStageBytes;
+  const int TS = x_row_stride(p.max_chunks_per_cta);
+  uint8_t *ring = smem;
+  uint8_t *xs = smem + kWarps * kDepth * kStage;
+  float *red = reinterpret_cast<float *>(xs + (size_t)p.M * TS);      // [kTok][kRowsCta]
+  float *book = red + kTok * kRowsCta;                                 // [16]
+  uint16_t *xsum = reinterpret_cast<uint16_t *>(book + 16);            // [M][4 * max_chunks]
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int g = lane / 4, t = lane % 4;
+  const int S = gridDim.y;
+  const int split = blockIdx.y;
+  const int c_begin = (int)(((long long)split * p.chunks) / S);
+  const int c_end = (int)(((long long)(split + 1) * p.chunks) / S);
+  const int nch = c_end - c_begin;
+  const int row0 = blockIdx.x * kRowsCta + warp * 16 * RT;
+  const int G = p.K / 32;
+
+  // Per-lane sources.  Rows past N copy nothing (src-size 0 zero-fills the slot).
+  const uint8_t *wsrc[RT][2];
+  bool live[RT][2];
+#pragma unroll
+  for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = row0 + rt * 16 + g + 8 * h;
+      live[rt][h] = row < p.N;
+      wsrc[rt][h] = p.w + (live[rt][h] ? (size_t)row * (size_t)(p.K / 2) : 0) + (size_t)c_begin * 64 + t * 16;
+    }
+  // Scale run copied by this lane: INT4 lanes t = 0..3 copy (s, h0) (b, h0) (s, h1) (b, h1),
+  // 4 consecutive bf16 each; LUT4 lanes t = 0, 1 copy the f32 block scales of h = t.
+  const int sh = LUT ? t : (t >> 1);
+  const int sk = LUT ? 0 : (t & 1);
+  const bool scopy = LUT ? (t < 2) : true;
+  const uint8_t *ssrc[RT];
+  bool slive[RT];
+  int sbytes = 8;
+#pragma unroll
+  for (int rt = 0; rt < RT; ++rt) {
+    const int srow = row0 + rt * 16 + g + 8 * (sh & 1);
+    slive[rt] = scopy && srow < p.N;
+    if constexpr (LUT) {
+      const int per_chunk = p.lut_block_shift_div <= 4 ? 4 / p.lut_block_shift_div : 1;
+      sbytes = 4 * per_chunk;
+      ssrc[rt] = reinterpret_cast<const uint8_t *>(static_cast<const float *>(p.scales) +
+                                                   (slive[rt] ? (size_t)srow * p.lut_blocks_per_row : 0));
+    } else {
+      const uint16_t *base = sk ? p.biases : static_cast<const uint16_t *>(p.scales);
+      ssrc[rt] = reinterpret_cast<const uint8_t *>(base + (slive[rt] ? (size_t)srow * G : 0) + (size_t)c_begin * 4);
+    }
+  }
+  const uint32_t ring_warp = smem_u32(ring) + (uint32_t)(warp * kDepth * kStage);
+  const uint32_t sdst_off = 1024u + (uint32_t)(sh * 128 + g * 16 + sk * 8);
+
+  auto issue = [&](int c) {
+    const uint32_t slot = ring_warp + (uint32_t)((c % kDepth) * kStage);
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt) {
+      const uint32_t sl = slot + rt * kStageBytes;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        cp_async(sl + h * 512 + lane * 16, wsrc[rt][h] + (size_t)c * 64, 16, live[rt][h] ? 16u : 0u);
+      if (scopy) {
+        const uint8_t *src;
+        if constexpr (LUT) {
+          src = ssrc[rt] + (size_t)(((c_begin + c) * 4) / p.lut_block_shift_div) * 4;
+        } else {
+          src = ssrc[rt] + (size_t)c * 8;
+        }
+        cp_async(sl + sdst_off, src, sbytes, slive[rt] ? (uint32_t)sbytes : 0u);
+      }
+    }
+  };
+
+#pragma unroll
+  for (int i = 0; i < kDepth - 1; ++i) {
+    if (i < nch) issue(i);
+    cp_async_commit();
+  }
+  if constexpr (LUT) {
+    if (threadIdx.x < 16) book[threadIdx.x] = p.book[threadIdx.x];
+  }
+  stage_x<LUT>(p, xs, c_begin, nch, LUT ? nullptr : xsum);
+  __syncthreads();
+
+  float acc[RT][MT][4];
+#pragma unroll
+  for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[rt][mt][i] = 0.f;
+  const uint8_t *xlane = xs + (size_t)g * TS + t * 16;
+  bool tok_live[MT];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) tok_live[mt] = g + 8 * mt < p.M;
+  const uint8_t *ring_ptr = ring + warp * kDepth * kStage;
+  const int xsum_stride = p.max_chunks_per_cta * 4;
+
+  for (int c = 0; c < nch; ++c) {
+    if (c + kDepth - 1 < nch) issue(c + kDepth - 1);
+    cp_async_commit();
+    cp_async_wait<kDepth - 1>();
+    __syncwarp();
+    const uint8_t *slot = ring_ptr + (c % kDepth) * kStage;
+    uint4 xb[4][MT];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+        xb[q][mt] = tok_live[mt] ? *reinterpret_cast<const uint4 *>(xlane + (size_t)(8 * mt) * TS + c * 256 + q * 64)
+                                 : make_uint4(0, 0, 0, 0);
+    uint32_t xs_b[MT];
+    if constexpr (!LUT) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+        xs_b[mt] = tok_live[mt] ? (uint32_t)xsum[(g + 8 * mt) * xsum_stride + c * 4 + t] : 0u;
+    }
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt) {
+      const uint8_t *sl = slot + rt * kStageBytes;
+      uint4 qv[2];
+      uint32_t s2[2], c2[2];
+      float clo[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        qv[h] = *reinterpret_cast<const uint4 *>(sl + h * 512 + lane * 16);
+        const uint8_t *sc = sl + 1024 + h * 128 + g * 16;
+        if constexpr (LUT) {
+          const int idx = p.lut_block_shift_div <= 4 ? t / p.lut_block_shift_div : 0;
+          s2[h] = *reinterpret_cast<const uint32_t *>(sc + 4 * idx);
+          c2[h] = 0;
+          clo[h] = 0.f;
+        } else {
+          const uint32_t sv = *reinterpret_cast<const uint16_t *>(sc + 2 * t);
+          const uint32_t bv = *reinterpret_cast<const uint16_t *>(sc + 8 + 2 * t);
+          const float cf = __fmaf_rn(-128.f, __uint_as_float(sv << 16), __uint_as_float(bv << 16));
+          const uint32_t chi = pack_bf16x2(cf, cf);
+          clo[h] = cf - __uint_as_float(chi << 16);
+          s2[h] = sv | (sv << 16);
+          c2[h] = chi;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t w0 = q == 0 ? qv[0].x : q == 1 ? qv[0].y : q == 2 ? qv[0].z : qv[0].w;
+        const uint32_t w1 = q == 0 ? qv[1].x : q == 1 ? qv[1].y : q == 2 ? qv[1].z : qv[1].w;
+        uint32_t pg[4], pg8[4];
+        if constexpr (LUT) {
+          Raw r0{qv[0], s2[0], 0}, r1{qv[1], s2[1], 0};
+          decode_word<true>(w0, r0, book, pg);
+          decode_word<true>(w1, r1, book, pg8);
+        } else {
+          constexpr uint32_t kMask = 0x000F000Fu, kMagic = 0x43004300u;
+          const uint32_t ws0[4] = {w0, w0 >> 4, w0 >> 8, w0 >> 12};
+          const uint32_t ws1[4] = {w1, w1 >> 4, w1 >> 8, w1 >> 12};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            pg[j] = bf16x2_fma(and_or(ws0[j], kMask, kMagic), s2[0], c2[0]);
+            pg8[j] = bf16x2_fma(and_or(ws1[j], kMask, kMagic), s2[1], c2[1]);
+          }
+        }
+        const uint32_t a0[4] = {pg[0], pg8[0], pg[1], pg8[1]};
+        const uint32_t a1[4] = {pg[2], pg8[2], pg[3], pg8[3]};
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          mma_bf16_16816(acc[rt][mt], a0, xb[q][mt].x, xb[q][mt].y);
+          mma_bf16_16816(acc[rt][mt], a1, xb[q][mt].z, xb[q][mt].w);
+        }
+      }
+      if constexpr (!LUT) {
+        // k-slot 2t: row g -> c_lo(g), row g+8 -> c_lo(g+8); token column -> x sum of the group
+        const uint32_t ac[4] = {pack_bf16x2(clo[0], 0.f), pack_bf16x2(clo[1], 0.f), 0u, 0u};
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) mma_bf16_16816(acc[rt][mt], ac, xs_b[mt], 0u);
+      }
+    }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+  cluster_reduce_store<MT, RT>(p, red, acc, warp, g, t);
+}
+
 struct Plan {
   int MT, RT, S, max_chunks;
   size_t smem;
@@ -293,10 +564,11 @@ Plan make_plan(int M, int N, int K) {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
   }
   const size_t smem_cap = 227 * 1024;
-  // Prefer 32 rows per warp (x staged once per 128 rows); drop to 16 rows per warp when
-  // that leaves too few CTAs to keep every SM streaming.
+  // Pick (rows per warp, K splits) so that one wave of CTAs fills the SMs as evenly as
+  // possible, with the fewest splits (each split re-stages x and adds a cluster
+  // reduction) and at least ~12 chunk-rows in flight per SM.
   Plan best{};
-  double best_score = -1.0;
+  double best_score = -1e30;
   for (int RT = 2; RT >= 1; --RT) {
     const int rows_cta = kWarps * 16 * RT;
     const int rb = (N + rows_cta - 1) / rows_cta;
@@ -304,16 +576,16 @@ Plan make_plan(int M, int N, int K) {
       const int maxc = (chunks + S - 1) / S;
       const size_t sm = smem_bytes(pl.MT, RT, maxc);
       if (sm > smem_cap) continue;
-      int per_sm = (int)(smem_cap / (sm + 1024));
-      per_sm = std::max(1, std::min(per_sm, 16));
+      int per_sm = std::min((int)(smem_cap / (sm + 1024)), 8);
+      per_sm = std::max(per_sm, 1);
       const long long ctas = (long long)rb * S;
-      const long long slots = (long long)sms * per_sm;
-      const long long waves = (ctas + slots - 1) / slots;
-      // fraction of SM-time doing useful streaming, with a mild preference for fewer
-      // splits (each split re-stages x) and for 32-row warps
-      const double fill = (double)ctas / (double)(waves * slots);
-      const double busy = std::min(1.0, (double)ctas / (2.0 * sms));
-      const double score = busy * (0.5 + 0.5 * fill) - 0.01 * S + (RT == 2 ? 0.02 : 0.0);
+      const long long per_sm_needed = (ctas + sms - 1) / sms;          // CTAs on the busiest SM
+      const double balance = (double)ctas / (double)(per_sm_needed * sms);
+      const double waves = (double)per_sm_needed / per_sm;               // > 1: CTAs queue
+      const double warps_per_sm = (double)std::min<long long>(per_sm_needed, per_sm) * kWarps;
+      const double mlp = std::min(1.0, warps_per_sm * RT / 12.0);        // loads in flight
+      double score = balance * mlp - 0.015 * S - (waves > 1.0 ? 0.05 * (waves - 1.0) : 0.0);
+      if (maxc < 4) score -= 0.05 * (4 - maxc);                          // very short CTAs
       if (score > best_score) {
         best_score = score;
         best = Plan{pl.MT, RT, S, maxc, sm};
@@ -344,10 +616,84 @@ cudaError_t launch_typed(const GemvParams &p, const Plan &pl, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+size_t async_smem_bytes(int M, int MT, int RT, int max_chunks) {
+  return (size_t)kWarps * kDepth * kStageBytes * RT + (size_t)M * (max_chunks * 256 + 64) +
+         (size_t)8 * MT * kWarps * 16 * RT * 4 + 16 * 4 + (size_t)M * max_chunks * 4 * 2 + 16;
+}
+
+// All CTAs resident in one wave; among those plans, the best-balanced one with the most
+// rows per warp and the fewest K splits.
+Plan make_async_plan(int M, int N, int K) {
+  Plan pl{};
+  pl.MT = M <= 8 ? 1 : 2;
+  const int chunks = K / 128;
+  int sms = 152, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
+  }
+  double best = -1e30;
+  for (int RT = 2; RT >= 1; --RT) {
+    const int rb = (N + kWarps * 16 * RT - 1) / (kWarps * 16 * RT);
+    for (int S = 1; S <= std::min(kMaxCluster, chunks); ++S) {
+      const int maxc = (chunks + S - 1) / S;
+      const size_t sm = async_smem_bytes(M, pl.MT, RT, maxc);
+      if (sm > 227 * 1024) continue;
+      const int per_sm = std::max(1, std::min((int)((228 * 1024) / (sm + 1024)), 8));
+      const long long ctas = (long long)rb * S;
+      const long long need = (ctas + sms - 1) / sms;
+      if (need > per_sm) continue;                                       // one wave only
+      const double balance = (double)ctas / (double)(need * sms);
+      const double warps = (double)need * kWarps * RT;                    // row-tile streams per SM
+      double score = balance * std::min(1.0, warps / 12.0) - 0.02 * S + 0.01 * RT;
+      if (maxc < 4) score -= 0.05 * (4 - maxc);
+      if (score > best) {
+        best = score;
+        pl.RT = RT;
+        pl.S = S;
+        pl.max_chunks = maxc;
+        pl.smem = sm;
+      }
+    }
+  }
+  return pl;
+}
+
+template <int MT, int RT, bool LUT>
+cudaError_t launch_async_typed(const GemvParams &p, const Plan &pl, cudaStream_t s) {
+  auto kern = gemv_async_kernel<MT, RT, LUT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((p.N + kWarps * 16 * RT - 1) / (kWarps * 16 * RT)), (unsigned)pl.S, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = (unsigned)pl.S;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 template <bool LUT>
 cudaError_t launch_any(GemvParams &p, cudaStream_t s) {
-  const Plan pl = make_plan(p.M, p.N, p.K);
   p.chunks = (p.K / 32 + 3) / 4;
+  const bool lut_ok = !LUT || (p.lut_block_shift_div == 1 || p.lut_block_shift_div == 2 ||
+                               p.lut_block_shift_div % 4 == 0);
+  if (p.K % 128 == 0 && lut_ok) {
+    const Plan pa = make_async_plan(p.M, p.N, p.K);
+    if (pa.S > 0) {
+      p.max_chunks_per_cta = pa.max_chunks;
+      if (pa.MT == 1)
+        return pa.RT == 2 ? launch_async_typed<1, 2, LUT>(p, pa, s) : launch_async_typed<1, 1, LUT>(p, pa, s);
+      return pa.RT == 2 ? launch_async_typed<2, 2, LUT>(p, pa, s) : launch_async_typed<2, 1, LUT>(p, pa, s);
+    }
+  }
+  const Plan pl = make_plan(p.M, p.N, p.K);
   p.max_chunks_per_cta = pl.max_chunks;
   if (pl.MT == 1) {
     return pl.RT == 2 ? launch_typed<1, 2, LUT>(p, pl, s) : launch_typed<1, 1, LUT>(p, pl, s);
