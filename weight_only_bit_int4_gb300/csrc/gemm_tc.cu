@@ -9,20 +9,23 @@
 // simdgroup 8x8 MMA, a half-precision transposed W tile) is prior art only; this is the
 // GB300 design:
 //
-//  * Weights are the MMA's M side: a CTA owns 128 weight rows x 256 tokens.  The fp32
-//    accumulator tile (128 lanes x 256 columns) lives in tensor memory.
+//  * Weights are the MMA's M side: a tile is 128 weight rows x 256 tokens, its fp32
+//    accumulator (128 lanes x 256 columns) lives in tensor memory.  Two accumulators (all
+//    512 columns) let the epilogue of one tile overlap the main loop of the next.
+//  * Persistent CTAs, one per SM (the 4-stage ring takes ~197 KB of shared memory).
 //  * Warp 0, one lane: TMA loads x tiles [256 tokens x 64 k] (bf16, 128-byte swizzle).
-//  * Warps 2-5 (128 threads, one weight row each): load the raw codes for the next K
-//    block from global memory (two 16-byte loads per row per 64 k, prefetched two
-//    blocks ahead), dequantise them in registers (INT4: magic-number bf16 conversion +
-//    one bf16x2 FMA per pair, so each value is code*s+b rounded once; LUT4: codebook
-//    lookup in shared memory, one fp32 product, rounded to bf16), and write the bf16 row
-//    into the 128-byte-swizzled K-major tile the MMA reads.
-//  * Warp 1, one lane: issues tcgen05.mma (M=128, N=256, K=16) x4 per 64-wide K block and
-//    commits each stage back to the producers.
-//  * Epilogue (warps 2-5): tcgen05.ld 32 columns at a time, round to bf16, store y.
-//  * Four-stage mbarrier pipeline; every wait is bounded (a timeout sets the device error
-//    word and unwinds the CTA; tensor memory is always released).
+//  * Warps 2-5 (128 threads, one weight row each): load the raw codes of a 64-wide K block
+//    (two 16-byte loads per row, prefetched three blocks ahead, across tile boundaries),
+//    dequantise in registers (INT4: magic-number bf16 conversion + one bf16x2 FMA per
+//    pair, so each value is code*s+b rounded once; LUT4: codebook lookup in shared
+//    memory, one fp32 product, rounded to bf16), and write the bf16 row into the
+//    128-byte-swizzled K-major tile the MMA reads.
+//  * Warp 1, one lane: issues tcgen05.mma (M=128, N=256, K=16) x4 per K block and commits
+//    each stage back to the producers, and each finished accumulator to the epilogue.
+//  * Warps 6-9: tcgen05.ld 32 columns at a time, round to bf16, store y, release the
+//    accumulator.
+//  * Every mbarrier wait is bounded (a timeout sets the device error word and unwinds the
+//    CTA; tensor memory is always released).
 #include "tc_common.cuh"
 
 #include <cudaTypedefs.h>
@@ -37,8 +40,8 @@ constexpr int kTileW = 128;     // weight rows per CTA (MMA M)
 constexpr int kTileT = 256;     // tokens per CTA (MMA N)
 constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle row)
 constexpr int kStages = 4;
-constexpr int kThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 producers + epilogue
-constexpr uint32_t kTmemCols = 256;
+constexpr int kThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-5 producers, warps 6-9 epilogue
+constexpr uint32_t kTmemCols = 512;   // two 256-column fp32 accumulators
 constexpr uint32_t kABytes = kTileW * kBK * 2;   // 16 KB
 constexpr uint32_t kBBytes = kTileT * kBK * 2;   // 32 KB
 
@@ -50,14 +53,15 @@ struct TcGemmParams {
   int M, N, K;
   int lut_blocks_per_row;  // LUT4: K / block
   int lut_kb_per_block;    // LUT4: block / 64
+  int lut_sc_box;          // LUT4 TMA path: f32 scales per 8 K blocks (8 for block 64, 4 for 128)
   float book[16];
 };
 
 struct SmemLayout {
   static constexpr uint32_t a = 0;
   static constexpr uint32_t b = a + kStages * kABytes;
-  static constexpr uint32_t bars = b + kStages * kBBytes;          // full_a, full_b, empty, accum
-  static constexpr uint32_t misc = bars + (3 * kStages + 1) * 8;
+  static constexpr uint32_t bars = b + kStages * kBBytes;  // full_a, full_b, empty, acc_full[2], acc_empty[2]
+  static constexpr uint32_t misc = bars + (3 * kStages + 4) * 8;
   static constexpr uint32_t book = misc + 16;
   static constexpr uint32_t total = book + 16 * 4;
 };
@@ -121,6 +125,9 @@ __device__ __forceinline__ uint4 decode_chunk(uint32_t word, int c, const RawKb 
   }
 }
 
+// Persistent: one CTA per SM walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...; tile t is
+// (weight-row tile t / m_tiles, token tile t % m_tiles), so neighbouring CTAs share W tiles
+// in L2.  Every role counts pipeline steps j = (tile index within the CTA) * KB + kb.
 template <bool LUT>
 __global__ void __launch_bounds__(kThreads, 1)
     qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ TcGemmParams p) {
@@ -134,15 +141,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_full_a = base + SmemLayout::bars;
   const uint32_t bar_full_b = bar_full_a + kStages * 8;
   const uint32_t bar_empty = bar_full_b + kStages * 8;
-  const uint32_t bar_accum = bar_empty + kStages * 8;
+  const uint32_t bar_acc_full = bar_empty + kStages * 8;    // [2]
+  const uint32_t bar_acc_empty = bar_acc_full + 2 * 8;      // [2]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SmemLayout::misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SmemLayout::misc + 4);
   float *book = reinterpret_cast<float *>(smem + SmemLayout::book);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int n0 = blockIdx.x * kTileW;
-  const int m0 = blockIdx.y * kTileT;
   const int KB = (p.K + kBK - 1) / kBK;
+  const int m_tiles = (p.M + kTileT - 1) / kTileT;
+  const int n_tiles = (p.N + kTileW - 1) / kTileW;
+  const int T = m_tiles * n_tiles;
+  const int my_tiles = (int)blockIdx.x < T ? (T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int steps = my_tiles * KB;
+  auto tile_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -150,7 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(bar_full_b + 8 * s, 1);
       tc::mbar_init(bar_empty + 8 * s, 1);
     }
-    tc::mbar_init(bar_accum, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(bar_acc_full + 8 * b, 1);
+      tc::mbar_init(bar_acc_empty + 8 * b, 4);
+    }
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::tma_prefetch_desc(&tmap_x);
@@ -169,9 +184,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- TMA producer: x tiles ----------------
     if (lane == 0) {
       int issued = 0;
-      for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % kStages;
-        const uint32_t ph = (kb / kStages) & 1;
+      for (int j = 0; j < steps; ++j) {
+        const int i = j / KB, kb = j - i * KB;
+        const int m0 = (tile_of(i) % m_tiles) * kTileT;
+        const int s = j % kStages;
+        const uint32_t ph = (j / kStages) & 1;
         if (!tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag)) break;
         tc::mbar_arrive_expect_tx(bar_full_b + 8 * s, kBBytes);
         tc::tma_load_2d(sB + s * kBBytes, &tmap_x, kb * kBK, m0, bar_full_b + 8 * s);
@@ -179,11 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (*abort_flag) {
         // drain our own copies still in flight before the CTA can exit
-        for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb) {
-          const int s = kb % kStages;
-          const uint32_t ph = (kb / kStages) & 1;
+        for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j) {
           volatile int dummy = 0;
-          tc::mbar_wait(bar_full_b + 8 * s, ph, &dummy);
+          tc::mbar_wait(bar_full_b + 8 * (j % kStages), (j / kStages) & 1, &dummy);
         }
       }
     }
@@ -192,66 +207,339 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(kTileW, kTileT);
       bool ok = true;
-      for (int kb = 0; kb < KB && ok; ++kb) {
-        const int s = kb % kStages;
-        const uint32_t ph = (kb / kStages) & 1;
-        ok = tc::mbar_wait(bar_full_a + 8 * s, ph, abort_flag) && tc::mbar_wait(bar_full_b + 8 * s, ph, abort_flag);
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        const int ab = i & 1;
+        ok = tc::mbar_wait(bar_acc_empty + 8 * ab, ((i >> 1) & 1) ^ 1, abort_flag);
         if (!ok) break;
         tc::tc_fence_after();
-        const uint64_t ad = tc::smem_desc_sw128(sA + s * kABytes);
-        const uint64_t bd = tc::smem_desc_sw128(sB + s * kBBytes);
+        const uint32_t dtm = tmem + (uint32_t)(ab * kTileT);
+        for (int kb = 0; kb < KB; ++kb) {
+          const int j = i * KB + kb;
+          const int s = j % kStages;
+          const uint32_t ph = (j / kStages) & 1;
+          ok = tc::mbar_wait(bar_full_a + 8 * s, ph, abort_flag) && tc::mbar_wait(bar_full_b + 8 * s, ph, abort_flag);
+          if (!ok) break;
+          tc::tc_fence_after();
+          const uint64_t ad = tc::smem_desc_sw128(sA + s * kABytes);
+          const uint64_t bd = tc::smem_desc_sw128(sB + s * kBBytes);
 #pragma unroll
-        for (int j = 0; j < kBK / 16; ++j)
-          tc::mma_bf16(tmem, ad + 2 * j, bd + 2 * j, idesc, (kb | j) != 0);
-        tc::mma_commit(bar_empty + 8 * s);
+          for (int k = 0; k < kBK / 16; ++k)
+            tc::mma_bf16(dtm, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+          tc::mma_commit(bar_empty + 8 * s);
+        }
+        if (ok) tc::mma_commit(bar_acc_full + 8 * ab);
       }
-      if (ok) tc::mma_commit(bar_accum);
     }
-  } else {
+  } else if (warp < 6) {
     // ---------------- dequant producers (one weight row per thread) ----------------
     const int tp = threadIdx.x - 64;          // 0..127
-    const int row = n0 + tp;
-    RawKb r0, r1, r2;
-    load_kb<LUT>(r0, p, row, 0);
-    if (KB > 1) load_kb<LUT>(r1, p, row, 1);
-    bool ok = true;
-    for (int kb = 0; kb < KB; ++kb) {
-      if (kb + 2 < KB) load_kb<LUT>(r2, p, row, kb + 2);
-      const int s = kb % kStages;
-      const uint32_t ph = (kb / kStages) & 1;
-      if (!tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag)) { ok = false; break; }
+    auto row_of = [&](int j) { return (tile_of(j / KB) / m_tiles) * kTileW + tp; };
+    // Four statically rotated buffers: a block's loads are issued three steps before it is
+    // decoded, and no register copy ever waits on a load still in flight.
+    RawKb b0, b1, b2, b3;
+    auto load = [&](RawKb &r, int j) { load_kb<LUT>(r, p, row_of(j), j % KB); };
+    auto step = [&](const RawKb &r, int j) -> bool {
+      const int s = j % kStages;
+      const uint32_t ph = (j / kStages) & 1;
+      if (!tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, 200)) return false;
       uint8_t *a_tile = smem + SmemLayout::a + s * kABytes;
-      const uint32_t words[8] = {r0.q0.x, r0.q0.y, r0.q0.z, r0.q0.w, r0.q1.x, r0.q1.y, r0.q1.z, r0.q1.w};
+      const uint32_t words[8] = {r.q0.x, r.q0.y, r.q0.z, r.q0.w, r.q1.x, r.q1.y, r.q1.z, r.q1.w};
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         *reinterpret_cast<uint4 *>(a_tile + tc::sw128_offset((uint32_t)tp, (uint32_t)c)) =
-            decode_chunk<LUT>(words[c], c, r0, book);
+            decode_chunk<LUT>(words[c], c, r, book);
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(bar_full_a + 8 * s);
-      r0 = r1;
-      r1 = r2;
+      return true;
+    };
+    if (steps > 0) load(b0, 0);
+    if (steps > 1) load(b1, 1);
+    if (steps > 2) load(b2, 2);
+    for (int j = 0; j < steps; j += 4) {
+      if (j + 3 < steps) load(b3, j + 3);
+      if (!step(b0, j)) break;
+      if (j + 1 >= steps) break;
+      if (j + 4 < steps) load(b0, j + 4);
+      if (!step(b1, j + 1)) break;
+      if (j + 2 >= steps) break;
+      if (j + 5 < steps) load(b1, j + 5);
+      if (!step(b2, j + 2)) break;
+      if (j + 3 >= steps) break;
+      if (j + 6 < steps) load(b2, j + 6);
+      if (!step(b3, j + 3)) break;
     }
-    // ---------------- epilogue ----------------
-    if (ok && tc::mbar_wait(bar_accum, 0, abort_flag)) {
+  } else {
+    // ---------------- epilogue: TMEM -> bf16 y ----------------
+    const int quarter = warp & 3;
+    for (int i = 0; i < my_tiles; ++i) {
+      const int ab = i & 1;
+      if (!tc::mbar_wait(bar_acc_full + 8 * ab, (i >> 1) & 1, abort_flag)) break;
       tc::tc_fence_after();
-      const int quarter = warp & 3;
-      const int n = n0 + quarter * 32 + lane;
+      const int t = tile_of(i);
+      const int m0 = (t % m_tiles) * kTileT;
+      const int n = (t / m_tiles) * kTileW + quarter * 32 + lane;
       for (int c0 = 0; c0 < kTileT; c0 += 32) {
         if (m0 + c0 >= p.M) break;
         uint32_t v[32];
-        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * kTileT + c0), v);
         tc::tmem_ld_wait();
         if (n < p.N) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int m = m0 + c0 + j;
+          for (int jj = 0; jj < 32; ++jj) {
+            const int m = m0 + c0 + jj;
             if (m < p.M) {
-              __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(v[j]));
+              __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(v[jj]));
               p.y[(size_t)m * p.N + n] = *reinterpret_cast<uint16_t *>(&h);
             }
           }
         }
       }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(bar_acc_empty + 8 * ab);
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// TMA-fed variant (K % 256 == 0; LUT4 block 64 or 128): the producers issue no global loads.
+// Per K block the TMA warp brings the x tile (32 KB, swizzled) and the raw code tile
+// [128 rows x 32 B] (4 KB); every 8 K blocks it brings the scale (and bias) tile
+// [128 rows x 32 B] into a two-slot ring.  Producers read codes and scales from shared
+// memory, so the L1 data pipe only sees their 16-byte swizzled stores.
+// ---------------------------------------------------------------------------------------
+constexpr uint32_t kRawBytes = kTileW * 32;          // 4 KB of codes per K block
+constexpr uint32_t kScBytes = kTileW * 32;           // 4 KB of scales (or biases) per 8 K blocks
+constexpr int kScKb = 8;                             // K blocks per scale tile
+
+struct SmemLayoutT {
+  static constexpr uint32_t a = 0;
+  static constexpr uint32_t b = a + kStages * kABytes;
+  static constexpr uint32_t raw = b + kStages * kBBytes;
+  static constexpr uint32_t sc = raw + kStages * kRawBytes;      // [2] scales
+  static constexpr uint32_t bi = sc + 2 * kScBytes;              // [2] biases
+  // full_a, full_b, full_w, empty, acc_full[2], acc_empty[2], sc_full[2], sc_empty[2]
+  static constexpr uint32_t bars = bi + 2 * kScBytes;
+  static constexpr uint32_t misc = bars + (4 * kStages + 8) * 8;
+  static constexpr uint32_t book = misc + 16;
+  static constexpr uint32_t total = book + 16 * 4;
+};
+constexpr size_t kSmemBytesT = SmemLayoutT::total + 1024;
+
+struct TmaMaps {
+  CUtensorMap x, w, s, b;
+};
+
+template <bool LUT>
+__global__ void __launch_bounds__(kThreads, 1)
+    qgemm_tma_kernel(const __grid_constant__ TmaMaps maps, const __grid_constant__ TcGemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - raw_base);
+
+  const uint32_t sA = base + SmemLayoutT::a;
+  const uint32_t sB = base + SmemLayoutT::b;
+  const uint32_t sR = base + SmemLayoutT::raw;
+  const uint32_t sS = base + SmemLayoutT::sc;
+  const uint32_t sBi = base + SmemLayoutT::bi;
+  const uint32_t bar_full_a = base + SmemLayoutT::bars;
+  const uint32_t bar_full_b = bar_full_a + kStages * 8;
+  const uint32_t bar_full_w = bar_full_b + kStages * 8;
+  const uint32_t bar_empty = bar_full_w + kStages * 8;
+  const uint32_t bar_acc_full = bar_empty + kStages * 8;   // [2]
+  const uint32_t bar_acc_empty = bar_acc_full + 2 * 8;     // [2]
+  const uint32_t bar_sc_full = bar_acc_empty + 2 * 8;      // [2]
+  const uint32_t bar_sc_empty = bar_sc_full + 2 * 8;       // [2]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SmemLayoutT::misc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SmemLayoutT::misc + 4);
+  float *book = reinterpret_cast<float *>(smem + SmemLayoutT::book);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int KB = p.K / kBK;
+  const int SCB = (KB + kScKb - 1) / kScKb;      // scale tiles per weight tile
+  const int m_tiles = (p.M + kTileT - 1) / kTileT;
+  const int n_tiles = (p.N + kTileW - 1) / kTileW;
+  const int T = m_tiles * n_tiles;
+  const int my_tiles = (int)blockIdx.x < T ? (T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int steps = my_tiles * KB;
+  auto tile_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
+  const uint32_t sc_tx = LUT ? (uint32_t)(kTileW * p.lut_sc_box * 4) : 2u * kScBytes;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(bar_full_a + 8 * s, 128);
+      tc::mbar_init(bar_full_b + 8 * s, 1);
+      tc::mbar_init(bar_full_w + 8 * s, 1);
+      tc::mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(bar_acc_full + 8 * b, 1);
+      tc::mbar_init(bar_acc_empty + 8 * b, 4);
+      tc::mbar_init(bar_sc_full + 8 * b, 1);
+      tc::mbar_init(bar_sc_empty + 8 * b, 128);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+    tc::tma_prefetch_desc(&maps.x);
+    tc::tma_prefetch_desc(&maps.w);
+    tc::tma_prefetch_desc(&maps.s);
+    if (!LUT) tc::tma_prefetch_desc(&maps.b);
+  }
+  if (LUT && threadIdx.x < 16) book[threadIdx.x] = p.book[threadIdx.x];
+  if (warp == 1) {
+    tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA: x tiles, code tiles, scale tiles ----------------
+    if (lane == 0) {
+      int issued = 0, sc_issued = 0;
+      bool ok = true;
+      for (int j = 0; j < steps && ok; ++j) {
+        const int i = j / KB, kb = j - i * KB;
+        const int t = tile_of(i);
+        const int m0 = (t % m_tiles) * kTileT;
+        const int n0 = (t / m_tiles) * kTileW;
+        if (kb % kScKb == 0) {
+          const int q = i * SCB + kb / kScKb;              // scale tile counter
+          const int slot = q & 1;
+          if (!tc::mbar_wait(bar_sc_empty + 8 * slot, ((q >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          tc::mbar_arrive_expect_tx(bar_sc_full + 8 * slot, sc_tx);
+          if (LUT) {
+            tc::tma_load_2d(sS + slot * kScBytes, &maps.s, (kb / kScKb) * p.lut_sc_box, n0, bar_sc_full + 8 * slot);
+          } else {
+            tc::tma_load_2d(sS + slot * kScBytes, &maps.s, (kb / kScKb) * 16, n0, bar_sc_full + 8 * slot);
+            tc::tma_load_2d(sBi + slot * kScBytes, &maps.b, (kb / kScKb) * 16, n0, bar_sc_full + 8 * slot);
+          }
+          ++sc_issued;
+        }
+        const int s = j % kStages;
+        const uint32_t ph = (j / kStages) & 1;
+        if (!tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag)) break;
+        tc::mbar_arrive_expect_tx(bar_full_w + 8 * s, kRawBytes);
+        tc::tma_load_2d(sR + s * kRawBytes, &maps.w, kb * 32, n0, bar_full_w + 8 * s);
+        tc::mbar_arrive_expect_tx(bar_full_b + 8 * s, kBBytes);
+        tc::tma_load_2d(sB + s * kBBytes, &maps.x, kb * kBK, m0, bar_full_b + 8 * s);
+        ++issued;
+      }
+      if (*abort_flag) {
+        // drain our own copies still in flight before the CTA can exit
+        for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j) {
+          volatile int dummy = 0;
+          tc::mbar_wait(bar_full_b + 8 * (j % kStages), (j / kStages) & 1, &dummy);
+          tc::mbar_wait(bar_full_w + 8 * (j % kStages), (j / kStages) & 1, &dummy);
+        }
+        for (int q = (sc_issued > 2 ? sc_issued - 2 : 0); q < sc_issued; ++q) {
+          volatile int dummy = 0;
+          tc::mbar_wait(bar_sc_full + 8 * (q & 1), (q >> 1) & 1, &dummy);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kTileW, kTileT);
+      bool ok = true;
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        const int ab = i & 1;
+        ok = tc::mbar_wait(bar_acc_empty + 8 * ab, ((i >> 1) & 1) ^ 1, abort_flag);
+        if (!ok) break;
+        tc::tc_fence_after();
+        const uint32_t dtm = tmem + (uint32_t)(ab * kTileT);
+        for (int kb = 0; kb < KB; ++kb) {
+          const int j = i * KB + kb;
+          const int s = j % kStages;
+          const uint32_t ph = (j / kStages) & 1;
+          ok = tc::mbar_wait(bar_full_a + 8 * s, ph, abort_flag, 100) &&
+               tc::mbar_wait(bar_full_b + 8 * s, ph, abort_flag, 100);
+          if (!ok) break;
+          tc::tc_fence_after();
+          const uint64_t ad = tc::smem_desc_sw128(sA + s * kABytes);
+          const uint64_t bd = tc::smem_desc_sw128(sB + s * kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            tc::mma_bf16(dtm, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+          tc::mma_commit(bar_empty + 8 * s);
+        }
+        if (ok) tc::mma_commit(bar_acc_full + 8 * ab);
+      }
+    }
+  } else if (warp < 6) {
+    // ---------------- dequant producers (one weight row per thread) ----------------
+    const int tp = threadIdx.x - 64;
+    const uint8_t *raw_row = smem + SmemLayoutT::raw + tp * 32;
+    const uint8_t *sc_row = smem + SmemLayoutT::sc + tp * 32;
+    const uint8_t *bi_row = smem + SmemLayoutT::bi + tp * 32;
+    for (int j = 0; j < steps; ++j) {
+      const int i = j / KB, kb = j - i * KB;
+      const int q = i * SCB + kb / kScKb, slot = q & 1;
+      if (kb % kScKb == 0 && !tc::mbar_wait(bar_sc_full + 8 * slot, (q >> 1) & 1, abort_flag, 100)) break;
+      const int s = j % kStages;
+      const uint32_t ph = (j / kStages) & 1;
+      if (!tc::mbar_wait(bar_full_w + 8 * s, ph, abort_flag, 100)) break;
+      RawKb r;
+      r.q0 = *reinterpret_cast<const uint4 *>(raw_row + s * kRawBytes);
+      r.q1 = *reinterpret_cast<const uint4 *>(raw_row + s * kRawBytes + 16);
+      const int kk = kb % kScKb;
+      if constexpr (LUT) {
+        r.s = *reinterpret_cast<const uint32_t *>(sc_row + slot * kScBytes + 4 * (kk / p.lut_kb_per_block));
+        r.b = 0;
+      } else {
+        r.s = *reinterpret_cast<const uint32_t *>(sc_row + slot * kScBytes + 4 * kk);
+        r.b = *reinterpret_cast<const uint32_t *>(bi_row + slot * kScBytes + 4 * kk);
+      }
+      uint8_t *a_tile = smem + SmemLayoutT::a + s * kABytes;
+      const uint32_t words[8] = {r.q0.x, r.q0.y, r.q0.z, r.q0.w, r.q1.x, r.q1.y, r.q1.z, r.q1.w};
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4 *>(a_tile + tc::sw128_offset((uint32_t)tp, (uint32_t)c)) =
+            decode_chunk<LUT>(words[c], c, r, book);
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(bar_full_a + 8 * s);
+      if (kk == kScKb - 1 || kb == KB - 1) tc::mbar_arrive(bar_sc_empty + 8 * slot);
+    }
+  } else {
+    // ---------------- epilogue: TMEM -> bf16 y ----------------
+    const int quarter = warp & 3;
+    for (int i = 0; i < my_tiles; ++i) {
+      const int ab = i & 1;
+      if (!tc::mbar_wait(bar_acc_full + 8 * ab, (i >> 1) & 1, abort_flag)) break;
+      tc::tc_fence_after();
+      const int t = tile_of(i);
+      const int m0 = (t % m_tiles) * kTileT;
+      const int n = (t / m_tiles) * kTileW + quarter * 32 + lane;
+      for (int c0 = 0; c0 < kTileT; c0 += 32) {
+        if (m0 + c0 >= p.M) break;
+        uint32_t v[32];
+        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * kTileT + c0), v);
+        tc::tmem_ld_wait();
+        if (n < p.N) {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int m = m0 + c0 + jj;
+            if (m < p.M) {
+              __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(v[jj]));
+              p.y[(size_t)m * p.N + n] = *reinterpret_cast<uint16_t *>(&h);
+            }
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(bar_acc_empty + 8 * ab);
     }
   }
 
@@ -290,16 +578,67 @@ cudaError_t make_x_map(CUtensorMap *map, const void *x, int rows, int K, int box
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Generic 2D tensor map, no swizzle, zero fill out of bounds.
+cudaError_t make_plain_map(CUtensorMap *map, const void *base, CUtensorMapDataType dt, int esize,
+                           long long inner, long long rows, int box_inner, int box_rows) {
+  auto enc = get_encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)inner * (cuuint64_t)esize};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+unsigned persistent_grid(const TcGemmParams &p) {
+  int sms = 148, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long tiles = (long long)((p.N + kTileW - 1) / kTileW) * ((p.M + kTileT - 1) / kTileT);
+  return (unsigned)(tiles < sms ? tiles : sms);
+}
+
 template <bool LUT>
 cudaError_t launch_tc(const TcGemmParams &p, const void *x, cudaStream_t s) {
+  const bool tma_path = p.K % 256 == 0 && (!LUT || p.lut_kb_per_block == 1 || p.lut_kb_per_block == 2);
+  if (tma_path) {
+    TmaMaps maps;
+    cudaError_t e = make_x_map(&maps.x, x, p.M, p.K, kTileT);
+    if (e == cudaSuccess)
+      e = make_plain_map(&maps.w, p.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.K / 2, p.N, 32, kTileW);
+    if (LUT) {
+      TcGemmParams q = p;
+      q.lut_sc_box = 8 / q.lut_kb_per_block;
+      if (e == cudaSuccess)
+        e = make_plain_map(&maps.s, p.scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.lut_blocks_per_row, p.N,
+                           q.lut_sc_box, kTileW);
+      maps.b = maps.s;
+      if (e != cudaSuccess) return e;
+      auto kern = qgemm_tma_kernel<true>;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesT);
+      if (e != cudaSuccess) return e;
+      kern<<<persistent_grid(q), kThreads, kSmemBytesT, s>>>(maps, q);
+      return cudaGetLastError();
+    }
+    if (e == cudaSuccess)
+      e = make_plain_map(&maps.s, p.scales, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.K / 32, p.N, 16, kTileW);
+    if (e == cudaSuccess)
+      e = make_plain_map(&maps.b, p.biases, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.K / 32, p.N, 16, kTileW);
+    if (e != cudaSuccess) return e;
+    auto kern = qgemm_tma_kernel<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesT);
+    if (e != cudaSuccess) return e;
+    kern<<<persistent_grid(p), kThreads, kSmemBytesT, s>>>(maps, p);
+    return cudaGetLastError();
+  }
   CUtensorMap map;
   cudaError_t e = make_x_map(&map, x, p.M, p.K, kTileT);
   if (e != cudaSuccess) return e;
   auto kern = qgemm_tc_kernel<LUT>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((p.N + kTileW - 1) / kTileW), (unsigned)((p.M + kTileT - 1) / kTileT), 1);
-  kern<<<grid, kThreads, kSmemBytes, s>>>(map, p);
+  kern<<<persistent_grid(p), kThreads, kSmemBytes, s>>>(map, p);
   return cudaGetLastError();
 }
 

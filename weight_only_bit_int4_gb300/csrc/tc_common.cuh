@@ -40,19 +40,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that lets the thread sleep in hardware for up to `hint_ns` while the phase is
+// incomplete, so idle roles do not take issue slots from the working warps.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t addr, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of parity `parity` to complete.  Gives up (returns false) after
 // kWaitLimitNs, or as soon as another role has given up (*abort != 0); the first thread to
 // time out records Q4MM_DEVERR_WAIT_TIMEOUT and sets *abort so the whole CTA unwinds.
-__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, volatile int *abort) {
+// The clock and the abort flag are looked at only every 16 polls.
+__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, volatile int *abort,
+                                          uint32_t hint_ns = 2000) {
   if (mbar_try_wait(addr, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
-  while (true) {
-    if (mbar_try_wait(addr, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      *abort = 1;
-      raise_device_error(Q4MM_DEVERR_WAIT_TIMEOUT);
-      return false;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_sleep(addr, parity, hint_ns)) return true;
+    if ((it & 15u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        raise_device_error(Q4MM_DEVERR_WAIT_TIMEOUT);
+        return false;
+      }
     }
   }
 }
