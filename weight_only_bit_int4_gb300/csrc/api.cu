@@ -62,6 +62,7 @@ q4mm_status q4mm_device_errors(uint32_t *out_flags, int clear) {
   unsigned int v = 0;
   if (read_errors_moe(&v, clear) != cudaSuccess) return Q4MM_ERR_CUDA;
   if (read_errors_gemm(&v, clear) != cudaSuccess) return Q4MM_ERR_CUDA;
+  if (read_errors_moe_tc(&v, clear) != cudaSuccess) return Q4MM_ERR_CUDA;
   *out_flags = v;
   return Q4MM_OK;
 }

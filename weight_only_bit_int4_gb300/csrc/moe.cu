@@ -15,32 +15,6 @@
 
 namespace q4mm {
 
-// ---------------------------------------------------------------------------------------
-// Workspace layout of the mat-mat path (all offsets 256-byte aligned):
-//   htpe    u32 [E]        per-expert routed counts
-//   offs    u32 [E + 1]    exclusive prefix of htpe (offs[E] = number of valid rows)
-//   hids    i32 [R]        routed rows grouped by expert, ascending within an expert
-//   invalid u32 [1]        rows whose id is >= E
-//   xs      bf16 [R, K]    x rows gathered in hids order (the mm operand)
-// ---------------------------------------------------------------------------------------
-struct MoeWorkspace {
-  size_t htpe, offs, hids, invalid, xs, total;
-};
-
-static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
-
-static MoeWorkspace moe_workspace_layout(int64_t n_rows, int64_t K, int64_t E) {
-  MoeWorkspace w{};
-  size_t o = 0;
-  w.htpe = o; o = align256(o + 4 * (size_t)E);
-  w.offs = o; o = align256(o + 4 * (size_t)(E + 1));
-  w.hids = o; o = align256(o + 4 * (size_t)n_rows);
-  w.invalid = o; o = align256(o + 4);
-  w.xs = o; o = align256(o + 2 * (size_t)n_rows * (size_t)K);
-  w.total = o;
-  return w;
-}
-
 size_t q4_0_mm_workspace_bytes(int64_t n_tokens, int64_t top_k, int64_t N, int64_t K,
                                int64_t n_experts) {
   (void)N;
@@ -63,7 +37,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const uint32_t *__
                                                               uint32_t *__restrict__ htpe,
                                                               uint32_t *__restrict__ offs,
                                                               int32_t *__restrict__ hids,
-                                                              uint32_t *__restrict__ n_invalid) {
+                                                              uint32_t *__restrict__ n_invalid,
+                                                              int4 *__restrict__ blk = nullptr,
+                                                              uint32_t *__restrict__ n_blk = nullptr) {
   extern __shared__ uint32_t sm[];
   uint32_t *cnt = sm;                       // [n_warps][E]
   uint32_t *pos = sm + n_warps * E;         // [n_warps][E]
@@ -115,6 +91,15 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const uint32_t *__
     if (offs) offs[E] = run;
     if (n_invalid) *n_invalid = bad_count;
     if (bad_count) raise_device_error(Q4MM_DEVERR_BAD_EXPERT);
+    if (blk) {   // token blocks of at most kMoeTokBlock rows, expert by expert
+      uint32_t nb = 0;
+      for (int e = 0; e < E; ++e) {
+        const uint32_t c = (e + 1 < E ? scan[e + 1] : run) - scan[e];
+        for (uint32_t b0 = 0; b0 < c; b0 += kMoeTokBlock)
+          blk[nb++] = make_int4(e, (int)(scan[e] + b0), (int)min((uint32_t)kMoeTokBlock, c - b0), 0);
+      }
+      *n_blk = nb;
+    }
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -285,12 +270,12 @@ size_t route_smem(int E, int n_warps) { return (size_t)(2 * n_warps * E + E + 1)
 
 cudaError_t launch_route_internal(const uint32_t *ids, int n_rows, int E, uint32_t *htpe,
                                   uint32_t *offs, int32_t *hids, uint32_t *n_invalid,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, int4 *blk = nullptr, uint32_t *n_blk = nullptr) {
   const int nw = route_warps(E);
   const size_t sm = route_smem(E, nw);
   cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  route_kernel<<<1, nw * 32, sm, s>>>(ids, n_rows, E, nw, htpe, offs, hids, n_invalid);
+  route_kernel<<<1, nw * 32, sm, s>>>(ids, n_rows, E, nw, htpe, offs, hids, n_invalid, blk, n_blk);
   return cudaGetLastError();
 }
 
@@ -328,10 +313,17 @@ cudaError_t launch_q4_0_mm(const float *x, const uint8_t *w, const uint32_t *ids
   uint32_t *offs = reinterpret_cast<uint32_t *>(ws + L.offs);
   int32_t *hids = reinterpret_cast<int32_t *>(ws + L.hids);
   uint32_t *invalid = reinterpret_cast<uint32_t *>(ws + L.invalid);
-  cudaError_t e = launch_route_internal(ids, n_rows, n_experts, htpe, offs, hids, invalid, s);
+  int4 *blk = reinterpret_cast<int4 *>(ws + L.blk);
+  uint32_t *n_blk = reinterpret_cast<uint32_t *>(ws + L.n_blk);
+  cudaError_t e = launch_route_internal(ids, n_rows, n_experts, htpe, offs, hids, invalid, s, blk, n_blk);
   if (e != cudaSuccess) return e;
   zero_invalid_rows_kernel<<<(unsigned)n_rows, 128, 0, s>>>(ids, n_rows, n_experts, N, out);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // Tensor-core form: K a multiple of 256 (whole 144-byte TMA boxes of Q4_0 blocks) and
+  // 16-byte aligned expert slabs.
+  const bool tc_ok = K % 256 == 0 && expert_stride % 16 == 0 && (reinterpret_cast<uintptr_t>(w) & 15) == 0;
+  if (tc_ok)
+    return launch_q4_0_mm_tc(x, w, out, n_tokens, top_k, N, K, n_experts, expert_stride, workspace, s);
   MvParams p{};
   p.x = x; p.w = w; p.ids = ids; p.order = hids; p.n_order = offs + n_experts; p.out = out;
   p.n_rows = n_rows; p.top_k = top_k; p.N = N; p.K = K; p.E = n_experts;

@@ -1,0 +1,377 @@
+// moe_tc.cu -- GGML Q4_0 expert-routed matmul, mat-mat form, on the tensor cores.
+//
+// quantized_matmul_id_ggml.rs (mlx-native 0.9.0): `dispatch_id_mm_for_test` regroups the
+// routed rows per expert (map0) so that a matmul tile reads a single expert's weights and
+// reuses them across that expert's routed rows instead of re-reading them per row.  Here:
+//
+//  1. routing (moe.cu): per-expert counts, ascending row lists, and a list of token blocks
+//     of <= 128 rows, each inside one expert;
+//  2. gather: xs[p] = fp16(x[hids[p] / top_k]) -- the rows of x in routed order;
+//  3. this kernel, persistent over work items (token block, 128-row weight tile):
+//       A = the expert's Q4_0 weight rows, decoded to fp16 by four producer warps from
+//           144-byte TMA boxes (8 blocks of 18 bytes = 256 k per box);
+//       B = the block's gathered x rows (TMA, 64-row boxes, 128-byte swizzle);
+//       D = 128 weight rows x (rows rounded up to 16) fp32 in tensor memory;
+//     epilogue warps scatter D column j to out[hids[p0 + j]][n0 .. n0+127] (fp32).
+//     Each expert's weights stream once from HBM per token block.
+//
+// Operands are fp16 (fp32 accumulation): Q4_0's d is already fp16, so (q - 8) * d is formed
+// with one fp16 multiply (a single rounding of the exact product), and x is rounded from fp32
+// to fp16 once in the gather.  Values |x| > 65504 would overflow; the gather flags them in
+// the device error word (Q4MM_DEVERR_F16_RANGE).  The mat-vec form stays in fp32 throughout.
+#include "tc_common.cuh"
+
+#include <cudaTypedefs.h>
+
+namespace q4mm {
+
+Q4MM_DEFINE_ERROR_READER(read_errors_moe_tc)
+
+namespace {
+
+constexpr int kTW = 128;            // weight rows per tile (MMA M)
+constexpr int kBK = 64;             // K per pipeline stage
+constexpr int kStages = 4;
+constexpr int kThreads = 320;       // warp 0 TMA, 1 MMA, 2-5 producers, 6-9 epilogue
+constexpr uint32_t kTmemCols = 256; // two 128-column accumulators
+constexpr uint32_t kABytes = kTW * kBK * 2;               // 16 KB
+constexpr uint32_t kBBytes = kMoeTokBlock * kBK * 2;      // 16 KB
+constexpr uint32_t kBoxTok = 64;                          // x rows per TMA box
+constexpr uint32_t kRawRow = 144;                         // 8 Q4_0 blocks = 4 K blocks
+constexpr uint32_t kRawBytes = kTW * kRawRow;             // 18 KB
+
+struct SmemL {
+  static constexpr uint32_t a = 0;
+  static constexpr uint32_t b = a + kStages * kABytes;
+  static constexpr uint32_t raw = b + kStages * kBBytes;   // [2]
+  // full_a, full_b, empty, acc_full[2], acc_empty[2], raw_full[2], raw_empty[2]
+  static constexpr uint32_t bars = raw + 2 * kRawBytes;
+  static constexpr uint32_t misc = bars + (3 * kStages + 8) * 8;
+  static constexpr uint32_t total = misc + 16;
+};
+constexpr size_t kSmem = SmemL::total + 1024;
+
+struct MmParams {
+  float *out;
+  const int32_t *hids;
+  const int4 *blk;
+  const uint32_t *n_blk;
+  int N, K;
+};
+
+struct MmMaps {
+  CUtensorMap w;   // 3D: [E][N][row bytes] uint8
+  CUtensorMap xs;  // 2D: [R][K] fp16, 128-byte swizzle
+};
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(mbar)
+      : "memory");
+}
+
+// Four nibbles (lo or hi halves of four qs bytes) as (q - 8) * d in fp16, natural-order
+// pairs.  (code | 0x6400) is the fp16 value 1024 + q; subtracting 1032 gives q - 8 exactly.
+__device__ __forceinline__ uint2 q4_0_pairs(uint32_t word, bool hi, uint32_t d2) {
+  constexpr uint32_t kMask = 0x000F000Fu, kMagic = 0x64006400u, kOff = 0x64086408u;   // 1024, 1032
+  uint32_t t01 = prmt(word, 0u, 0x4140u), t23 = prmt(word, 0u, 0x4342u);
+  if (hi) {
+    t01 >>= 4;
+    t23 >>= 4;
+  }
+  uint32_t q01, q23, r01, r23;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(q01) : "r"(and_or(t01, kMask, kMagic)), "r"(kOff));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(q23) : "r"(and_or(t23, kMask, kMagic)), "r"(kOff));
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r01) : "r"(q01), "r"(d2));
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r23) : "r"(q23), "r"(d2));
+  return make_uint2(r01, r23);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    q4_0_mm_tc_kernel(const __grid_constant__ MmMaps maps, const __grid_constant__ MmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - raw_base);
+  const uint32_t sA = base + SmemL::a, sB = base + SmemL::b, sR = base + SmemL::raw;
+  const uint32_t bar_full_a = base + SmemL::bars;
+  const uint32_t bar_full_b = bar_full_a + kStages * 8;
+  const uint32_t bar_empty = bar_full_b + kStages * 8;
+  const uint32_t bar_acc_full = bar_empty + kStages * 8;
+  const uint32_t bar_acc_empty = bar_acc_full + 16;
+  const uint32_t bar_raw_full = bar_acc_empty + 16;
+  const uint32_t bar_raw_empty = bar_raw_full + 16;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SmemL::misc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SmemL::misc + 4);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int KB = p.K / kBK;                 // multiple of 4
+  const int n_tiles = (p.N + kTW - 1) / kTW;
+  const int items = (int)*p.n_blk * n_tiles;
+  const int my_items = (int)blockIdx.x < items ? (items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int steps = my_items * KB;
+  auto item_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(bar_full_a + 8 * s, 128);
+      tc::mbar_init(bar_full_b + 8 * s, 1);
+      tc::mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(bar_acc_full + 8 * b, 1);
+      tc::mbar_init(bar_acc_empty + 8 * b, 4);
+      tc::mbar_init(bar_raw_full + 8 * b, 1);
+      tc::mbar_init(bar_raw_empty + 8 * b, 128);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+    tc::tma_prefetch_desc(&maps.w);
+    tc::tma_prefetch_desc(&maps.xs);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA: weight boxes every 4 K blocks, x rows every K block ----------------
+    if (lane == 0) {
+      int issued = 0, raw_issued = 0;
+      int cur_i = -1;
+      int4 bi = make_int4(0, 0, 0, 0);
+      int n0 = 0;
+      for (int j = 0; j < steps; ++j) {
+        const int i = j / KB, kb = j - i * KB;
+        if (i != cur_i) {
+          cur_i = i;
+          const int w = item_of(i);
+          bi = p.blk[w / n_tiles];
+          n0 = (w % n_tiles) * kTW;
+        }
+        if (kb % 4 == 0) {
+          const int q = i * (KB / 4) + kb / 4, slot = q & 1;
+          if (!tc::mbar_wait(bar_raw_empty + 8 * slot, ((q >> 1) & 1) ^ 1, abort_flag)) break;
+          tc::mbar_arrive_expect_tx(bar_raw_full + 8 * slot, kRawBytes);
+          tma_load_3d(sR + slot * kRawBytes, &maps.w, (kb / 4) * (int)kRawRow, n0, bi.x, bar_raw_full + 8 * slot);
+          ++raw_issued;
+        }
+        const int s = j % kStages;
+        const uint32_t ph = (j / kStages) & 1;
+        if (!tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag)) break;
+        const int boxes = (bi.z + (int)kBoxTok - 1) / (int)kBoxTok;
+        tc::mbar_arrive_expect_tx(bar_full_b + 8 * s, (uint32_t)boxes * kBoxTok * kBK * 2);
+        for (int bx = 0; bx < boxes; ++bx)
+          tc::tma_load_2d(sB + s * kBBytes + bx * kBoxTok * kBK * 2, &maps.xs, kb * kBK, bi.y + bx * (int)kBoxTok,
+                          bar_full_b + 8 * s);
+        ++issued;
+      }
+      if (*abort_flag) {
+        for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j) {
+          volatile int dummy = 0;
+          tc::mbar_wait(bar_full_b + 8 * (j % kStages), (j / kStages) & 1, &dummy);
+        }
+        for (int q = (raw_issued > 2 ? raw_issued - 2 : 0); q < raw_issued; ++q) {
+          volatile int dummy = 0;
+          tc::mbar_wait(bar_raw_full + 8 * (q & 1), (q >> 1) & 1, &dummy);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      bool ok = true;
+      for (int i = 0; i < my_items && ok; ++i) {
+        const int ab = i & 1;
+        const int cnt = p.blk[item_of(i) / n_tiles].z;
+        const uint32_t idesc = tc::idesc_f16_f32(kTW, ((cnt + 15) / 16) * 16);
+        ok = tc::mbar_wait(bar_acc_empty + 8 * ab, ((i >> 1) & 1) ^ 1, abort_flag);
+        if (!ok) break;
+        tc::tc_fence_after();
+        const uint32_t dtm = tmem + (uint32_t)(ab * kMoeTokBlock);
+        for (int kb = 0; kb < KB; ++kb) {
+          const int j = i * KB + kb, s = j % kStages;
+          const uint32_t ph = (j / kStages) & 1;
+          ok = tc::mbar_wait(bar_full_a + 8 * s, ph, abort_flag, 100) &&
+               tc::mbar_wait(bar_full_b + 8 * s, ph, abort_flag, 100);
+          if (!ok) break;
+          tc::tc_fence_after();
+          const uint64_t ad = tc::smem_desc_sw128(sA + s * kABytes);
+          const uint64_t bd = tc::smem_desc_sw128(sB + s * kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) tc::mma_bf16(dtm, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+          tc::mma_commit(bar_empty + 8 * s);
+        }
+        if (ok) tc::mma_commit(bar_acc_full + 8 * ab);
+      }
+    }
+  } else if (warp < 6) {
+    // ---------------- Q4_0 decode producers (one weight row per thread) ----------------
+    const int tp = threadIdx.x - 64;
+    for (int j = 0; j < steps; ++j) {
+      const int i = j / KB, kb = j - i * KB;
+      const int q = i * (KB / 4) + kb / 4, slot = q & 1;
+      if (kb % 4 == 0 && !tc::mbar_wait(bar_raw_full + 8 * slot, (q >> 1) & 1, abort_flag, 100)) break;
+      const int s = j % kStages;
+      const uint32_t ph = (j / kStages) & 1;
+      if (!tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, 100)) break;
+      // 36 bytes = blocks 2kk and 2kk+1 of this row, 4-byte aligned
+      const uint32_t *u = reinterpret_cast<const uint32_t *>(smem + SmemL::raw + slot * kRawBytes +
+                                                             tp * kRawRow + 36 * (kb % 4));
+      uint32_t v[9];
+#pragma unroll
+      for (int m = 0; m < 9; ++m) v[m] = u[m];
+      uint32_t qs[2][4], d2[2];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        qs[0][m] = prmt(v[m], v[m + 1], 0x5432u);   // block 0 bytes 2 + 4m .. 5 + 4m
+        qs[1][m] = v[5 + m];                        // block 1 bytes 20 + 4m ..
+      }
+      d2[0] = (v[0] & 0xFFFFu) | (v[0] << 16);
+      d2[1] = (v[4] >> 16) | (v[4] & 0xFFFF0000u);
+      uint8_t *a_tile = smem + SmemL::a + s * kABytes;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int h = c / 4, sub = c % 4;
+        const bool hi = sub >= 2;
+        const int wq = 2 * (sub & 1);
+        const uint2 p0 = q4_0_pairs(qs[h][wq], hi, d2[h]);
+        const uint2 p1 = q4_0_pairs(qs[h][wq + 1], hi, d2[h]);
+        *reinterpret_cast<uint4 *>(a_tile + tc::sw128_offset((uint32_t)tp, (uint32_t)c)) =
+            make_uint4(p0.x, p0.y, p1.x, p1.y);
+      }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(bar_full_a + 8 * s);
+      if (kb % 4 == 3) tc::mbar_arrive(bar_raw_empty + 8 * slot);
+    }
+  } else {
+    // ---------------- epilogue: TMEM -> out rows (fp32) ----------------
+    const int quarter = warp & 3;
+    for (int i = 0; i < my_items; ++i) {
+      const int ab = i & 1;
+      if (!tc::mbar_wait(bar_acc_full + 8 * ab, (i >> 1) & 1, abort_flag)) break;
+      tc::tc_fence_after();
+      const int w = item_of(i);
+      const int4 bi = p.blk[w / n_tiles];
+      const int n = (w % n_tiles) * kTW + quarter * 32 + lane;
+      for (int c0 = 0; c0 < bi.z; c0 += 32) {
+        uint32_t v[32];
+        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * kMoeTokBlock + c0), v);
+        tc::tmem_ld_wait();
+        const int r_lane = c0 + lane < bi.z ? p.hids[bi.y + c0 + lane] : 0;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int r = __shfl_sync(0xFFFFFFFFu, r_lane, jj);
+          if (c0 + jj < bi.z && n < p.N) p.out[(size_t)r * p.N + n] = __uint_as_float(v[jj]);
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(bar_acc_empty + 8 * ab);
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// xs[p] = fp16(x[hids[p] / top_k]) for p < number of valid routed rows.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const float *__restrict__ x, const int32_t *__restrict__ hids,
+                                                          const uint32_t *__restrict__ n_valid, int top_k, int K,
+                                                          uint16_t *__restrict__ xs, int n_rows) {
+  const int nv = (int)*n_valid;
+  for (int pos = blockIdx.x; pos < nv && pos < n_rows; pos += gridDim.x) {
+    const float4 *src = reinterpret_cast<const float4 *>(x + (size_t)(hids[pos] / top_k) * K);
+    uint2 *dst = reinterpret_cast<uint2 *>(xs + (size_t)pos * K);
+    bool out_of_range = false;
+    for (int k4 = threadIdx.x; k4 < K / 4; k4 += blockDim.x) {
+      const float4 f = __ldg(src + k4);
+      const float m = fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w)));
+      out_of_range |= !(m <= 65504.f);
+      __half2 h01 = __floats2half2_rn(f.x, f.y), h23 = __floats2half2_rn(f.z, f.w);
+      dst[k4] = make_uint2(*reinterpret_cast<uint32_t *>(&h01), *reinterpret_cast<uint32_t *>(&h23));
+    }
+    if (out_of_range) raise_device_error(Q4MM_DEVERR_F16_RANGE);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+}  // namespace
+
+cudaError_t launch_q4_0_mm_tc(const float *x, const uint8_t *w, float *out, int n_tokens, int top_k, int N,
+                              int K, int n_experts, uint64_t expert_stride, void *workspace, cudaStream_t s) {
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const int n_rows = n_tokens * top_k;
+  const MoeWorkspace L = moe_workspace_layout(n_rows, K, n_experts);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  const int32_t *hids = reinterpret_cast<const int32_t *>(ws + L.hids);
+  const uint32_t *offs = reinterpret_cast<const uint32_t *>(ws + L.offs);
+  uint16_t *xs = reinterpret_cast<uint16_t *>(ws + L.xs);
+  int sms = 148, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+
+  gather_rows_kernel<<<(unsigned)(n_rows < 4 * sms ? n_rows : 4 * sms), 256, 0, s>>>(x, hids, offs + n_experts, top_k,
+                                                                                    K, xs, n_rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  MmMaps maps;
+  const uint64_t row_bytes = (uint64_t)(K / 32) * 18;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)row_bytes, (cuuint64_t)N, (cuuint64_t)n_experts};
+    cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)expert_stride};
+    cuuint32_t box[3] = {kRawRow, (cuuint32_t)kTW, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(w), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)n_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, kBoxTok};
+    cuuint32_t estr[2] = {1, 1};
+    if (enc(&maps.xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xs, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  MmParams p{};
+  p.out = out;
+  p.hids = hids;
+  p.blk = reinterpret_cast<const int4 *>(ws + L.blk);
+  p.n_blk = reinterpret_cast<const uint32_t *>(ws + L.n_blk);
+  p.N = N;
+  p.K = K;
+  e = cudaFuncSetAttribute(q4_0_mm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+  if (e != cudaSuccess) return e;
+  q4_0_mm_tc_kernel<<<(unsigned)sms, kThreads, kSmem, s>>>(maps, p);
+  return cudaGetLastError();
+}
+
+}  // namespace q4mm

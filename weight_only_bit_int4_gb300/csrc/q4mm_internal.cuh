@@ -34,6 +34,7 @@ static __device__ unsigned int g_device_error = 0;
 
 cudaError_t read_errors_moe(unsigned int *out, int clear);
 cudaError_t read_errors_gemm(unsigned int *out, int clear);
+cudaError_t read_errors_moe_tc(unsigned int *out, int clear);
 
 __device__ __forceinline__ void raise_device_error(unsigned int bit) {
   atomicOr(&g_device_error, bit);
@@ -217,5 +218,39 @@ cudaError_t launch_q4_0_mm(const float *x, const uint8_t *w, const uint32_t *ids
 
 size_t q4_0_mm_workspace_bytes(int64_t n_tokens, int64_t top_k, int64_t N, int64_t K,
                                int64_t n_experts);
+
+// Workspace of the Q4_0 mat-mat path (every part 256-byte aligned):
+//   htpe    u32 [E]        per-expert routed counts
+//   offs    u32 [E + 1]    exclusive prefix of htpe (offs[E] = number of valid rows)
+//   hids    i32 [R]        routed rows grouped by expert, ascending within an expert
+//   invalid u32 [1]        rows whose id is >= E
+//   blk     int4 [B]       token blocks (expert, first position in hids, count <= 128, 0)
+//   n_blk   u32 [1]        number of token blocks
+//   xs      fp16 [R, K]    x rows gathered in hids order (the mm operand)
+constexpr int kMoeTokBlock = 128;
+struct MoeWorkspace {
+  size_t htpe, offs, hids, invalid, blk, n_blk, xs, total;
+};
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+inline MoeWorkspace moe_workspace_layout(int64_t n_rows, int64_t K, int64_t E) {
+  MoeWorkspace w{};
+  size_t o = 0;
+  w.htpe = o; o = align256(o + 4 * (size_t)E);
+  w.offs = o; o = align256(o + 4 * (size_t)(E + 1));
+  w.hids = o; o = align256(o + 4 * (size_t)n_rows);
+  w.invalid = o; o = align256(o + 4);
+  const size_t max_blk = (size_t)(n_rows + kMoeTokBlock - 1) / kMoeTokBlock + (size_t)E;
+  w.blk = o; o = align256(o + 16 * max_blk);
+  w.n_blk = o; o = align256(o + 4);
+  w.xs = o; o = align256(o + 2 * (size_t)n_rows * (size_t)K);
+  w.total = o;
+  return w;
+}
+
+cudaError_t launch_q4_0_route_blocks(const uint32_t *ids, int n_rows, int n_experts, void *workspace,
+                                     cudaStream_t s);
+cudaError_t launch_q4_0_mm_tc(const float *x, const uint8_t *w, float *out, int n_tokens, int top_k,
+                              int N, int K, int n_experts, uint64_t expert_stride, void *workspace,
+                              cudaStream_t s);
 
 }  // namespace q4mm
