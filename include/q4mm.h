@@ -169,6 +169,28 @@ q4mm_status q4_0_matmul_id(const float *x, const void *w, const uint32_t *ids, f
                            int64_t n_experts, uint64_t expert_stride, int mode,
                            void *workspace, size_t workspace_bytes, q4mm_stream_t stream);
 
+/* ======================================================================================
+ * Allocation-free variant of the mat-mat form (the source pages have no counterpart).
+ *
+ * For callers that cannot obtain device memory at the moment of the call -- code running
+ * inside a stream capture they do not control, serving loops that must never wait on or fail
+ * in the device allocator, hosts that own all device buffers.  Computes exactly what
+ * q4_0_matmul_id computes in mode 2 (mat-mat), with the same argument rules, but takes no
+ * workspace: its scratch is a fixed Q4MM_NOALLOC_SCRATCH_BYTES array built into the library,
+ * held on every device that loads the library until process exit.
+ *   - Returns Q4MM_ERR_WORKSPACE, launching nothing, when
+ *     q4_0_matmul_id_workspace_size(n_tokens, top_k, N, K, n_experts) exceeds the array.
+ *   - The first call on a device (made with that device current) looks up the array's device
+ *     address; make that first call before any stream capture that includes this call.
+ *   - All calls on a device share the array.  Calls that overlap on the GPU race on it and
+ *     give wrong results: order them (for instance on one stream).
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ * ====================================================================================*/
+#define Q4MM_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+q4mm_status q4_0_matmul_id_noalloc(const float *x, const void *w, const uint32_t *ids, float *out,
+                                   int64_t n_tokens, int64_t top_k, int64_t N, int64_t K,
+                                   int64_t n_experts, uint64_t expert_stride, q4mm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -111,3 +111,13 @@ def q4_0_matmul_id(x, w, ids, out, top_k: int, N: int, K: int, n_experts: int,
     _check("q4_0_matmul_id", lib().q4_0_matmul_id(
         _ptr(x), _ptr(w), _ptr(ids), _ptr(out), n_tokens, top_k, N, K, n_experts, expert_stride,
         mode, _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def q4_0_matmul_id_noalloc(x, w, ids, out, top_k: int, N: int, K: int, n_experts: int,
+                           expert_stride: int, stream=None) -> None:
+    """Mat-mat form of q4_0_matmul_id for callers that cannot provide (or allocate) a
+    workspace: the library's own fixed scratch array is used instead (see q4mm.h)."""
+    n_tokens = x.shape[0]
+    _check("q4_0_matmul_id_noalloc", lib().q4_0_matmul_id_noalloc(
+        _ptr(x), _ptr(w), _ptr(ids), _ptr(out), n_tokens, top_k, N, K, n_experts, expert_stride,
+        _stream(stream)))
