@@ -42,6 +42,22 @@ PREFILL_M = [512, 2048, 8192]
 HEADLINE = (1, 4096, 14336)   # (M, K, N) of the kernel whose roofline is reported
 
 
+def profiled_traffic(summary: str):
+    """DRAM bytes per launch from a committed ncu summary, or None once the kernel source
+    has changed since the capture (the summary records the source file's SHA-256)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", summary)
+    try:
+        fields = dict(line.split(": ", 1) for line in open(path).read().splitlines() if ": " in line
+                      and line.split(": ", 1)[0] in ("traffic_bytes_per_launch", "source", "source_sha256"))
+        src = os.path.join(ROOT, fields["source"])
+        if hashlib.sha256(open(src, "rb").read()).hexdigest() != fields["source_sha256"]:
+            return None
+        return int(fields["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def decode_shapes():
     return [(M, K, N) for (K, N) in DECODE_KN for M in DECODE_M]
 
@@ -295,7 +311,8 @@ def run_ours(args, rank, world, local_rank):
                        "frac": round(by_h / t_h / 1e9 / pk["hbm_gbs"], 3),
                        "frac_vs_8TBs": round(by_h / t_h / 8e12, 3),
                        "peak_source": pk["source"] + " (hbm_gbs, burst copy)",
-                       "traffic": None}
+                       "traffic": profiled_traffic("gemv_async_kernel_q4_gemv_M1_K4096_N14336.md"),
+                       "algorithmic_bytes_per_launch": by_h}
 
     # ---------------- e2e through the public API with host buffers ----------------
     out["e2e"] = e2e_decode(args, q, synth, rings, dev)
