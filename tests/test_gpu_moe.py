@@ -22,8 +22,10 @@ def _route_gpu(ids, E):
     return htpe.cpu().numpy().view(np.uint32), hids.cpu().numpy(), int(bad.cpu().numpy()[0])
 
 
+# (2000, 8, 64) and (20000, 1, 3) hold more ids than the per-expert form stages in shared
+# memory and take the single-CTA form.
 @pytest.mark.parametrize("n_tokens,top_k,E", [(1, 8, 64), (512, 8, 64), (37, 3, 5), (1000, 1, 7),
-                                              (3, 8, 1024), (700, 8, 64)])
+                                              (3, 8, 1024), (700, 8, 64), (2000, 8, 64), (20000, 1, 3)])
 def test_route_exact(n_tokens, top_k, E):
     ids = synth.routing_ids(90 + n_tokens, n_tokens, top_k, E) if top_k <= E else None
     htpe, hids, bad = _route_gpu(ids, E)
@@ -73,15 +75,19 @@ def test_moe_parity(mode, n_tokens, top_k, E, N, K, pad):
     assert_within_tolerance(got, ref, f"q4_0_matmul_id mode={mode}")
 
 
+# Invalid ids in one 32-row chunk, in chunks zeroed by different CTAs, and in an id count
+# large enough for the single-CTA routing form.
 @pytest.mark.parametrize("mode", [1, 2])
-def test_moe_invalid_id_gives_zero_row(mode):
-    n_tokens, top_k, E, N, K = 6, 2, 4, 64, 128
+@pytest.mark.parametrize("n_tokens,top_k,E,bad_rows", [(6, 2, 4, [5]), (300, 4, 8, [5, 100, 101, 700, 1199]),
+                                                       (1600, 8, 8, [0, 4000, 12799])])
+def test_moe_invalid_id_gives_zero_row(mode, n_tokens, top_k, E, bad_rows):
+    N, K = 64, 128
     x, w, stride, ids = _moe_case(7, n_tokens, top_k, E, N, K)
     ids = ids.copy()
-    ids[5] = 99
+    ids[bad_rows] = 99
     ref = oracle.q4_0_matmul_id(x, w, ids, n_tokens, top_k, N, K, E, stride)
     got = _run(x, w, ids, top_k, N, K, E, stride, mode)
-    assert np.all(got[5] == 0.0)
+    assert np.all(got[bad_rows] == 0.0)
     assert_within_tolerance(got, ref, "invalid id")
     assert q.device_errors() & 0x2
 

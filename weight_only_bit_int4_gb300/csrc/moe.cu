@@ -27,10 +27,19 @@ namespace {
 // Routing: stable counting sort of row indices by expert id.
 // Each warp owns a contiguous segment of rows.  Pass 1 counts ids per (warp, expert);
 // a scan over (expert, warp) gives every warp its write position per expert; pass 2
-// walks the segment again 32 rows at a time, ranking equal ids inside the step with
-// __match_any_sync, so the output order equals the input order within each expert.
+// walks the segment again 32 rows at a time, ranking equal ids inside the step by their
+// lane order, so the output order equals the input order within each expert.
 // ---------------------------------------------------------------------------------------
-constexpr int kRouteThreads = 1024;
+constexpr int kRouteThreads = 512;
+
+// Mask of the lanes whose key equals this lane's key (32 shuffles; measured much faster
+// here than the match instruction).
+__device__ __forceinline__ unsigned lanes_with_same_key(uint32_t key) {
+  unsigned m = 0;
+#pragma unroll
+  for (int l = 0; l < 32; ++l) m |= (__shfl_sync(0xFFFFFFFFu, key, l) == key ? 1u : 0u) << l;
+  return m;
+}
 
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const uint32_t *__restrict__ ids,
                                                               int n_rows, int E, int n_warps,
@@ -39,7 +48,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const uint32_t *__
                                                               int32_t *__restrict__ hids,
                                                               uint32_t *__restrict__ n_invalid,
                                                               int4 *__restrict__ blk = nullptr,
-                                                              uint32_t *__restrict__ n_blk = nullptr) {
+                                                              uint32_t *__restrict__ n_blk = nullptr,
+                                                              float *__restrict__ zero_out = nullptr,
+                                                              int zero_cols = 0) {
   extern __shared__ uint32_t sm[];
   uint32_t *cnt = sm;                       // [n_warps][E]
   uint32_t *pos = sm + n_warps * E;         // [n_warps][E]
@@ -55,17 +66,39 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const uint32_t *__
   const int r_begin = warp * seg;
   const int r_end = min(n_rows, r_begin + seg);
   const unsigned lt = (1u << lane) - 1u;
+  // Ids are read 8 x 32 at a time with all loads issued before any is used.
+  constexpr int kBatch = 8;
   if (warp < active_warps) {
     uint32_t bad = 0;
-    for (int base = r_begin; base < r_end; base += 32) {
+    for (int base0 = r_begin; base0 < r_end; base0 += 32 * kBatch) {
+    uint32_t ev[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int r = base0 + 32 * u + lane;
+      ev[u] = r < r_end ? __ldg(ids + r) : 0xFFFFFFFFu;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int base = base0 + 32 * u;
+      if (base >= r_end) break;
       const int r = base + lane;
       const bool in = r < r_end;
-      const uint32_t e = in ? __ldg(ids + r) : 0xFFFFFFFFu;
+      const uint32_t e = ev[u];
       const bool valid = in && e < (uint32_t)E;
       bad += (in && !valid) ? 1u : 0u;
-      const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : 0xFFFFFFFFu);
+      if (zero_out) {   // rows routed to no expert get zeros (the matmul visits valid rows only)
+        unsigned inv = __ballot_sync(0xFFFFFFFFu, in && !valid);
+        while (inv) {
+          const int l = __ffs(inv) - 1;
+          inv &= inv - 1;
+          float *row = zero_out + (size_t)(base + l) * zero_cols;
+          for (int n = lane; n < zero_cols; n += 32) row[n] = 0.f;
+        }
+      }
+      const unsigned peers = lanes_with_same_key(valid ? e : 0xFFFFFFFFu);
       if (valid && (peers & lt) == 0) cnt[warp * E + e] += __popc(peers);
       __syncwarp();
+    }
     }
     if (bad) atomicAdd(&bad_count, bad);
   }
@@ -112,19 +145,30 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const uint32_t *__
   __syncthreads();
 
   if (warp < active_warps) {
-    for (int base = r_begin; base < r_end; base += 32) {
-      const int r = base + lane;
-      const bool in = r < r_end;
-      const uint32_t e = in ? __ldg(ids + r) : 0xFFFFFFFFu;
-      const bool valid = in && e < (uint32_t)E;
-      const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : 0xFFFFFFFFu);
-      if (valid) {
-        const uint32_t p = pos[warp * E + e] + __popc(peers & lt);
-        hids[p] = r;
+    for (int base0 = r_begin; base0 < r_end; base0 += 32 * kBatch) {
+      uint32_t ev[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int r = base0 + 32 * u + lane;
+        ev[u] = r < r_end ? __ldg(ids + r) : 0xFFFFFFFFu;
       }
-      __syncwarp();
-      if (valid && (peers & lt) == 0) pos[warp * E + e] += __popc(peers);
-      __syncwarp();
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int base = base0 + 32 * u;
+        if (base >= r_end) break;
+        const int r = base + lane;
+        const bool in = r < r_end;
+        const uint32_t e = ev[u];
+        const bool valid = in && e < (uint32_t)E;
+        const unsigned peers = lanes_with_same_key(valid ? e : 0xFFFFFFFFu);
+        if (valid) {
+          const uint32_t p = pos[warp * E + e] + __popc(peers & lt);
+          hids[p] = r;
+        }
+        __syncwarp();
+        if (valid && (peers & lt) == 0) pos[warp * E + e] += __popc(peers);
+        __syncwarp();
+      }
     }
   }
 }
@@ -251,12 +295,111 @@ __global__ void __launch_bounds__(kMvWarps * 32) q4_0_mv_kernel(const __grid_con
   }
 }
 
-// Zero the output rows whose id is out of range (the mat-mat path only visits valid rows).
-__global__ void zero_invalid_rows_kernel(const uint32_t *__restrict__ ids, int n_rows, int E,
-                                         int N, float *__restrict__ out) {
-  const int r = blockIdx.x;
-  if (r >= n_rows || __ldg(ids + r) < (uint32_t)E) return;
-  for (int n = threadIdx.x; n < N; n += blockDim.x) out[(size_t)r * N + n] = 0.f;
+// ---------------------------------------------------------------------------------------
+// Routing, parallel form (used when n_experts * n_rows is moderate): CTA e owns expert e.
+// Every CTA histograms all ids in shared memory, which gives it the start of its list
+// (the number of valid ids below e) and its token-block base, with no cross-CTA traffic;
+// it then places the rows of expert e in ascending order: each warp scans a contiguous
+// segment with ballots, and a scan over the warps' counts orders the segments.
+// ---------------------------------------------------------------------------------------
+constexpr int kRouteParThreads = 256;
+constexpr size_t kRouteParSmemMax = 48 * 1024;   // E counts + all ids, without an opt-in
+
+__global__ void __launch_bounds__(kRouteParThreads) route_par_kernel(
+    const uint32_t *__restrict__ ids, int n_rows, int E, uint32_t *__restrict__ htpe,
+    uint32_t *__restrict__ offs, int32_t *__restrict__ hids, uint32_t *__restrict__ n_invalid,
+    int4 *__restrict__ blk, uint32_t *__restrict__ n_blk, float *__restrict__ zero_out, int zero_cols) {
+  extern __shared__ uint32_t hist[];                 // [E] counts, then the ids [n_rows]
+  __shared__ uint32_t warp_cnt[kRouteParThreads / 32];
+  __shared__ uint32_t s_less, s_blkbase, s_total, s_total_blk;
+  const int e = blockIdx.x;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const unsigned lt = (1u << lane) - 1u;
+  uint32_t *s_ids = hist + E;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+  {   // stage the ids: four independent loads in flight per thread
+    int r = threadIdx.x;
+    for (; r + 3 * kRouteParThreads < n_rows; r += 4 * kRouteParThreads) {
+      const uint32_t a = __ldg(ids + r), b = __ldg(ids + r + kRouteParThreads),
+                     c = __ldg(ids + r + 2 * kRouteParThreads), d = __ldg(ids + r + 3 * kRouteParThreads);
+      s_ids[r] = a;
+      s_ids[r + kRouteParThreads] = b;
+      s_ids[r + 2 * kRouteParThreads] = c;
+      s_ids[r + 3 * kRouteParThreads] = d;
+    }
+    for (; r < n_rows; r += kRouteParThreads) s_ids[r] = __ldg(ids + r);
+  }
+  __syncthreads();
+  // Histogram.  Warp w reads 32-row chunks w, w+8, ...; a chunk's ids routed to no expert
+  // are zeroed in the output by CTA (chunk mod E), so that work is spread over the grid.
+  for (int base = warp * 32; base < n_rows; base += blockDim.x) {
+    const int r = base + lane;
+    const uint32_t id = r < n_rows ? s_ids[r] : 0u;
+    const bool bad = r < n_rows && id >= (uint32_t)E;
+    if (r < n_rows && !bad) atomicAdd(&hist[id], 1u);
+    if (zero_out != nullptr && (base / 32) % E == e) {
+      unsigned m = __ballot_sync(0xFFFFFFFFu, bad);
+      while (m) {
+        const int rr = base + __ffs(m) - 1;
+        m &= m - 1;
+        for (int n = lane; n < zero_cols; n += 32) zero_out[(size_t)rr * zero_cols + n] = 0.f;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {   // prefix of counts and of block counts below e (and totals)
+    uint32_t less = 0, bbase = 0, tot = 0, tblk = 0;
+    for (int i = lane; i < E; i += 32) {
+      const uint32_t c = hist[i], b = (c + kMoeTokBlock - 1) / kMoeTokBlock;
+      tot += c;
+      tblk += b;
+      if (i < e) { less += c; bbase += b; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      less += __shfl_xor_sync(0xFFFFFFFFu, less, o);
+      bbase += __shfl_xor_sync(0xFFFFFFFFu, bbase, o);
+      tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
+      tblk += __shfl_xor_sync(0xFFFFFFFFu, tblk, o);
+    }
+    if (lane == 0) { s_less = less; s_blkbase = bbase; s_total = tot; s_total_blk = tblk; }
+  }
+  // rows of expert e: warp w scans rows [w*seg, (w+1)*seg)
+  const int nw = blockDim.x / 32;
+  const int seg = ((n_rows + nw - 1) / nw + 31) / 32 * 32;
+  const int r0 = warp * seg, r1 = min(n_rows, r0 + seg);
+  uint32_t mine = 0;
+  for (int b = r0; b < r1; b += 32) {
+    const int r = b + lane;
+    const bool hit = r < r1 && s_ids[r] == (uint32_t)e;
+    mine += __popc(__ballot_sync(0xFFFFFFFFu, hit));
+  }
+  if (lane == 0) warp_cnt[warp] = mine;
+  __syncthreads();
+  uint32_t pos = s_less;
+  for (int w = 0; w < warp; ++w) pos += warp_cnt[w];
+  for (int b = r0; b < r1; b += 32) {
+    const int r = b + lane;
+    const bool hit = r < r1 && s_ids[r] == (uint32_t)e;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, hit);
+    if (hit) hids[pos + __popc(m & lt)] = r;
+    pos += __popc(m);
+  }
+  if (threadIdx.x == 0) {
+    const uint32_t c = hist[e];
+    htpe[e] = c;
+    if (offs) offs[e] = s_less;
+    if (blk) {
+      for (uint32_t b0 = 0, k = 0; b0 < c; b0 += kMoeTokBlock, ++k)
+        blk[s_blkbase + k] = make_int4(e, (int)(s_less + b0), (int)min((uint32_t)kMoeTokBlock, c - b0), 0);
+    }
+    if (e == E - 1) {
+      if (offs) offs[E] = s_total;
+      if (n_blk) *n_blk = s_total_blk;
+      if (n_invalid) *n_invalid = (uint32_t)n_rows - s_total;
+      if ((uint32_t)n_rows != s_total) raise_device_error(Q4MM_DEVERR_BAD_EXPERT);
+    }
+  }
 }
 
 int route_warps(int E) {
@@ -270,12 +413,19 @@ size_t route_smem(int E, int n_warps) { return (size_t)(2 * n_warps * E + E + 1)
 
 cudaError_t launch_route_internal(const uint32_t *ids, int n_rows, int E, uint32_t *htpe,
                                   uint32_t *offs, int32_t *hids, uint32_t *n_invalid,
-                                  cudaStream_t s, int4 *blk = nullptr, uint32_t *n_blk = nullptr) {
+                                  cudaStream_t s, int4 *blk = nullptr, uint32_t *n_blk = nullptr,
+                                  float *zero_out = nullptr, int zero_cols = 0) {
+  if ((size_t)(E + n_rows) * 4 <= kRouteParSmemMax) {
+    route_par_kernel<<<(unsigned)E, kRouteParThreads, (size_t)(E + n_rows) * 4, s>>>(ids, n_rows, E, htpe, offs, hids,
+                                                                          n_invalid, blk, n_blk, zero_out, zero_cols);
+    return cudaGetLastError();
+  }
   const int nw = route_warps(E);
   const size_t sm = route_smem(E, nw);
   cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  route_kernel<<<1, nw * 32, sm, s>>>(ids, n_rows, E, nw, htpe, offs, hids, n_invalid, blk, n_blk);
+  route_kernel<<<1, nw * 32, sm, s>>>(ids, n_rows, E, nw, htpe, offs, hids, n_invalid, blk, n_blk, zero_out,
+                                      zero_cols);
   return cudaGetLastError();
 }
 
@@ -315,10 +465,9 @@ cudaError_t launch_q4_0_mm(const float *x, const uint8_t *w, const uint32_t *ids
   uint32_t *invalid = reinterpret_cast<uint32_t *>(ws + L.invalid);
   int4 *blk = reinterpret_cast<int4 *>(ws + L.blk);
   uint32_t *n_blk = reinterpret_cast<uint32_t *>(ws + L.n_blk);
-  cudaError_t e = launch_route_internal(ids, n_rows, n_experts, htpe, offs, hids, invalid, s, blk, n_blk);
+  cudaError_t e =
+      launch_route_internal(ids, n_rows, n_experts, htpe, offs, hids, invalid, s, blk, n_blk, out, N);
   if (e != cudaSuccess) return e;
-  zero_invalid_rows_kernel<<<(unsigned)n_rows, 128, 0, s>>>(ids, n_rows, n_experts, N, out);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // Tensor-core form: K a multiple of 256 (whole 144-byte TMA boxes of Q4_0 blocks) and
   // 16-byte aligned expert slabs.
   const bool tc_ok = K % 256 == 0 && expert_stride % 16 == 0 && (reinterpret_cast<uintptr_t>(w) & 15) == 0;

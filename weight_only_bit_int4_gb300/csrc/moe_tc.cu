@@ -32,21 +32,23 @@ namespace {
 constexpr int kTW = 128;            // weight rows per tile (MMA M)
 constexpr int kBK = 64;             // K per pipeline stage
 constexpr int kStages = 4;
-constexpr int kThreads = 320;       // warp 0 TMA, 1 MMA, 2-5 producers, 6-9 epilogue
+constexpr int kThreads = 480;       // warp 0 x TMA, 1 MMA, 2-9 producers, 10-13 epilogue, 14 weight TMA
+constexpr int kProducers = 256;     // two threads per weight row, one Q4_0 block each per K block
 constexpr uint32_t kTmemCols = 256; // two 128-column accumulators
 constexpr uint32_t kABytes = kTW * kBK * 2;               // 16 KB
 constexpr uint32_t kBBytes = kMoeTokBlock * kBK * 2;      // 16 KB
 constexpr uint32_t kBoxTok = 64;                          // x rows per TMA box
 constexpr uint32_t kRawRow = 144;                         // 8 Q4_0 blocks = 4 K blocks
 constexpr uint32_t kRawBytes = kTW * kRawRow;             // 18 KB
+constexpr int kRawSlots = 4;                              // weight boxes in flight
 
 struct SmemL {
   static constexpr uint32_t a = 0;
   static constexpr uint32_t b = a + kStages * kABytes;
-  static constexpr uint32_t raw = b + kStages * kBBytes;   // [2]
-  // full_a, full_b, empty, acc_full[2], acc_empty[2], raw_full[2], raw_empty[2]
-  static constexpr uint32_t bars = raw + 2 * kRawBytes;
-  static constexpr uint32_t misc = bars + (3 * kStages + 8) * 8;
+  static constexpr uint32_t raw = b + kStages * kBBytes;   // [kRawSlots]
+  // full_a, full_b, empty, acc_full[2], acc_empty[2], raw_full[kRawSlots], raw_empty[kRawSlots]
+  static constexpr uint32_t bars = raw + kRawSlots * kRawBytes;
+  static constexpr uint32_t misc = bars + (3 * kStages + 4 + 2 * kRawSlots) * 8;
   static constexpr uint32_t total = misc + 16;
 };
 constexpr size_t kSmem = SmemL::total + 1024;
@@ -103,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_acc_full = bar_empty + kStages * 8;
   const uint32_t bar_acc_empty = bar_acc_full + 16;
   const uint32_t bar_raw_full = bar_acc_empty + 16;
-  const uint32_t bar_raw_empty = bar_raw_full + 16;
+  const uint32_t bar_raw_empty = bar_raw_full + 8 * kRawSlots;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SmemL::misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SmemL::misc + 4);
 
@@ -117,15 +119,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(bar_full_a + 8 * s, 128);
+      tc::mbar_init(bar_full_a + 8 * s, kProducers);
       tc::mbar_init(bar_full_b + 8 * s, 1);
       tc::mbar_init(bar_empty + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(bar_acc_full + 8 * b, 1);
       tc::mbar_init(bar_acc_empty + 8 * b, 4);
+    }
+    for (int b = 0; b < kRawSlots; ++b) {
       tc::mbar_init(bar_raw_full + 8 * b, 1);
-      tc::mbar_init(bar_raw_empty + 8 * b, 128);
+      tc::mbar_init(bar_raw_empty + 8 * b, kProducers);
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -141,27 +145,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ---------------- TMA: weight boxes every 4 K blocks, x rows every K block ----------------
+  if (warp == 14) {
+    // ---------------- weight TMA: one 144-byte x 128-row box per 4 K blocks ----------------
+    // Runs ahead of the MMA by up to kRawSlots boxes, independently of the x stages.
     if (lane == 0) {
-      int issued = 0, raw_issued = 0;
+      int raw_issued = 0;
+      const int boxes_per_item = KB / 4;
+      for (int q = 0; q < my_items * boxes_per_item; ++q) {
+        const int i = q / boxes_per_item, bq = q - i * boxes_per_item;
+        const int w = item_of(i);
+        const int e = p.blk[w / n_tiles].x;
+        const int n0 = (w % n_tiles) * kTW;
+        const int slot = q % kRawSlots;
+        if (!tc::mbar_wait(bar_raw_empty + 8 * slot, ((q / kRawSlots) & 1) ^ 1, abort_flag)) break;
+        tc::mbar_arrive_expect_tx(bar_raw_full + 8 * slot, kRawBytes);
+        tma_load_3d(sR + slot * kRawBytes, &maps.w, bq * (int)kRawRow, n0, e, bar_raw_full + 8 * slot);
+        ++raw_issued;
+      }
+      if (*abort_flag) {
+        for (int q = (raw_issued > kRawSlots ? raw_issued - kRawSlots : 0); q < raw_issued; ++q) {
+          volatile int dummy = 0;
+          tc::mbar_wait(bar_raw_full + 8 * (q % kRawSlots), (q / kRawSlots) & 1, &dummy);
+        }
+      }
+    }
+  } else if (warp == 0) {
+    // ---------------- x TMA: the block's gathered rows, every K block ----------------
+    if (lane == 0) {
+      int issued = 0;
       int cur_i = -1;
       int4 bi = make_int4(0, 0, 0, 0);
-      int n0 = 0;
       for (int j = 0; j < steps; ++j) {
         const int i = j / KB, kb = j - i * KB;
         if (i != cur_i) {
           cur_i = i;
-          const int w = item_of(i);
-          bi = p.blk[w / n_tiles];
-          n0 = (w % n_tiles) * kTW;
-        }
-        if (kb % 4 == 0) {
-          const int q = i * (KB / 4) + kb / 4, slot = q & 1;
-          if (!tc::mbar_wait(bar_raw_empty + 8 * slot, ((q >> 1) & 1) ^ 1, abort_flag)) break;
-          tc::mbar_arrive_expect_tx(bar_raw_full + 8 * slot, kRawBytes);
-          tma_load_3d(sR + slot * kRawBytes, &maps.w, (kb / 4) * (int)kRawRow, n0, bi.x, bar_raw_full + 8 * slot);
-          ++raw_issued;
+          bi = p.blk[item_of(i) / n_tiles];
         }
         const int s = j % kStages;
         const uint32_t ph = (j / kStages) & 1;
@@ -177,10 +195,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j) {
           volatile int dummy = 0;
           tc::mbar_wait(bar_full_b + 8 * (j % kStages), (j / kStages) & 1, &dummy);
-        }
-        for (int q = (raw_issued > 2 ? raw_issued - 2 : 0); q < raw_issued; ++q) {
-          volatile int dummy = 0;
-          tc::mbar_wait(bar_raw_full + 8 * (q & 1), (q >> 1) & 1, &dummy);
         }
       }
     }
@@ -212,44 +226,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) tc::mma_commit(bar_acc_full + 8 * ab);
       }
     }
-  } else if (warp < 6) {
-    // ---------------- Q4_0 decode producers (one weight row per thread) ----------------
-    const int tp = threadIdx.x - 64;
-    for (int j = 0; j < steps; ++j) {
-      const int i = j / KB, kb = j - i * KB;
-      const int q = i * (KB / 4) + kb / 4, slot = q & 1;
-      if (kb % 4 == 0 && !tc::mbar_wait(bar_raw_full + 8 * slot, (q >> 1) & 1, abort_flag, 100)) break;
-      const int s = j % kStages;
-      const uint32_t ph = (j / kStages) & 1;
-      if (!tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, 100)) break;
-      // 36 bytes = blocks 2kk and 2kk+1 of this row, 4-byte aligned
-      const uint32_t *u = reinterpret_cast<const uint32_t *>(smem + SmemL::raw + slot * kRawBytes +
-                                                             tp * kRawRow + 36 * (kb % 4));
-      uint32_t v[9];
+  } else if (warp < 10) {
+    // ---------------- Q4_0 decode producers: thread (row, half) ----------------
+    // A row's 144-byte box (4 K blocks = 8 Q4_0 blocks) is read once with nine 16-byte loads
+    // (the 144-byte row stride puts 8 consecutive rows on distinct bank quads); thread half h
+    // then decodes block 2*kk + h of K block kk into chunks 4h .. 4h+3 of the bf16 row.
+    const int pt = threadIdx.x - 64;          // 0..255
+    const int tp = pt & (kTW - 1), half = pt >> 7;
+    const int boxes_per_item = KB / 4;
+    bool ok = true;
+    for (int q = 0; q < my_items * boxes_per_item && ok; ++q) {
+      const int slot = q % kRawSlots;
+      if (!tc::mbar_wait(bar_raw_full + 8 * slot, (q / kRawSlots) & 1, abort_flag, 100)) break;
+      uint32_t v[36];
+      {
+        const uint4 *row = reinterpret_cast<const uint4 *>(smem + SmemL::raw + slot * kRawBytes + tp * kRawRow);
 #pragma unroll
-      for (int m = 0; m < 9; ++m) v[m] = u[m];
-      uint32_t qs[2][4], d2[2];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        qs[0][m] = prmt(v[m], v[m + 1], 0x5432u);   // block 0 bytes 2 + 4m .. 5 + 4m
-        qs[1][m] = v[5 + m];                        // block 1 bytes 20 + 4m ..
+        for (int m = 0; m < 9; ++m) {
+          const uint4 r4 = row[m];
+          v[4 * m] = r4.x; v[4 * m + 1] = r4.y; v[4 * m + 2] = r4.z; v[4 * m + 3] = r4.w;
+        }
       }
-      d2[0] = (v[0] & 0xFFFFu) | (v[0] << 16);
-      d2[1] = (v[4] >> 16) | (v[4] & 0xFFFF0000u);
-      uint8_t *a_tile = smem + SmemL::a + s * kABytes;
+      tc::mbar_arrive(bar_raw_empty + 8 * slot);   // registers hold the box now
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int h = c / 4, sub = c % 4;
-        const bool hi = sub >= 2;
-        const int wq = 2 * (sub & 1);
-        const uint2 p0 = q4_0_pairs(qs[h][wq], hi, d2[h]);
-        const uint2 p1 = q4_0_pairs(qs[h][wq + 1], hi, d2[h]);
-        *reinterpret_cast<uint4 *>(a_tile + tc::sw128_offset((uint32_t)tp, (uint32_t)c)) =
-            make_uint4(p0.x, p0.y, p1.x, p1.y);
+      for (int kk = 0; kk < 4; ++kk) {
+        const int j = q * 4 + kk;                 // pipeline step (K block)
+        const int s = j % kStages;
+        const uint32_t ph = (j / kStages) & 1;
+        // block 2kk+half: 18 bytes at byte 36kk + 18 half
+        uint32_t qs[4], d2;
+        if (half == 0) {
+          const uint32_t *u = v + 9 * kk;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) qs[m] = prmt(u[m], u[m + 1], 0x5432u);
+          d2 = (u[0] & 0xFFFFu) | (u[0] << 16);
+        } else {
+          const uint32_t *u = v + 9 * kk + 4;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) qs[m] = u[1 + m];
+          d2 = (u[0] >> 16) | (u[0] & 0xFFFF0000u);
+        }
+        if (!tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, 100)) { ok = false; break; }
+        uint8_t *a_tile = smem + SmemL::a + s * kABytes;
+#pragma unroll
+        for (int sub = 0; sub < 4; ++sub) {
+          const bool hi = sub >= 2;
+          const int wq = 2 * (sub & 1);
+          const uint2 p0 = q4_0_pairs(qs[wq], hi, d2);
+          const uint2 p1 = q4_0_pairs(qs[wq + 1], hi, d2);
+          *reinterpret_cast<uint4 *>(a_tile + tc::sw128_offset((uint32_t)tp, (uint32_t)(4 * half + sub))) =
+              make_uint4(p0.x, p0.y, p1.x, p1.y);
+        }
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(bar_full_a + 8 * s);
       }
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(bar_full_a + 8 * s);
-      if (kb % 4 == 3) tc::mbar_arrive(bar_raw_empty + 8 * slot);
     }
   } else {
     // ---------------- epilogue: TMEM -> out rows (fp32) ----------------
