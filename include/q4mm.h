@@ -96,6 +96,23 @@ q4mm_status q4_gemv(const uint16_t *x, const uint32_t *w, const uint16_t *scales
                     const uint16_t *biases, uint16_t *y, int64_t M, int64_t N, int64_t K,
                     q4mm_stream_t stream);
 
+/* q4_gemv with launch flags (q4_gemv is q4_gemv_ex with flags = 0).
+ *
+ * Q4MM_GEMV_STATIC_WEIGHTS: the caller promises that w, scales and biases are not written
+ *   by the kernel that precedes this call in the stream.  The call is then launched with
+ *   programmatic stream serialization: its CTAs may start while that kernel is still
+ *   running and begin streaming W at once; they read x and write y only after that kernel
+ *   has completed and its writes are visible, so chaining calls whose x is the previous
+ *   call's y (or whose y is the previous call's x) stays correct.  Back-to-back decode
+ *   matmuls then overlap one call's weight stream with the previous call's tail.  Results
+ *   are bit-identical to flags = 0.  If the preceding kernel does write the weights, the
+ *   result is undefined.
+ * Unknown flag bits: Q4MM_ERR_INVALID_ARG. */
+#define Q4MM_GEMV_STATIC_WEIGHTS 0x1u
+q4mm_status q4_gemv_ex(const uint16_t *x, const uint32_t *w, const uint16_t *scales,
+                       const uint16_t *biases, uint16_t *y, int64_t M, int64_t N, int64_t K,
+                       uint32_t flags, q4mm_stream_t stream);
+
 /* Prefill matmul (meant for M > 16; any M >= 1 is served).  Fifth-generation tensor
  * cores: W tiles are dequantised to bf16 in shared memory, x tiles arrive by TMA,
  * fp32 accumulators live in tensor memory. */

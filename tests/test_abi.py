@@ -56,6 +56,9 @@ def test_int4_argument_checks(L):
     assert L.q4_gemv(FAKE + 2, FAKE, FAKE, FAKE, FAKE, 1, 64, 64, None) == 2
     # zero tokens -> OK with nothing enqueued
     assert L.q4_gemv(None, None, None, None, None, 0, 64, 64, None) == 0
+    # unknown launch flag bits -> INVALID_ARG (checked first); the known flag passes the check
+    assert L.q4_gemv_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 64, 0x2, None) == 1
+    assert L.q4_gemv_ex(None, None, None, None, None, 0, 64, 64, 0x1, None) == 0
     assert L.q4_gemm(None, None, None, None, None, 0, 64, 64, None) == 0
 
 

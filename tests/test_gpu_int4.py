@@ -35,7 +35,9 @@ def test_q4_dequant_bit_exact(N, K):
 
 # ---------------------------------------------------------------- decode GEMV
 @pytest.mark.parametrize("M,N,K", [(16, 256, 512), (1, 256, 512), (4, 256, 512), (7, 200, 96),
-                                   (9, 130, 1024), (16, 64, 4096), (3, 1000, 2080)])
+                                   (9, 130, 1024), (16, 64, 4096), (3, 1000, 2080), (2, 304, 1024),
+                                   (3, 200, 384), (1, 72, 14336), (4, 1000, 128), (3, 1000, 512),
+                                   (1, 9, 256), (2, 4104, 2048)])
 def test_q4_gemv_parity(M, N, K):
     x, w, s, b = _case(20 + M, M, N, K)
     ref = oracle.q4_matmul(x, w, s, b, M, N, K)
@@ -59,12 +61,13 @@ def test_q4_gemv_deterministic_and_no_stray_writes():
     assert np.all(g[0] == 0x7FC3) and np.all(g[-1] == 0x7FC3)
 
 
+@pytest.mark.parametrize("static_weights", [False, True])
 @pytest.mark.parametrize("M", [1, 4, 16])
 @pytest.mark.parametrize("K,N", [(4096, 14336), (14336, 4096), (4096, 4096)])
-def test_q4_gemv_full_size_sampled(M, K, N):
+def test_q4_gemv_full_size_sampled(M, K, N, static_weights):
     x, w, s, b = _case(1000 + M, M, N, K)
     y = poisoned_bf16(M, N)
-    q.q4_gemv(dev(x), dev(w), dev(s), dev(b), y)
+    q.q4_gemv(dev(x), dev(w), dev(s), dev(b), y, static_weights=static_weights)
     got_all = bf16_out(y)
     assert np.all(np.isfinite(got_all))
     rng = np.random.default_rng(M * 7 + K)
@@ -72,6 +75,63 @@ def test_q4_gemv_full_size_sampled(M, K, N):
     ni = np.concatenate([rng.integers(0, N, 590), np.arange(N - 10, N)])
     ref = oracle.q4_matmul_at(x, w, s, b, K, mi, ni)
     assert_within_tolerance(got_all[mi, ni], ref, f"q4_gemv full M={M} K={K} N={N}")
+
+
+# ------------------------------------------------ overlapped launches (Q4MM_GEMV_STATIC_WEIGHTS)
+def _chain(M, D, layers, static_weights, ping_pong, graph=False):
+    """Run `layers` dependent D x D decode matmuls back to back on one stream, each reading
+    the previous call's output (and, with ping_pong, writing over the previous call's input);
+    two weight sets alternate.  Returns every stored activation as host uint16."""
+    sets = [tuple(dev(a) for a in synth.int4_weights(700 + i, D, D)) for i in range(2)]
+    x0 = dev(synth.activations_bf16(710, M, D))
+    n_buf = 2 if ping_pong else layers + 1
+    bufs = [poisoned_bf16(M, D) for _ in range(n_buf)]
+    bufs[0].copy_(x0)
+
+    def calls():
+        for i in range(layers):
+            src, dst = bufs[i % n_buf], bufs[(i + 1) % n_buf]
+            q.q4_gemv(src, *sets[i % 2], dst, static_weights=static_weights)
+
+    if graph:
+        st = torch.cuda.Stream()
+        st.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            calls()
+        bufs[0].copy_(x0)
+        torch.cuda.synchronize()
+        g.replay()
+    else:
+        calls()
+    torch.cuda.synchronize()
+    return [host_u16(b_).copy() for b_ in bufs], sets
+
+
+@pytest.mark.parametrize("M,D", [(1, 4096), (16, 1024), (4, 1056)])
+@pytest.mark.parametrize("ping_pong", [False, True])
+def test_q4_gemv_static_weights_chain_is_bit_identical(M, D, ping_pong):
+    """Chained calls launched to overlap give exactly the outputs of plain launches: x is
+    read only after the producing call has finished (a read-after-write chain), and y is
+    written only after the previous call has finished reading it (ping-pong buffers)."""
+    layers = 6
+    plain, _ = _chain(M, D, layers, False, ping_pong)
+    over, _ = _chain(M, D, layers, True, ping_pong)
+    for a, b_ in zip(plain, over):
+        np.testing.assert_array_equal(a, b_)
+    graphed, _ = _chain(M, D, layers, True, ping_pong, graph=True)
+    for a, b_ in zip(plain, graphed):
+        np.testing.assert_array_equal(a, b_)
+
+
+def test_q4_gemv_static_weights_first_link_matches_oracle():
+    M, D = 4, 1024
+    bufs, _ = _chain(M, D, 2, True, False)
+    w, s, b = synth.int4_weights(700, D, D)
+    x = synth.activations_bf16(710, M, D)
+    ref = oracle.q4_matmul(x, w, s, b, M, D, D)
+    got = synth.bf16_bits_to_f32(bufs[1]).astype(np.float64)
+    assert_within_tolerance(got, ref, "first link")
 
 
 # ---------------------------------------------------------------- prefill GEMM (tensor cores)

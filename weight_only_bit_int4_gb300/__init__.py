@@ -56,10 +56,21 @@ def q4_dequant(w, scales, biases, out, stream=None) -> None:
                                           _DTYPES[out.dtype], _stream(stream)))
 
 
-def q4_gemv(x, w, scales, biases, y, stream=None) -> None:
-    """y[M, N] = x[M, K] . W^T for 1 <= M <= 16 (bf16 in/out)."""
+GEMV_STATIC_WEIGHTS = 0x1
+
+
+def q4_gemv(x, w, scales, biases, y, stream=None, static_weights: bool = False) -> None:
+    """y[M, N] = x[M, K] . W^T for 1 <= M <= 16 (bf16 in/out).
+
+    static_weights=True promises that the kernel before this call in the stream does not
+    write w/scales/biases; the call then streams W while that kernel finishes (q4_gemv_ex
+    with Q4MM_GEMV_STATIC_WEIGHTS).  Results are identical either way."""
     M, K = x.shape
     N = w.shape[0]
+    if static_weights:
+        _check("q4_gemv_ex", lib().q4_gemv_ex(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(y), M, N, K,
+                                              GEMV_STATIC_WEIGHTS, _stream(stream)))
+        return
     _check("q4_gemv", lib().q4_gemv(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(y), M, N, K,
                                     _stream(stream)))
 

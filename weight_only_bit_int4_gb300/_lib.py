@@ -18,6 +18,7 @@ SIGNATURES = {
     "q4mm_device_errors": ([_P, _S], _S),
     "q4_dequant": ([_P, _P, _P, _I, _I, _P, _S, _P], _S),
     "q4_gemv": ([_P, _P, _P, _P, _P, _I, _I, _I, _P], _S),
+    "q4_gemv_ex": ([_P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_uint32, _P], _S),
     "q4_gemm": ([_P, _P, _P, _P, _P, _I, _I, _I, _P], _S),
     "lut4_matmul": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _S, _P], _S),
     "lut4_dequant": ([_P, _P, _P, _I, _I, _I, _P, _S, _P], _S),

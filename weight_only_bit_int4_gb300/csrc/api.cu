@@ -91,6 +91,13 @@ q4mm_status q4_dequant(const uint32_t *w, const uint16_t *scales, const uint16_t
 q4mm_status q4_gemv(const uint16_t *x, const uint32_t *w, const uint16_t *scales,
                     const uint16_t *biases, uint16_t *y, int64_t M, int64_t N, int64_t K,
                     q4mm_stream_t stream) {
+  return q4_gemv_ex(x, w, scales, biases, y, M, N, K, 0u, stream);
+}
+
+q4mm_status q4_gemv_ex(const uint16_t *x, const uint32_t *w, const uint16_t *scales,
+                       const uint16_t *biases, uint16_t *y, int64_t M, int64_t N, int64_t K,
+                       uint32_t flags, q4mm_stream_t stream) {
+  if ((flags & ~Q4MM_GEMV_STATIC_WEIGHTS) != 0u) return Q4MM_ERR_INVALID_ARG;
   if (M == 0) return Q4MM_OK;
   if (M < 0 || M > 16) return Q4MM_ERR_INVALID_ARG;
   q4mm_status st = check_int4(w, scales, biases, N, K);
@@ -98,7 +105,8 @@ q4mm_status q4_gemv(const uint16_t *x, const uint32_t *w, const uint16_t *scales
   if (!x || !y) return Q4MM_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16)) return Q4MM_ERR_UNSUPPORTED;
   if ((st = check_device()) != Q4MM_OK) return st;
-  return from_cuda(launch_q4_gemv(x, w, scales, biases, y, (int)M, (int)N, (int)K, (cudaStream_t)stream));
+  return from_cuda(launch_q4_gemv(x, w, scales, biases, y, (int)M, (int)N, (int)K, (cudaStream_t)stream,
+                                  (flags & Q4MM_GEMV_STATIC_WEIGHTS) != 0u));
 }
 
 q4mm_status q4_gemm(const uint16_t *x, const uint32_t *w, const uint16_t *scales,

@@ -124,7 +124,7 @@ __device__ __forceinline__ int x_row_stride(int max_chunks) { return max_chunks 
 
 template <bool LUT>
 __device__ void stage_x(const GemvParams &p, uint8_t *xs, int c_begin, int nch,
-                        uint16_t *xsum = nullptr) {
+                        uint16_t *xsum = nullptr, float *xsum32 = nullptr) {
   const int TS = x_row_stride(p.max_chunks_per_cta);
   const int G = p.K / 32;
   const int items = p.M * nch * 4;   // tokens >= M are never read (their B fragments are zero)
@@ -167,16 +167,23 @@ __device__ void stage_x(const GemvParams &p, uint8_t *xs, int c_begin, int nch,
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       *reinterpret_cast<uint4 *>(dst + j * 64) = make_uint4(e[4 * j], e[4 * j + 1], e[4 * j + 2], e[4 * j + 3]);
-    if (xsum != nullptr) {   // sum of the group's 32 x values (fp32, fixed order) as bf16
+    if (xsum != nullptr || xsum32 != nullptr) {   // sum of the group's 32 x values (fp32, fixed order)
       float sum = 0.f;
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         sum += __uint_as_float(X[i] << 16) + __uint_as_float(X[i] & 0xFFFF0000u);
-      __nv_bfloat16 hb = __float2bfloat16_rn(sum);
-      xsum[tok * (p.max_chunks_per_cta * 4) + gl] = *reinterpret_cast<uint16_t *>(&hb);
+      if (xsum32 != nullptr) {
+        xsum32[tok * (p.max_chunks_per_cta * 4) + gl] = sum;
+      } else {
+        __nv_bfloat16 hb = __float2bfloat16_rn(sum);
+        xsum[tok * (p.max_chunks_per_cta * 4) + gl] = *reinterpret_cast<uint16_t *>(&hb);
+      }
     }
   }
 }
+
+template <int kRowsCta>
+__device__ __forceinline__ void cluster_sum_store(const GemvParams &p, float *red);
 
 // Partial tile -> shared memory (token-major red[tok][row]) -> sum over the cluster's
 // K splits in rank order through distributed shared memory -> bf16 y.
@@ -185,7 +192,6 @@ __device__ __forceinline__ void cluster_reduce_store(const GemvParams &p, float 
                                                      const float (&acc)[RT][MT][4], int warp,
                                                      int g, int t) {
   constexpr int kRowsCta = kWarps * 16 * RT;
-  const int S = gridDim.y;
 #pragma unroll
   for (int rt = 0; rt < RT; ++rt)
 #pragma unroll
@@ -197,6 +203,14 @@ __device__ __forceinline__ void cluster_reduce_store(const GemvParams &p, float 
       red[(tk + 0) * kRowsCta + rl + 8] = acc[rt][mt][2];
       red[(tk + 1) * kRowsCta + rl + 8] = acc[rt][mt][3];
     }
+  cluster_sum_store<kRowsCta>(p, red);
+}
+
+// red[tok][row] of every CTA in the cluster (one per K split) -> sum in rank order -> bf16 y.
+// Every thread of every CTA in the cluster calls this.
+template <int kRowsCta>
+__device__ __forceinline__ void cluster_sum_store(const GemvParams &p, float *red) {
+  const int S = gridDim.y;
   cluster_sync_all();
 
   // Each cluster rank finishes a strided share of the tile, summing ranks 0..S-1 in order.
@@ -204,7 +218,8 @@ __device__ __forceinline__ void cluster_reduce_store(const GemvParams &p, float 
   const int quads = kRowsCta / 4;
   const int items = p.M * quads;
   const uint32_t red_addr = smem_u32(red);
-  for (int i = (int)rank * kThreads + threadIdx.x; i < items; i += S * kThreads) {
+  const int nthr = (int)blockDim.x;
+  for (int i = (int)rank * nthr + (int)threadIdx.x; i < items; i += S * nthr) {
     const int tok = i / quads, qd = i % quads;
     const uint32_t off = (uint32_t)((tok * kRowsCta + qd * 4) * sizeof(float));
     float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -265,6 +280,9 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
   if (nch > 0) load(b0, 0);
   if (nch > 1) load(b1, 1);
   if (nch > 2) load(b2, 2);
+  // Weights are in flight; x may be the previous kernel's output, and y may still be read by it.
+  griddep_launch_dependents();
+  griddep_wait();
 
   if constexpr (LUT) {
     if (threadIdx.x < 16) book[threadIdx.x] = p.book[threadIdx.x];
@@ -337,6 +355,10 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
 // ---------------------------------------------------------------------------------------
 constexpr int kDepth = 8;
 constexpr int kStageBytes = 2 * 512 + 2 * 128;
+// Scale-block ring of the M <= 4 kernel: chunk a reads block a/4 while chunk a + kDepth - 1
+// is being fetched, at most (kDepth + 2) / 4 blocks later.
+constexpr int kSbSlots = (kDepth + 2) / 4 + 1;
+constexpr int kSbRow = 80, kSbSlot = 16 * kSbRow;
 
 __device__ __forceinline__ void cp_async(uint32_t dst, const void *src, int bytes, uint32_t src_bytes) {
   if (bytes == 16)
@@ -439,6 +461,9 @@ __global__ void __launch_bounds__(kThreads) gemv_async_kernel(const __grid_const
     if (i < nch) issue(i);
     cp_async_commit();
   }
+  // Weights are in flight; x may be the previous kernel's output, and y may still be read by it.
+  griddep_launch_dependents();
+  griddep_wait();
   if constexpr (LUT) {
     if (threadIdx.x < 16) book[threadIdx.x] = p.book[threadIdx.x];
   }
@@ -543,6 +568,442 @@ __global__ void __launch_bounds__(kThreads) gemv_async_kernel(const __grid_const
   cluster_reduce_store<MT, RT>(p, red, acc, warp, g, t);
 }
 
+// ---------------------------------------------------------------------------------------
+// INT4, 1 <= M <= 4: the scale and bias are applied after the tensor core, per group.
+//
+// With at most 4 tokens most B columns of an m16n8k16 step would be zero, so the columns
+// are spent on quantisation groups instead: in every step the quad lane t supplies the
+// k-slots of group t (its own 16-byte code vector) for every row, and B column n = 8u + j
+// carries token 2u + j/4 on the k-slots of group j%4 and zeros elsewhere.  Column n of the
+// product is then sum_{k in group} (128 + q) x for one (group, token) pair, with the codes
+// entering as exact bf16 integers 128 + q (one LOP3 each, no dequantising multiply).
+// After the chunk's 8 steps the lane holds columns 2t, 2t+1 of each tile, i.e. groups
+// 2(t&1) and 2(t&1)+1 of token 2u + t/2 for rows g and g+8, and adds, in fp32,
+//   s * D + (b - 128 s) * X,   X = sum of the group's x,
+// which is sum_k (q s + b) x_k for the group: the same dot product, reassociated.
+// ---------------------------------------------------------------------------------------
+// SB (K % 256 == 0, 16-byte aligned scales and biases): the scales and biases of 4 chunks
+// arrive together, two 16-byte copies per lane into a kSbSlots ring of [16 rows][s 32 B |
+// b 32 B | 16 B pad]; otherwise each chunk carries its own 8-byte runs as in the stage
+// layout above.
+template <int MT2, int RT, bool SB>
+__global__ void __launch_bounds__(kThreads) gemv_gc_kernel(const __grid_constant__ GemvParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int kRowsCta = kWarps * 16 * RT;
+  constexpr int kStageC = SB ? 1024 : kStageBytes;   // per row tile
+  constexpr int kStage = RT * kStageC;
+
+  const int TS = x_row_stride(p.max_chunks_per_cta);
+  const int xsum_stride = p.max_chunks_per_cta * 4;
+  uint8_t *ring = smem;
+  uint8_t *xs = smem + kWarps * kDepth * kStage;
+  uint8_t *sbr = ring + kWarps * kDepth * kStage;                     // SB: [warp][slot][RT]
+  if constexpr (SB) xs = sbr + kWarps * kSbSlots * kSbSlot * RT;
+  float *red = reinterpret_cast<float *>(xs + (size_t)p.M * TS);      // [M][kRowsCta]
+  float *xsum = red + p.M * kRowsCta;                                  // [M][4 * max_chunks]
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int g = lane / 4, t = lane % 4;
+  const int S = gridDim.y;
+  const int split = blockIdx.y;
+  const int c_begin = (int)(((long long)split * p.chunks) / S);
+  const int c_end = (int)(((long long)(split + 1) * p.chunks) / S);
+  const int nch = c_end - c_begin;
+  const int row0 = blockIdx.x * kRowsCta + warp * 16 * RT;
+  const int G = p.K / 32;
+
+  const uint8_t *wsrc[RT][2];
+  bool live[RT][2];
+#pragma unroll
+  for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = row0 + rt * 16 + g + 8 * h;
+      live[rt][h] = row < p.N;
+      wsrc[rt][h] = p.w + (live[rt][h] ? (size_t)row * (size_t)(p.K / 2) : 0) + (size_t)c_begin * 64 + t * 16;
+    }
+  // Lane (g, t) copies 4 consecutive bf16 (scales if t is even, biases if odd) of row
+  // g + 8 * (t >> 1) per chunk.
+  const int sh = t >> 1, sk = t & 1;
+  const uint8_t *ssrc[RT];
+  bool slive[RT];
+#pragma unroll
+  for (int rt = 0; rt < RT; ++rt) {
+    const int srow = row0 + rt * 16 + g + 8 * sh;
+    slive[rt] = srow < p.N;
+    const uint16_t *base = sk ? p.biases : static_cast<const uint16_t *>(p.scales);
+    ssrc[rt] = reinterpret_cast<const uint8_t *>(base + (slive[rt] ? (size_t)srow * G : 0) + (size_t)c_begin * 4);
+  }
+  const uint32_t ring_warp = smem_u32(ring) + (uint32_t)(warp * kDepth * kStage);
+  const uint32_t sdst_off = 1024u + (uint32_t)(sh * 128 + g * 16 + sk * 8);
+
+  const uint32_t sb_warp = smem_u32(sbr) + (uint32_t)(warp * kSbSlots * kSbSlot * RT);
+  const int blk0 = c_begin / 4;
+  auto issue = [&](int c) {
+    const uint32_t slot = ring_warp + (uint32_t)((c % kDepth) * kStage);
+    const int a = c_begin + c;
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt) {
+      const uint32_t sl = slot + rt * kStageC;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        cp_async(sl + h * 512 + lane * 16, wsrc[rt][h] + (size_t)c * 64, 16, live[rt][h] ? 16u : 0u);
+      if constexpr (!SB) {
+        cp_async(sl + sdst_off, ssrc[rt] + (size_t)c * 8, 8, slive[rt] ? 8u : 0u);
+      } else if (c == 0 || (a & 3) == 0) {
+        // block a/4: groups 16(a/4) .. +15 of 16 rows, scales and biases, in two halves
+        const int b = a >> 2;
+        const uint32_t sslot = sb_warp + (uint32_t)((((b - blk0) % kSbSlots) * RT + rt) * kSbSlot);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int idx = lane + 32 * i;
+          const int r = idx >> 2, ten = (idx >> 1) & 1, half = idx & 1;
+          const int row = row0 + rt * 16 + r;
+          const int g0 = 16 * b + 8 * half;
+          const bool ok = row < p.N && g0 < G;
+          const uint16_t *base = ten ? p.biases : static_cast<const uint16_t *>(p.scales);
+          const uint16_t *src = base + (ok ? (size_t)row * G + g0 : 0);
+          cp_async(sslot + (uint32_t)(r * kSbRow + ten * 32 + half * 16), src, 16, ok ? 16u : 0u);
+        }
+      }
+    }
+  };
+
+#pragma unroll
+  for (int i = 0; i < kDepth - 1; ++i) {
+    if (i < nch) issue(i);
+    cp_async_commit();
+  }
+  // Weights are in flight; x may be the previous kernel's output, and y may still be read by it.
+  griddep_launch_dependents();
+  griddep_wait();
+  stage_x<false>(p, xs, c_begin, nch, nullptr, xsum);
+  __syncthreads();
+
+  // B operand: tile u, column g -> token 2u + g/4 on group g%4, which is nonzero only in
+  // the k-slots of quad lane t == g%4.
+  bool bl[MT2];
+  const uint8_t *xl[MT2];
+#pragma unroll
+  for (int u = 0; u < MT2; ++u) {
+    const int tok = 2 * u + g / 4;
+    bl[u] = (g & 3) == t && tok < p.M;
+    xl[u] = xs + (size_t)(bl[u] ? tok : 0) * TS + t * 16;
+  }
+  // Accumulated columns: tile u -> token 2u + t/2, groups 2(t&1), 2(t&1)+1.
+  bool al[MT2];
+  const float *xsl[MT2];
+#pragma unroll
+  for (int u = 0; u < MT2; ++u) {
+    const int tok = 2 * u + t / 2;
+    al[u] = tok < p.M;
+    xsl[u] = xsum + (al[u] ? tok : 0) * xsum_stride + 2 * (t & 1);
+  }
+  float acc[RT][MT2][2];
+#pragma unroll
+  for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+    for (int u = 0; u < MT2; ++u) acc[rt][u][0] = acc[rt][u][1] = 0.f;
+  const uint8_t *ring_ptr = ring + warp * kDepth * kStage;
+
+  for (int c = 0; c < nch; ++c) {
+    if (c + kDepth - 1 < nch) issue(c + kDepth - 1);
+    cp_async_commit();
+    cp_async_wait<kDepth - 1>();
+    __syncwarp();
+    const uint8_t *slot = ring_ptr + (c % kDepth) * kStage;
+    uint4 xb[4][MT2];
+    float2 X[MT2];
+#pragma unroll
+    for (int u = 0; u < MT2; ++u) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        xb[q][u] = bl[u] ? *reinterpret_cast<const uint4 *>(xl[u] + c * 256 + q * 64) : make_uint4(0, 0, 0, 0);
+      X[u] = al[u] ? *reinterpret_cast<const float2 *>(xsl[u] + c * 4) : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt) {
+      const uint8_t *sl = slot + rt * kStageC;
+      const uint4 q0 = *reinterpret_cast<const uint4 *>(sl + lane * 16);
+      const uint4 q1 = *reinterpret_cast<const uint4 *>(sl + 512 + lane * 16);
+      uint32_t su[2], bu[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if constexpr (SB) {
+          const int a = c_begin + c;
+          const uint8_t *sc = sbr + (size_t)((warp * kSbSlots + ((a >> 2) - blk0) % kSbSlots) * RT + rt) * kSbSlot +
+                              (g + 8 * h) * kSbRow + (a & 3) * 8 + 4 * (t & 1);
+          su[h] = *reinterpret_cast<const uint32_t *>(sc);
+          bu[h] = *reinterpret_cast<const uint32_t *>(sc + 32);
+        } else {
+          const uint8_t *sc = sl + 1024 + h * 128 + g * 16 + 4 * (t & 1);
+          su[h] = *reinterpret_cast<const uint32_t *>(sc);
+          bu[h] = *reinterpret_cast<const uint32_t *>(sc + 8);
+        }
+      }
+      float D[MT2][4];
+#pragma unroll
+      for (int u = 0; u < MT2; ++u) D[u][0] = D[u][1] = D[u][2] = D[u][3] = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t w0 = q == 0 ? q0.x : q == 1 ? q0.y : q == 2 ? q0.z : q0.w;
+        const uint32_t w1 = q == 0 ? q1.x : q == 1 ? q1.y : q == 2 ? q1.z : q1.w;
+        constexpr uint32_t kMask = 0x000F000Fu, kMagic = 0x43004300u;   // bf16 128 + q
+        const uint32_t a0[4] = {and_or(w0, kMask, kMagic), and_or(w1, kMask, kMagic),
+                                and_or(w0 >> 4, kMask, kMagic), and_or(w1 >> 4, kMask, kMagic)};
+        const uint32_t a1[4] = {and_or(w0 >> 8, kMask, kMagic), and_or(w1 >> 8, kMask, kMagic),
+                                and_or(w0 >> 12, kMask, kMagic), and_or(w1 >> 12, kMask, kMagic)};
+#pragma unroll
+        for (int u = 0; u < MT2; ++u) {
+          mma_bf16_16816(D[u], a0, xb[q][u].x, xb[q][u].y);
+          mma_bf16_16816(D[u], a1, xb[q][u].z, xb[q][u].w);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float s0 = __uint_as_float(su[h] << 16), s1 = __uint_as_float(su[h] & 0xFFFF0000u);
+        const float b0 = __uint_as_float(bu[h] << 16), b1 = __uint_as_float(bu[h] & 0xFFFF0000u);
+        const float c0 = __fmaf_rn(-128.f, s0, b0), c1 = __fmaf_rn(-128.f, s1, b1);
+#pragma unroll
+        for (int u = 0; u < MT2; ++u) {
+          float a = acc[rt][u][h];
+          a = __fmaf_rn(s0, D[u][2 * h], a);
+          a = __fmaf_rn(s1, D[u][2 * h + 1], a);
+          a = __fmaf_rn(c0, X[u].x, a);
+          a = __fmaf_rn(c1, X[u].y, a);
+          acc[rt][u][h] = a;
+        }
+      }
+    }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+
+  // Lanes t and t^1 hold the two group pairs of the same token: add them, store red[tok][row].
+#pragma unroll
+  for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+    for (int u = 0; u < MT2; ++u)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float v = acc[rt][u][h] + __shfl_xor_sync(0xFFFFFFFFu, acc[rt][u][h], 1);
+        if ((t & 1) == 0 && al[u])
+          red[(2 * u + t / 2) * kRowsCta + warp * 16 * RT + rt * 16 + g + 8 * h] = v;
+      }
+  cluster_sum_store<kRowsCta>(p, red);
+}
+
+// ---------------------------------------------------------------------------------------
+// INT4, 1 <= M <= 4, K % 256 == 0: the group-column product of gemv_gc_kernel with the K
+// split inside the CTA.  A CTA owns one 16-row group and its KS warps take consecutive K
+// slices; each warp streams its slice through a private cp.async ring (DEPTH code stages
+// and a ring of 4-chunk scale blocks) and stages only the x it needs, so nothing couples
+// the warps until their partial tiles meet in shared memory, where they are summed in warp
+// order.  A further split across the CTAs of a cluster (S > 1) is combined through
+// distributed shared memory as above.
+// ---------------------------------------------------------------------------------------
+__host__ __device__ constexpr int ks_sb_slots(int depth) { return (depth + 2) / 4 + 1; }
+__host__ __device__ inline int ks_x_stride(int maxc) { return maxc * 256 + 64; }
+// Per-warp shared memory: code ring, scale-block ring, x [M][ks_x_stride], x sums [M][4 maxc].
+__host__ __device__ inline size_t ks_warp_bytes(int depth, int M, int maxc) {
+  return (size_t)depth * 1024 + (size_t)ks_sb_slots(depth) * kSbSlot + (size_t)M * ks_x_stride(maxc) +
+         (size_t)M * maxc * 16;
+}
+
+template <int MT2, int KS, int DEPTH>
+__global__ void __launch_bounds__(KS * 32) gemv_ks_kernel(const __grid_constant__ GemvParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int kSlots = ks_sb_slots(DEPTH);
+  const int maxc = p.max_chunks_per_cta;
+  const int XS = ks_x_stride(maxc);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int g = lane / 4, t = lane % 4;
+  uint8_t *wbase = smem + (size_t)warp * ks_warp_bytes(DEPTH, p.M, maxc);
+  uint8_t *ring = wbase;
+  uint8_t *sbr = wbase + DEPTH * 1024;
+  uint8_t *xs = sbr + kSlots * kSbSlot;
+  float *xsum = reinterpret_cast<float *>(xs + (size_t)p.M * XS);                  // [M][4 maxc]
+  float *red = reinterpret_cast<float *>(smem + (size_t)KS * ks_warp_bytes(DEPTH, p.M, maxc));  // [KS][M][16]
+
+  const int splits = (int)gridDim.y * KS;
+  const int sp = (int)blockIdx.y * KS + warp;
+  const int c_begin = (int)(((long long)sp * p.chunks) / splits);
+  const int c_end = (int)(((long long)(sp + 1) * p.chunks) / splits);
+  const int nch = c_end - c_begin;
+  const int row0 = blockIdx.x * 16;
+  const int G = p.K / 32;
+
+  const uint8_t *wsrc[2];
+  bool live[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int row = row0 + g + 8 * h;
+    live[h] = row < p.N;
+    wsrc[h] = p.w + (live[h] ? (size_t)row * (size_t)(p.K / 2) : 0) + (size_t)c_begin * 64 + t * 16;
+  }
+  const uint32_t ring_s = smem_u32(ring), sb_s = smem_u32(sbr);
+  const int blk0 = c_begin / 4;
+  auto issue = [&](int c) {
+    const uint32_t slot = ring_s + (uint32_t)((c % DEPTH) * 1024);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      cp_async(slot + h * 512 + lane * 16, wsrc[h] + (size_t)c * 64, 16, live[h] ? 16u : 0u);
+    const int a = c_begin + c;
+    if (c == 0 || (a & 3) == 0) {   // scales and biases of chunks 4(a/4) .. +3, 16 rows
+      const int b = a >> 2;
+      const uint32_t sslot = sb_s + (uint32_t)(((b - blk0) % kSlots) * kSbSlot);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int idx = lane + 32 * i;
+        const int r = idx >> 2, ten = (idx >> 1) & 1, half = idx & 1;
+        const int row = row0 + r;
+        const int g0 = 16 * b + 8 * half;
+        const bool ok = row < p.N && g0 < G;
+        const uint16_t *base = ten ? p.biases : static_cast<const uint16_t *>(p.scales);
+        cp_async(sslot + (uint32_t)(r * kSbRow + ten * 32 + half * 16), base + (ok ? (size_t)row * G + g0 : 0), 16,
+                 ok ? 16u : 0u);
+      }
+    }
+  };
+
+#pragma unroll
+  for (int i = 0; i < DEPTH - 1; ++i) {
+    if (i < nch) issue(i);
+    cp_async_commit();
+  }
+  // Weights are in flight; x may be the previous kernel's output, and y may still be read by it.
+  griddep_launch_dependents();
+  griddep_wait();
+
+  // This warp's x slice, permuted to the decode's (i, i+4) pair order, and its group sums.
+  for (int it = lane; it < p.M * nch * 4; it += 32) {
+    const int tok = it / (nch * 4);
+    const int gl = it % (nch * 4);
+    const int c = gl / 4, tq = gl % 4;
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.x + (size_t)tok * p.K + (size_t)((c_begin + c) * 4 + tq) * 32);
+    uint32_t X[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = __ldg(src + i);
+      X[4 * i] = v.x; X[4 * i + 1] = v.y; X[4 * i + 2] = v.z; X[4 * i + 3] = v.w;
+    }
+    uint8_t *dst = xs + (size_t)tok * XS + c * 256 + tq * 16;
+    float sum = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t a0 = X[4 * q], b0 = X[4 * q + 2], a1 = X[4 * q + 1], b1 = X[4 * q + 3];
+      *reinterpret_cast<uint4 *>(dst + q * 64) =
+          make_uint4(prmt(a0, b0, 0x5410), prmt(a0, b0, 0x7632), prmt(a1, b1, 0x5410), prmt(a1, b1, 0x7632));
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sum += __uint_as_float(X[i] << 16) + __uint_as_float(X[i] & 0xFFFF0000u);
+    xsum[tok * maxc * 4 + gl] = sum;
+  }
+  __syncwarp();
+
+  bool bl[MT2], al[MT2];
+  const uint8_t *xl[MT2];
+  const float *xsl[MT2];
+#pragma unroll
+  for (int u = 0; u < MT2; ++u) {
+    const int tb = 2 * u + g / 4;
+    bl[u] = (g & 3) == t && tb < p.M;
+    xl[u] = xs + (size_t)(bl[u] ? tb : 0) * XS + t * 16;
+    const int ta = 2 * u + t / 2;
+    al[u] = ta < p.M;
+    xsl[u] = xsum + (al[u] ? ta : 0) * maxc * 4 + 2 * (t & 1);
+  }
+  float acc[MT2][2];
+#pragma unroll
+  for (int u = 0; u < MT2; ++u) acc[u][0] = acc[u][1] = 0.f;
+
+  for (int c = 0; c < nch; ++c) {
+    if (c + DEPTH - 1 < nch) issue(c + DEPTH - 1);
+    cp_async_commit();
+    cp_async_wait<DEPTH - 1>();
+    __syncwarp();
+    const uint8_t *sl = ring + (c % DEPTH) * 1024;
+    uint4 xb[4][MT2];
+    float2 X[MT2];
+#pragma unroll
+    for (int u = 0; u < MT2; ++u) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        xb[q][u] = bl[u] ? *reinterpret_cast<const uint4 *>(xl[u] + c * 256 + q * 64) : make_uint4(0, 0, 0, 0);
+      X[u] = al[u] ? *reinterpret_cast<const float2 *>(xsl[u] + c * 4) : make_float2(0.f, 0.f);
+    }
+    const uint4 q0 = *reinterpret_cast<const uint4 *>(sl + lane * 16);
+    const uint4 q1 = *reinterpret_cast<const uint4 *>(sl + 512 + lane * 16);
+    const int a = c_begin + c;
+    const uint8_t *sc = sbr + ((a >> 2) - blk0) % kSlots * kSbSlot + g * kSbRow + (a & 3) * 8 + 4 * (t & 1);
+    uint32_t su[2], bu[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      su[h] = *reinterpret_cast<const uint32_t *>(sc + h * 8 * kSbRow);
+      bu[h] = *reinterpret_cast<const uint32_t *>(sc + h * 8 * kSbRow + 32);
+    }
+    float D[MT2][4];
+#pragma unroll
+    for (int u = 0; u < MT2; ++u) D[u][0] = D[u][1] = D[u][2] = D[u][3] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t w0 = q == 0 ? q0.x : q == 1 ? q0.y : q == 2 ? q0.z : q0.w;
+      const uint32_t w1 = q == 0 ? q1.x : q == 1 ? q1.y : q == 2 ? q1.z : q1.w;
+      constexpr uint32_t kMask = 0x000F000Fu, kMagic = 0x43004300u;   // bf16 128 + q
+      const uint32_t a0[4] = {and_or(w0, kMask, kMagic), and_or(w1, kMask, kMagic),
+                              and_or(w0 >> 4, kMask, kMagic), and_or(w1 >> 4, kMask, kMagic)};
+      const uint32_t a1[4] = {and_or(w0 >> 8, kMask, kMagic), and_or(w1 >> 8, kMask, kMagic),
+                              and_or(w0 >> 12, kMask, kMagic), and_or(w1 >> 12, kMask, kMagic)};
+#pragma unroll
+      for (int u = 0; u < MT2; ++u) {
+        mma_bf16_16816(D[u], a0, xb[q][u].x, xb[q][u].y);
+        mma_bf16_16816(D[u], a1, xb[q][u].z, xb[q][u].w);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float s0 = __uint_as_float(su[h] << 16), s1 = __uint_as_float(su[h] & 0xFFFF0000u);
+      const float b0 = __uint_as_float(bu[h] << 16), b1 = __uint_as_float(bu[h] & 0xFFFF0000u);
+      const float c0 = __fmaf_rn(-128.f, s0, b0), c1 = __fmaf_rn(-128.f, s1, b1);
+#pragma unroll
+      for (int u = 0; u < MT2; ++u) {
+        float v = acc[u][h];
+        v = __fmaf_rn(s0, D[u][2 * h], v);
+        v = __fmaf_rn(s1, D[u][2 * h + 1], v);
+        v = __fmaf_rn(c0, X[u].x, v);
+        v = __fmaf_rn(c1, X[u].y, v);
+        acc[u][h] = v;
+      }
+    }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+
+#pragma unroll
+  for (int u = 0; u < MT2; ++u)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float v = acc[u][h] + __shfl_xor_sync(0xFFFFFFFFu, acc[u][h], 1);
+      if ((t & 1) == 0 && al[u]) red[(warp * p.M + 2 * u + t / 2) * 16 + g + 8 * h] = v;
+    }
+  __syncthreads();
+  // Sum the KS slices in warp order into red[tok][row] (slice 0's place), then to y.
+  for (int i = threadIdx.x; i < p.M * 16; i += KS * 32) {
+    float v = red[i];
+#pragma unroll
+    for (int w = 1; w < KS; ++w) v += red[w * p.M * 16 + i];
+    red[i] = v;
+    if (gridDim.y == 1) {
+      const int row = row0 + (i & 15);
+      if (row < p.N) {
+        __nv_bfloat16 hb = __float2bfloat16_rn(v);
+        p.y[(size_t)(i >> 4) * p.N + row] = *reinterpret_cast<uint16_t *>(&hb);
+      }
+    }
+  }
+  if (gridDim.y > 1) cluster_sum_store<16>(p, red);
+}
+
 struct Plan {
   int MT, RT, S, max_chunks;
   size_t smem;
@@ -596,7 +1057,7 @@ Plan make_plan(int M, int N, int K) {
 }
 
 template <int MT, int RT, bool LUT>
-cudaError_t launch_typed(const GemvParams &p, const Plan &pl, cudaStream_t s) {
+cudaError_t launch_typed(const GemvParams &p, const Plan &pl, cudaStream_t s, bool overlap) {
   auto kern = gemv_kernel<MT, RT, LUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   if (e != cudaSuccess) return e;
@@ -606,13 +1067,15 @@ cudaError_t launch_typed(const GemvParams &p, const Plan &pl, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = (unsigned)pl.S;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = overlap ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
@@ -623,7 +1086,10 @@ size_t async_smem_bytes(int M, int MT, int RT, int max_chunks) {
 
 // All CTAs resident in one wave; among those plans, the best-balanced one with the most
 // rows per warp and the fewest K splits.
-Plan make_async_plan(int M, int N, int K) {
+size_t gc_smem_bytes(int M, int RT, int max_chunks);
+
+// gc: plan for gemv_gc_kernel (INT4, M <= 4), whose shared-memory footprint differs.
+Plan make_async_plan(int M, int N, int K, bool gc) {
   Plan pl{};
   pl.MT = M <= 8 ? 1 : 2;
   const int chunks = K / 128;
@@ -637,7 +1103,7 @@ Plan make_async_plan(int M, int N, int K) {
     const int rb = (N + kWarps * 16 * RT - 1) / (kWarps * 16 * RT);
     for (int S = 1; S <= std::min(kMaxCluster, chunks); ++S) {
       const int maxc = (chunks + S - 1) / S;
-      const size_t sm = async_smem_bytes(M, pl.MT, RT, maxc);
+      const size_t sm = gc ? gc_smem_bytes(M, RT, maxc) : async_smem_bytes(M, pl.MT, RT, maxc);
       if (sm > 227 * 1024) continue;
       const int per_sm = std::max(1, std::min((int)((228 * 1024) / (sm + 1024)), 8));
       const long long ctas = (long long)rb * S;
@@ -660,7 +1126,7 @@ Plan make_async_plan(int M, int N, int K) {
 }
 
 template <int MT, int RT, bool LUT>
-cudaError_t launch_async_typed(const GemvParams &p, const Plan &pl, cudaStream_t s) {
+cudaError_t launch_async_typed(const GemvParams &p, const Plan &pl, cudaStream_t s, bool overlap) {
   auto kern = gemv_async_kernel<MT, RT, LUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   if (e != cudaSuccess) return e;
@@ -669,43 +1135,175 @@ cudaError_t launch_async_typed(const GemvParams &p, const Plan &pl, cudaStream_t
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = (unsigned)pl.S;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = overlap ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+size_t gc_smem_bytes(int M, int RT, int max_chunks) {   // the larger of the two layouts (SB)
+  return (size_t)kWarps * (kDepth * 1024 + kSbSlots * kSbSlot) * RT + (size_t)M * (max_chunks * 256 + 64) +
+         (size_t)M * kWarps * 16 * RT * 4 + (size_t)M * max_chunks * 4 * 4;
+}
+
+template <int MT2, int RT>
+cudaError_t launch_gc_typed(const GemvParams &p, const Plan &pl, cudaStream_t s, bool overlap) {
+  const bool sb = p.K % 256 == 0 && (reinterpret_cast<uintptr_t>(p.scales) & 15u) == 0 &&
+                  (reinterpret_cast<uintptr_t>(p.biases) & 15u) == 0;
+  auto kern = sb ? gemv_gc_kernel<MT2, RT, true> : gemv_gc_kernel<MT2, RT, false>;
+  const size_t smem = gc_smem_bytes(p.M, RT, pl.max_chunks);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((p.N + kWarps * 16 * RT - 1) / (kWarps * 16 * RT)), (unsigned)pl.S, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = (unsigned)pl.S;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+struct KsPlan {
+  int KS = 0, S = 0, depth = 0, maxc = 0;
+  size_t smem = 0;
+};
+
+// Shapes for gemv_ks_kernel: all CTAs in one wave, as evenly spread over the SMs as possible,
+// with enough warps per SM to hide latency and enough chunk stages in flight per SM to keep
+// HBM busy; K splits across CTAs (clusters) only when the K split inside a CTA is not enough.
+KsPlan make_ks_plan(int M, int N, int K) {
+  KsPlan best;
+  int sms = 152, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
+  }
+  const int R = (N + 15) / 16, C = K / 128;
+  const int regs = M <= 2 ? 48 : 80;    // per thread, as compiled (ptxas -v)
+  double best_score = -1e30;
+  for (int depth : {4, 8})
+    for (int KS : {2, 4, 8})
+      for (int S : {1, 2, 4, 8}) {
+        if (KS * S > C) continue;
+        const int maxc = (C + KS * S - 1) / (KS * S);
+        const size_t smem = (size_t)KS * ks_warp_bytes(depth, M, maxc) + (size_t)KS * M * 16 * 4;
+        if (smem > 227 * 1024) continue;
+        int per_sm = (int)((228 * 1024) / (smem + 1024));
+        per_sm = std::min(per_sm, 2048 / (KS * 32));
+        per_sm = std::min(per_sm, 65536 / (KS * 32 * regs));
+        per_sm = std::min(per_sm, 32);
+        if (per_sm < 1) continue;
+        const long long ctas = (long long)R * S;
+        const long long need = (ctas + sms - 1) / sms;
+        if (need > per_sm) continue;
+        const double balance = (double)ctas / (double)(need * sms);
+        const double warps = (double)need * KS;                       // on the busiest SM
+        const double stages_kb = warps * (depth - 1);                  // code stages in flight
+        double score = balance * std::min(1.0, warps / 16.0) * std::min(1.0, stages_kb / 48.0);
+        score -= (S > 1 ? 0.03 : 0.0) + 0.01 * S;
+        if (maxc < 4) score -= 0.04 * (4 - maxc);
+        if (score > best_score) {
+          best_score = score;
+          best.KS = KS; best.S = S; best.depth = depth; best.maxc = maxc; best.smem = smem;
+        }
+      }
+  return best;
+}
+
+template <int MT2, int KS, int DEPTH>
+cudaError_t launch_ks_typed(const GemvParams &p, const KsPlan &pl, cudaStream_t s, bool overlap) {
+  auto kern = gemv_ks_kernel<MT2, KS, DEPTH>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((p.N + 15) / 16), (unsigned)pl.S, 1);
+  cfg.blockDim = dim3(KS * 32, 1, 1);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pl.S > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 1;
+    attr[n].val.clusterDim.y = (unsigned)pl.S;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (overlap) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = (unsigned)n;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int MT2>
+cudaError_t launch_ks(const GemvParams &p, const KsPlan &pl, cudaStream_t s, bool overlap) {
+  if (pl.depth == 4) {
+    if (pl.KS == 2) return launch_ks_typed<MT2, 2, 4>(p, pl, s, overlap);
+    if (pl.KS == 4) return launch_ks_typed<MT2, 4, 4>(p, pl, s, overlap);
+    return launch_ks_typed<MT2, 8, 4>(p, pl, s, overlap);
+  }
+  if (pl.KS == 2) return launch_ks_typed<MT2, 2, 8>(p, pl, s, overlap);
+  if (pl.KS == 4) return launch_ks_typed<MT2, 4, 8>(p, pl, s, overlap);
+  return launch_ks_typed<MT2, 8, 8>(p, pl, s, overlap);
+}
+
 template <bool LUT>
-cudaError_t launch_any(GemvParams &p, cudaStream_t s) {
+cudaError_t launch_any(GemvParams &p, cudaStream_t s, bool overlap) {
   p.chunks = (p.K / 32 + 3) / 4;
+  if (!LUT && p.M <= 4 && p.K % 256 == 0) {
+    const KsPlan kp = make_ks_plan(p.M, p.N, p.K);
+    if (kp.KS > 0) {
+      p.max_chunks_per_cta = kp.maxc;
+      return p.M <= 2 ? launch_ks<1>(p, kp, s, overlap) : launch_ks<2>(p, kp, s, overlap);
+    }
+  }
   const bool lut_ok = !LUT || (p.lut_block_shift_div == 1 || p.lut_block_shift_div == 2 ||
                                p.lut_block_shift_div % 4 == 0);
   if (p.K % 128 == 0 && lut_ok) {
-    const Plan pa = make_async_plan(p.M, p.N, p.K);
+    const Plan pa = make_async_plan(p.M, p.N, p.K, !LUT && p.M <= 4);
     if (pa.S > 0) {
       p.max_chunks_per_cta = pa.max_chunks;
+      if (!LUT && p.M <= 4) {
+        if (p.M <= 2)
+          return pa.RT == 2 ? launch_gc_typed<1, 2>(p, pa, s, overlap) : launch_gc_typed<1, 1>(p, pa, s, overlap);
+        return pa.RT == 2 ? launch_gc_typed<2, 2>(p, pa, s, overlap) : launch_gc_typed<2, 1>(p, pa, s, overlap);
+      }
       if (pa.MT == 1)
-        return pa.RT == 2 ? launch_async_typed<1, 2, LUT>(p, pa, s) : launch_async_typed<1, 1, LUT>(p, pa, s);
-      return pa.RT == 2 ? launch_async_typed<2, 2, LUT>(p, pa, s) : launch_async_typed<2, 1, LUT>(p, pa, s);
+        return pa.RT == 2 ? launch_async_typed<1, 2, LUT>(p, pa, s, overlap) : launch_async_typed<1, 1, LUT>(p, pa, s, overlap);
+      return pa.RT == 2 ? launch_async_typed<2, 2, LUT>(p, pa, s, overlap) : launch_async_typed<2, 1, LUT>(p, pa, s, overlap);
     }
   }
   const Plan pl = make_plan(p.M, p.N, p.K);
   p.max_chunks_per_cta = pl.max_chunks;
   if (pl.MT == 1) {
-    return pl.RT == 2 ? launch_typed<1, 2, LUT>(p, pl, s) : launch_typed<1, 1, LUT>(p, pl, s);
+    return pl.RT == 2 ? launch_typed<1, 2, LUT>(p, pl, s, overlap) : launch_typed<1, 1, LUT>(p, pl, s, overlap);
   }
-  return pl.RT == 2 ? launch_typed<2, 2, LUT>(p, pl, s) : launch_typed<2, 1, LUT>(p, pl, s);
+  return pl.RT == 2 ? launch_typed<2, 2, LUT>(p, pl, s, overlap) : launch_typed<2, 1, LUT>(p, pl, s, overlap);
 }
 
 }  // namespace
 
 cudaError_t launch_q4_gemv(const uint16_t *x, const uint32_t *w, const uint16_t *scales,
                            const uint16_t *biases, uint16_t *y, int M, int N, int K,
-                           cudaStream_t s) {
+                           cudaStream_t s, bool overlap) {
   GemvParams p{};
   p.x = x;
   p.w = reinterpret_cast<const uint8_t *>(w);
@@ -713,12 +1311,12 @@ cudaError_t launch_q4_gemv(const uint16_t *x, const uint32_t *w, const uint16_t 
   p.biases = biases;
   p.y = y;
   p.M = M; p.N = N; p.K = K;
-  return launch_any<false>(p, s);
+  return launch_any<false>(p, s, overlap);
 }
 
 cudaError_t launch_lut4_gemv(const uint16_t *x, const uint8_t *packed, const float *scales,
                              const float *book, uint16_t *y, int M, int N, int K, int block,
-                             cudaStream_t s) {
+                             cudaStream_t s, bool overlap) {
   GemvParams p{};
   p.x = x;
   p.w = packed;
@@ -729,7 +1327,7 @@ cudaError_t launch_lut4_gemv(const uint16_t *x, const uint8_t *packed, const flo
   p.lut_blocks_per_row = K / block;
   p.lut_block_shift_div = block / 32;
   for (int i = 0; i < 16; ++i) p.book[i] = book[i];
-  return launch_any<true>(p, s);
+  return launch_any<true>(p, s, overlap);
 }
 
 }  // namespace q4mm

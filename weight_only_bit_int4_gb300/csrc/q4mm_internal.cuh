@@ -43,6 +43,15 @@ __device__ __forceinline__ void raise_device_error(unsigned int bit) {
 // Wall-clock limit of every bounded wait in the library (nanoseconds).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel in the stream (if
+// it was launched with programmatic stream serialization) begin launching; wait blocks until
+// every grid this one depends on has completed and its writes are visible.  Both are no-ops
+// for a kernel launched without the attribute.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -181,13 +190,16 @@ __device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t addr) {
 cudaError_t launch_q4_dequant(const uint32_t *w, const uint16_t *scales, const uint16_t *biases,
                               int64_t N, int64_t K, void *out, int out_dtype, cudaStream_t s);
 
+// overlap: launch with programmatic stream serialization, so that the kernel streams its
+// weights while the previous kernel in the stream finishes (the weights must not be written
+// by that kernel); x is read and y written only after the previous kernel has completed.
 cudaError_t launch_q4_gemv(const uint16_t *x, const uint32_t *w, const uint16_t *scales,
                            const uint16_t *biases, uint16_t *y, int M, int N, int K,
-                           cudaStream_t s);
+                           cudaStream_t s, bool overlap = false);
 
 cudaError_t launch_lut4_gemv(const uint16_t *x, const uint8_t *packed, const float *scales,
                              const float *book, uint16_t *y, int M, int N, int K, int block,
-                             cudaStream_t s);
+                             cudaStream_t s, bool overlap = false);
 
 cudaError_t launch_lut4_general(const uint16_t *x, const uint8_t *packed, const float *scales,
                                 const float *book, uint16_t *y, int64_t M, int64_t N,
