@@ -355,8 +355,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
 // ---------------------------------------------------------------------------------------
 constexpr int kDepth = 8;
 constexpr int kStageBytes = 2 * 512 + 2 * 128;
-// Scale-block ring of the M <= 4 kernel: chunk a reads block a/4 while chunk a + kDepth - 1
-// is being fetched, at most (kDepth + 2) / 4 blocks later.
+// Chunk stages per warp of gemv_async_kernel: 16 tokens (MT = 2) stage four times the x of
+// one MMA column tile, and a shallower ring leaves room for more CTAs per SM.
+__host__ __device__ constexpr int async_depth(int MT) { return MT == 2 ? 4 : kDepth; }
+// Scale-block ring: chunk a reads block a/4 while chunk a + depth - 1 is being fetched, at
+// most (depth + 2) / 4 blocks later.
 constexpr int kSbSlots = (kDepth + 2) / 4 + 1;
 constexpr int kSbRow = 80, kSbSlot = 16 * kSbRow;
 
@@ -377,15 +380,22 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // a number of the weight's own size, so one rounding per weight as in the plain dequant.
 // The remainder sum_g c_lo[n][g] * sum_{k in g} x[m][k] is added by one extra MMA per chunk
 // whose k-slot 2t carries (c_lo of lane t's group, that group's x sum).
-template <int MT, int RT, bool LUT>
+// SB (INT4, K % 256 == 0): scales and biases arrive as 4-chunk blocks into a ring of
+// [16 rows][s 32 B | b 32 B | pad], as in gemv_gc_kernel; the code stages then hold codes only.
+template <int MT, int RT, bool LUT, bool SB>
 __global__ void __launch_bounds__(kThreads) gemv_async_kernel(const __grid_constant__ GemvParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int kRowsCta = kWarps * 16 * RT;
   constexpr int kTok = 8 * MT;
-  constexpr int kStage = RT * kStageBytes;
+  static_assert(!(LUT && SB), "scale blocks are INT4 only");
+  constexpr int kD = async_depth(MT);                  // chunk stages per warp
+  constexpr int kSl = (kD + 2) / 4 + 1;                // scale-block slots (SB)
+  constexpr int kStageC = SB ? 1024 : kStageBytes;   // per row tile
+  constexpr int kStage = RT * kStageC;
   const int TS = x_row_stride(p.max_chunks_per_cta);
   uint8_t *ring = smem;
-  uint8_t *xs = smem + kWarps * kDepth * kStage;
+  uint8_t *sbr = smem + kWarps * kD * kStage;                       // SB: [warp][slot][RT]
+  uint8_t *xs = sbr + (SB ? kWarps * kSl * kSbSlot * RT : 0);
   float *red = reinterpret_cast<float *>(xs + (size_t)p.M * TS);      // [kTok][kRowsCta]
   float *book = red + kTok * kRowsCta;                                 // [16]
   uint16_t *xsum = reinterpret_cast<uint16_t *>(book + 16);            // [M][4 * max_chunks]
@@ -433,18 +443,37 @@ __global__ void __launch_bounds__(kThreads) gemv_async_kernel(const __grid_const
       ssrc[rt] = reinterpret_cast<const uint8_t *>(base + (slive[rt] ? (size_t)srow * G : 0) + (size_t)c_begin * 4);
     }
   }
-  const uint32_t ring_warp = smem_u32(ring) + (uint32_t)(warp * kDepth * kStage);
+  const uint32_t ring_warp = smem_u32(ring) + (uint32_t)(warp * kD * kStage);
   const uint32_t sdst_off = 1024u + (uint32_t)(sh * 128 + g * 16 + sk * 8);
 
+  const uint32_t sb_warp = smem_u32(sbr) + (uint32_t)(warp * kSl * kSbSlot * RT);
+  const int blk0 = c_begin / 4;
   auto issue = [&](int c) {
-    const uint32_t slot = ring_warp + (uint32_t)((c % kDepth) * kStage);
+    const uint32_t slot = ring_warp + (uint32_t)((c % kD) * kStage);
+    const int a = c_begin + c;
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt) {
-      const uint32_t sl = slot + rt * kStageBytes;
+      const uint32_t sl = slot + rt * kStageC;
 #pragma unroll
       for (int h = 0; h < 2; ++h)
         cp_async(sl + h * 512 + lane * 16, wsrc[rt][h] + (size_t)c * 64, 16, live[rt][h] ? 16u : 0u);
-      if (scopy) {
+      if constexpr (SB) {
+        if (c == 0 || (a & 3) == 0) {   // block a/4: groups 16(a/4) .. +15, 16 rows, s and b
+          const int b = a >> 2;
+          const uint32_t sslot = sb_warp + (uint32_t)((((b - blk0) % kSl) * RT + rt) * kSbSlot);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int idx = lane + 32 * i;
+            const int r = idx >> 2, ten = (idx >> 1) & 1, half = idx & 1;
+            const int row = row0 + rt * 16 + r;
+            const int g0 = 16 * b + 8 * half;
+            const bool ok = row < p.N && g0 < G;
+            const uint16_t *base = ten ? p.biases : static_cast<const uint16_t *>(p.scales);
+            cp_async(sslot + (uint32_t)(r * kSbRow + ten * 32 + half * 16), base + (ok ? (size_t)row * G + g0 : 0),
+                     16, ok ? 16u : 0u);
+          }
+        }
+      } else if (scopy) {
         const uint8_t *src;
         if constexpr (LUT) {
           src = ssrc[rt] + (size_t)(((c_begin + c) * 4) / p.lut_block_shift_div) * 4;
@@ -457,7 +486,7 @@ __global__ void __launch_bounds__(kThreads) gemv_async_kernel(const __grid_const
   };
 
 #pragma unroll
-  for (int i = 0; i < kDepth - 1; ++i) {
+  for (int i = 0; i < kD - 1; ++i) {
     if (i < nch) issue(i);
     cp_async_commit();
   }
@@ -481,15 +510,15 @@ __global__ void __launch_bounds__(kThreads) gemv_async_kernel(const __grid_const
   bool tok_live[MT];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) tok_live[mt] = g + 8 * mt < p.M;
-  const uint8_t *ring_ptr = ring + warp * kDepth * kStage;
+  const uint8_t *ring_ptr = ring + warp * kD * kStage;
   const int xsum_stride = p.max_chunks_per_cta * 4;
 
   for (int c = 0; c < nch; ++c) {
-    if (c + kDepth - 1 < nch) issue(c + kDepth - 1);
+    if (c + kD - 1 < nch) issue(c + kD - 1);
     cp_async_commit();
-    cp_async_wait<kDepth - 1>();
+    cp_async_wait<kD - 1>();
     __syncwarp();
-    const uint8_t *slot = ring_ptr + (c % kDepth) * kStage;
+    const uint8_t *slot = ring_ptr + (c % kD) * kStage;
     uint4 xb[4][MT];
 #pragma unroll
     for (int q = 0; q < 4; ++q)
@@ -505,7 +534,7 @@ __global__ void __launch_bounds__(kThreads) gemv_async_kernel(const __grid_const
     }
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt) {
-      const uint8_t *sl = slot + rt * kStageBytes;
+      const uint8_t *sl = slot + rt * kStageC;
       uint4 qv[2];
       uint32_t s2[2], c2[2];
       float clo[2];
@@ -519,8 +548,17 @@ __global__ void __launch_bounds__(kThreads) gemv_async_kernel(const __grid_const
           c2[h] = 0;
           clo[h] = 0.f;
         } else {
-          const uint32_t sv = *reinterpret_cast<const uint16_t *>(sc + 2 * t);
-          const uint32_t bv = *reinterpret_cast<const uint16_t *>(sc + 8 + 2 * t);
+          uint32_t sv, bv;
+          if constexpr (SB) {
+            const int a = c_begin + c;
+            const uint8_t *sb = sbr + (size_t)((warp * kSl + ((a >> 2) - blk0) % kSl) * RT + rt) * kSbSlot +
+                                (g + 8 * h) * kSbRow + (a & 3) * 8 + 2 * t;
+            sv = *reinterpret_cast<const uint16_t *>(sb);
+            bv = *reinterpret_cast<const uint16_t *>(sb + 32);
+          } else {
+            sv = *reinterpret_cast<const uint16_t *>(sc + 2 * t);
+            bv = *reinterpret_cast<const uint16_t *>(sc + 8 + 2 * t);
+          }
           const float cf = __fmaf_rn(-128.f, __uint_as_float(sv << 16), __uint_as_float(bv << 16));
           const uint32_t chi = pack_bf16x2(cf, cf);
           clo[h] = cf - __uint_as_float(chi << 16);
@@ -1079,8 +1117,11 @@ cudaError_t launch_typed(const GemvParams &p, const Plan &pl, cudaStream_t s, bo
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-size_t async_smem_bytes(int M, int MT, int RT, int max_chunks) {
-  return (size_t)kWarps * kDepth * kStageBytes * RT + (size_t)M * (max_chunks * 256 + 64) +
+size_t async_smem_bytes(int M, int MT, int RT, int max_chunks, bool sb) {
+  const int d = async_depth(MT), slots = (d + 2) / 4 + 1;
+  const size_t ring = sb ? (size_t)kWarps * (d * 1024 + slots * kSbSlot) * RT
+                         : (size_t)kWarps * d * kStageBytes * RT;
+  return ring + (size_t)M * (max_chunks * 256 + 64) +
          (size_t)8 * MT * kWarps * 16 * RT * 4 + 16 * 4 + (size_t)M * max_chunks * 4 * 2 + 16;
 }
 
@@ -1089,7 +1130,7 @@ size_t async_smem_bytes(int M, int MT, int RT, int max_chunks) {
 size_t gc_smem_bytes(int M, int RT, int max_chunks);
 
 // gc: plan for gemv_gc_kernel (INT4, M <= 4), whose shared-memory footprint differs.
-Plan make_async_plan(int M, int N, int K, bool gc) {
+Plan make_async_plan(int M, int N, int K, bool gc, bool sb) {
   Plan pl{};
   pl.MT = M <= 8 ? 1 : 2;
   const int chunks = K / 128;
@@ -1101,11 +1142,30 @@ Plan make_async_plan(int M, int N, int K, bool gc) {
   double best = -1e30;
   for (int RT = 2; RT >= 1; --RT) {
     const int rb = (N + kWarps * 16 * RT - 1) / (kWarps * 16 * RT);
-    for (int S = 1; S <= std::min(kMaxCluster, chunks); ++S) {
+    for (int S = 1; S <= std::min(kMaxCluster, chunks); S *= 2) {   // clusters of 3, 5, 6, 7 pack poorly
       const int maxc = (chunks + S - 1) / S;
-      const size_t sm = gc ? gc_smem_bytes(M, RT, maxc) : async_smem_bytes(M, pl.MT, RT, maxc);
+      const size_t sm = gc ? gc_smem_bytes(M, RT, maxc) : async_smem_bytes(M, pl.MT, RT, maxc, sb);
       if (sm > 227 * 1024) continue;
       const int per_sm = std::max(1, std::min((int)((228 * 1024) / (sm + 1024)), 8));
+      if (pl.MT == 2 && !gc) {
+        // 16 tokens: staging x caps CTAs per SM, so several waves can beat one.  Cost in
+        // chunk-steps: waves x (chunks per warp x row tiles + per-CTA set-up and cluster
+        // reduction), slowed when fewer than 16 row-tile streams share an SM (fitted to
+        // timings on GB300 over K, N in {4096, 14336}).
+        const long long ctas = (long long)rb * S;
+        const long long waves = (ctas + (long long)sms * per_sm - 1) / ((long long)sms * per_sm);
+        const long long busiest = (ctas + sms - 1) / sms;
+        const double warps = (double)std::min<long long>(per_sm, busiest) * kWarps * RT;
+        const double cost = (double)waves * (maxc * RT + 12.0 + 2.0 * S) / std::min(1.0, warps / 16.0);
+        if (-cost > best) {
+          best = -cost;
+          pl.RT = RT;
+          pl.S = S;
+          pl.max_chunks = maxc;
+          pl.smem = sm;
+        }
+        continue;
+      }
       const long long ctas = (long long)rb * S;
       const long long need = (ctas + sms - 1) / sms;
       if (need > per_sm) continue;                                       // one wave only
@@ -1127,7 +1187,10 @@ Plan make_async_plan(int M, int N, int K, bool gc) {
 
 template <int MT, int RT, bool LUT>
 cudaError_t launch_async_typed(const GemvParams &p, const Plan &pl, cudaStream_t s, bool overlap) {
-  auto kern = gemv_async_kernel<MT, RT, LUT>;
+  auto kern = gemv_async_kernel<MT, RT, LUT, false>;
+  if constexpr (!LUT) {
+    if (p.K % 256 == 0) kern = gemv_async_kernel<MT, RT, false, true>;
+  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1213,8 +1276,9 @@ KsPlan make_ks_plan(int M, int N, int K) {
         const double balance = (double)ctas / (double)(need * sms);
         const double warps = (double)need * KS;                       // on the busiest SM
         const double stages_kb = warps * (depth - 1);                  // code stages in flight
-        double score = balance * std::min(1.0, warps / 16.0) * std::min(1.0, stages_kb / 48.0);
-        score -= (S > 1 ? 0.03 : 0.0) + 0.01 * S;
+        double score = balance * std::min(1.0, warps / 12.0) * std::min(1.0, stages_kb / 48.0);
+        score -= (S > 1 ? 0.15 : 0.0) + 0.01 * S;   // cluster reductions measured 10-20% slower
+        score += depth == 8 ? 0.01 : 0.0;            // deeper rings measured faster at equal occupancy
         if (maxc < 4) score -= 0.04 * (4 - maxc);
         if (score > best_score) {
           best_score = score;
@@ -1278,7 +1342,8 @@ cudaError_t launch_any(GemvParams &p, cudaStream_t s, bool overlap) {
   const bool lut_ok = !LUT || (p.lut_block_shift_div == 1 || p.lut_block_shift_div == 2 ||
                                p.lut_block_shift_div % 4 == 0);
   if (p.K % 128 == 0 && lut_ok) {
-    const Plan pa = make_async_plan(p.M, p.N, p.K, !LUT && p.M <= 4);
+    const bool sb = !LUT && p.K % 256 == 0;
+    const Plan pa = make_async_plan(p.M, p.N, p.K, !LUT && p.M <= 4, sb);
     if (pa.S > 0) {
       p.max_chunks_per_cta = pa.max_chunks;
       if (!LUT && p.M <= 4) {
