@@ -135,8 +135,9 @@ def test_q4_gemv_static_weights_first_link_matches_oracle():
 
 
 # ---------------------------------------------------------------- prefill GEMM (tensor cores)
+# (512, 4096, 256) and (300, 4096, 256) have few 256-token tiles and run 128-token tiles.
 @pytest.mark.parametrize("M,N,K", [(16, 256, 512), (256, 128, 64), (300, 200, 96), (17, 130, 1024),
-                                   (600, 384, 2048), (513, 256, 160)])
+                                   (600, 384, 2048), (513, 256, 160), (512, 4096, 256), (300, 4096, 256)])
 def test_q4_gemm_parity(M, N, K):
     # config-0 data (no outlier columns) at tile-spanning sizes with ragged M, N and K tails;
     # the outlier-column activations of the prefill configuration are checked at its own

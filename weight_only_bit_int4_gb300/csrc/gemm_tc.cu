@@ -319,10 +319,14 @@ constexpr uint32_t kRawBytes = kTileW * 32;          // 4 KB of codes per K bloc
 constexpr uint32_t kScBytes = kTileW * 32;           // 4 KB of scales (or biases) per 8 K blocks
 constexpr int kScKb = 8;                             // K blocks per scale tile
 
+// TT: tokens per tile (MMA N), 256 or 128.  128-token tiles double the tile count for
+// small M, at the price of dequantising each weight tile for half as many tokens.
+template <int TT>
 struct SmemLayoutT {
+  static constexpr uint32_t kB = TT * kBK * 2;                   // x stage bytes
   static constexpr uint32_t a = 0;
   static constexpr uint32_t b = a + kStages * kABytes;
-  static constexpr uint32_t raw = b + kStages * kBBytes;
+  static constexpr uint32_t raw = b + kStages * kB;
   static constexpr uint32_t sc = raw + kStages * kRawBytes;      // [2] scales
   static constexpr uint32_t bi = sc + 2 * kScBytes;              // [2] biases
   // full_a, full_b, full_w, empty, acc_full[2], acc_empty[2], sc_full[2], sc_empty[2]
@@ -331,26 +335,34 @@ struct SmemLayoutT {
   static constexpr uint32_t book = misc + 16;
   static constexpr uint32_t total = book + 16 * 4;
 };
-constexpr size_t kSmemBytesT = SmemLayoutT::total + 1024;
+template <int TT>
+constexpr size_t smem_bytes_t() { return SmemLayoutT<TT>::total + 1024; }
+// warp 0 TMA, warp 1 MMA, warps 2-9 producers (two threads per weight row), warps 10-13
+// epilogue (warp w reads TMEM lanes 32 (w % 4) .. + 31)
+constexpr int kProducersT = 2 * kTileW;
+constexpr int kThreadsT = 64 + kProducersT + 128;
 
 struct TmaMaps {
   CUtensorMap x, w, s, b;
 };
 
-template <bool LUT>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool LUT, int TT>
+__global__ void __launch_bounds__(kThreadsT, 1)
     qgemm_tma_kernel(const __grid_constant__ TmaMaps maps, const __grid_constant__ TcGemmParams p) {
+  using L = SmemLayoutT<TT>;
+  constexpr uint32_t kBBytesT = L::kB;
+  constexpr uint32_t kTmemColsT = 2 * TT;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
   uint8_t *smem = smem_raw + (base - raw_base);
 
-  const uint32_t sA = base + SmemLayoutT::a;
-  const uint32_t sB = base + SmemLayoutT::b;
-  const uint32_t sR = base + SmemLayoutT::raw;
-  const uint32_t sS = base + SmemLayoutT::sc;
-  const uint32_t sBi = base + SmemLayoutT::bi;
-  const uint32_t bar_full_a = base + SmemLayoutT::bars;
+  const uint32_t sA = base + L::a;
+  const uint32_t sB = base + L::b;
+  const uint32_t sR = base + L::raw;
+  const uint32_t sS = base + L::sc;
+  const uint32_t sBi = base + L::bi;
+  const uint32_t bar_full_a = base + L::bars;
   const uint32_t bar_full_b = bar_full_a + kStages * 8;
   const uint32_t bar_full_w = bar_full_b + kStages * 8;
   const uint32_t bar_empty = bar_full_w + kStages * 8;
@@ -358,14 +370,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_acc_empty = bar_acc_full + 2 * 8;     // [2]
   const uint32_t bar_sc_full = bar_acc_empty + 2 * 8;      // [2]
   const uint32_t bar_sc_empty = bar_sc_full + 2 * 8;       // [2]
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SmemLayoutT::misc);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SmemLayoutT::misc + 4);
-  float *book = reinterpret_cast<float *>(smem + SmemLayoutT::book);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::misc + 4);
+  float *book = reinterpret_cast<float *>(smem + L::book);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int KB = p.K / kBK;
   const int SCB = (KB + kScKb - 1) / kScKb;      // scale tiles per weight tile
-  const int m_tiles = (p.M + kTileT - 1) / kTileT;
+  const int m_tiles = (p.M + TT - 1) / TT;
   const int n_tiles = (p.N + kTileW - 1) / kTileW;
   const int T = m_tiles * n_tiles;
   const int my_tiles = (int)blockIdx.x < T ? (T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
@@ -375,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(bar_full_a + 8 * s, 128);
+      tc::mbar_init(bar_full_a + 8 * s, kProducersT);
       tc::mbar_init(bar_full_b + 8 * s, 1);
       tc::mbar_init(bar_full_w + 8 * s, 1);
       tc::mbar_init(bar_empty + 8 * s, 1);
@@ -384,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(bar_acc_full + 8 * b, 1);
       tc::mbar_init(bar_acc_empty + 8 * b, 4);
       tc::mbar_init(bar_sc_full + 8 * b, 1);
-      tc::mbar_init(bar_sc_empty + 8 * b, 128);
+      tc::mbar_init(bar_sc_empty + 8 * b, kProducersT);
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -395,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (LUT && threadIdx.x < 16) book[threadIdx.x] = p.book[threadIdx.x];
   if (warp == 1) {
-    tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tc::tmem_alloc(smem_u32(tmem_slot), kTmemColsT);
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
@@ -411,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < steps && ok; ++j) {
         const int i = j / KB, kb = j - i * KB;
         const int t = tile_of(i);
-        const int m0 = (t % m_tiles) * kTileT;
+        const int m0 = (t % m_tiles) * TT;
         const int n0 = (t / m_tiles) * kTileW;
         if (kb % kScKb == 0) {
           const int q = i * SCB + kb / kScKb;              // scale tile counter
@@ -431,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag)) break;
         tc::mbar_arrive_expect_tx(bar_full_w + 8 * s, kRawBytes);
         tc::tma_load_2d(sR + s * kRawBytes, &maps.w, kb * 32, n0, bar_full_w + 8 * s);
-        tc::mbar_arrive_expect_tx(bar_full_b + 8 * s, kBBytes);
-        tc::tma_load_2d(sB + s * kBBytes, &maps.x, kb * kBK, m0, bar_full_b + 8 * s);
+        tc::mbar_arrive_expect_tx(bar_full_b + 8 * s, kBBytesT);
+        tc::tma_load_2d(sB + s * kBBytesT, &maps.x, kb * kBK, m0, bar_full_b + 8 * s);
         ++issued;
       }
       if (*abort_flag) {
@@ -451,14 +463,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(kTileW, kTileT);
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kTileW, TT);
       bool ok = true;
       for (int i = 0; i < my_tiles && ok; ++i) {
         const int ab = i & 1;
         ok = tc::mbar_wait(bar_acc_empty + 8 * ab, ((i >> 1) & 1) ^ 1, abort_flag);
         if (!ok) break;
         tc::tc_fence_after();
-        const uint32_t dtm = tmem + (uint32_t)(ab * kTileT);
+        const uint32_t dtm = tmem + (uint32_t)(ab * TT);
         for (int kb = 0; kb < KB; ++kb) {
           const int j = i * KB + kb;
           const int s = j % kStages;
@@ -468,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc::tc_fence_after();
           const uint64_t ad = tc::smem_desc_sw128(sA + s * kABytes);
-          const uint64_t bd = tc::smem_desc_sw128(sB + s * kBBytes);
+          const uint64_t bd = tc::smem_desc_sw128(sB + s * kBBytesT);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
             tc::mma_bf16(dtm, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
@@ -477,12 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) tc::mma_commit(bar_acc_full + 8 * ab);
       }
     }
-  } else if (warp < 6) {
-    // ---------------- dequant producers (one weight row per thread) ----------------
+  } else if (warp < 2 + kProducersT / 32) {
+    // ---------------- dequant producers: half a weight row (32 k) per thread ----------------
     const int tp = threadIdx.x - 64;
-    const uint8_t *raw_row = smem + SmemLayoutT::raw + tp * 32;
-    const uint8_t *sc_row = smem + SmemLayoutT::sc + tp * 32;
-    const uint8_t *bi_row = smem + SmemLayoutT::bi + tp * 32;
+    const int row = tp & (kTileW - 1), half = tp / kTileW;
+    const uint8_t *raw_row = smem + L::raw + row * 32 + half * 16;
+    const uint8_t *sc_row = smem + L::sc + row * 32;
+    const uint8_t *bi_row = smem + L::bi + row * 32;
     for (int j = 0; j < steps; ++j) {
       const int i = j / KB, kb = j - i * KB;
       const int q = i * SCB + kb / kScKb, slot = q & 1;
@@ -492,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!tc::mbar_wait(bar_full_w + 8 * s, ph, abort_flag, 100)) break;
       RawKb r;
       r.q0 = *reinterpret_cast<const uint4 *>(raw_row + s * kRawBytes);
-      r.q1 = *reinterpret_cast<const uint4 *>(raw_row + s * kRawBytes + 16);
+      r.q1 = r.q0;
       const int kk = kb % kScKb;
       if constexpr (LUT) {
         r.s = *reinterpret_cast<const uint32_t *>(sc_row + slot * kScBytes + 4 * (kk / p.lut_kb_per_block));
@@ -501,12 +514,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         r.s = *reinterpret_cast<const uint32_t *>(sc_row + slot * kScBytes + 4 * kk);
         r.b = *reinterpret_cast<const uint32_t *>(bi_row + slot * kScBytes + 4 * kk);
       }
-      uint8_t *a_tile = smem + SmemLayoutT::a + s * kABytes;
-      const uint32_t words[8] = {r.q0.x, r.q0.y, r.q0.z, r.q0.w, r.q1.x, r.q1.y, r.q1.z, r.q1.w};
+      uint8_t *a_tile = smem + L::a + s * kABytes;
+      const uint32_t words[4] = {r.q0.x, r.q0.y, r.q0.z, r.q0.w};
+      if (half == 0) {
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4 *>(a_tile + tc::sw128_offset((uint32_t)tp, (uint32_t)c)) =
-            decode_chunk<LUT>(words[c], c, r, book);
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4 *>(a_tile + tc::sw128_offset((uint32_t)row, (uint32_t)c)) =
+              decode_chunk<LUT>(words[c], c, r, book);
+      } else {
+#pragma unroll
+        for (int c = 4; c < 8; ++c)
+          *reinterpret_cast<uint4 *>(a_tile + tc::sw128_offset((uint32_t)row, (uint32_t)c)) =
+              decode_chunk<LUT>(words[c - 4], c, r, book);
+      }
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(bar_full_a + 8 * s);
       if (kk == kScKb - 1 || kb == KB - 1) tc::mbar_arrive(bar_sc_empty + 8 * slot);
@@ -519,12 +539,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!tc::mbar_wait(bar_acc_full + 8 * ab, (i >> 1) & 1, abort_flag)) break;
       tc::tc_fence_after();
       const int t = tile_of(i);
-      const int m0 = (t % m_tiles) * kTileT;
+      const int m0 = (t % m_tiles) * TT;
       const int n = (t / m_tiles) * kTileW + quarter * 32 + lane;
-      for (int c0 = 0; c0 < kTileT; c0 += 32) {
+      for (int c0 = 0; c0 < TT; c0 += 32) {
         if (m0 + c0 >= p.M) break;
         uint32_t v[32];
-        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * kTileT + c0), v);
+        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * TT + c0), v);
         tc::tmem_ld_wait();
         if (n < p.N) {
 #pragma unroll
@@ -547,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, kTmemCols);
+    tc::tmem_dealloc(tmem, kTmemColsT);
   }
 }
 
@@ -592,19 +612,46 @@ cudaError_t make_plain_map(CUtensorMap *map, const void *base, CUtensorMapDataTy
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-unsigned persistent_grid(const TcGemmParams &p) {
+int sm_count() {
   int sms = 148, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long tiles = (long long)((p.N + kTileW - 1) / kTileW) * ((p.M + kTileT - 1) / kTileT);
+  return sms;
+}
+
+unsigned persistent_grid(const TcGemmParams &p, int tt = kTileT) {
+  const int sms = sm_count();
+  const long long tiles = (long long)((p.N + kTileW - 1) / kTileW) * ((p.M + tt - 1) / tt);
   return (unsigned)(tiles < sms ? tiles : sms);
+}
+
+// Tokens per tile.  The dequantising producers bound a tile's time, so a 128-token tile
+// costs about 7/8 of a 256-token one (measured on GB300); 128 is taken when its waves of
+// tiles finish sooner: 7 * waves(128) < 8 * waves(256).
+int pick_token_tile(const TcGemmParams &p) {
+  const int sms = sm_count();
+  auto waves = [&](int tt) {
+    const long long t = (long long)((p.N + kTileW - 1) / kTileW) * ((p.M + tt - 1) / tt);
+    return (t + sms - 1) / sms;
+  };
+  return 7 * waves(128) < 8 * waves(256) ? 128 : 256;
+}
+
+template <bool LUT, int TT>
+cudaError_t launch_tma_typed(const TmaMaps &maps, const TcGemmParams &q, cudaStream_t s) {
+  auto kern = qgemm_tma_kernel<LUT, TT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes_t<TT>());
+  if (e != cudaSuccess) return e;
+  kern<<<persistent_grid(q, TT), kThreadsT, smem_bytes_t<TT>(), s>>>(maps, q);
+  return cudaGetLastError();
 }
 
 template <bool LUT>
 cudaError_t launch_tc(const TcGemmParams &p, const void *x, cudaStream_t s) {
   const bool tma_path = p.K % 256 == 0 && (!LUT || p.lut_kb_per_block == 1 || p.lut_kb_per_block == 2);
   if (tma_path) {
+    const int tt = pick_token_tile(p);
     TmaMaps maps;
-    cudaError_t e = make_x_map(&maps.x, x, p.M, p.K, kTileT);
+    cudaError_t e = make_x_map(&maps.x, x, p.M, p.K, tt);
     if (e == cudaSuccess)
       e = make_plain_map(&maps.w, p.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.K / 2, p.N, 32, kTileW);
     if (LUT) {
@@ -615,22 +662,14 @@ cudaError_t launch_tc(const TcGemmParams &p, const void *x, cudaStream_t s) {
                            q.lut_sc_box, kTileW);
       maps.b = maps.s;
       if (e != cudaSuccess) return e;
-      auto kern = qgemm_tma_kernel<true>;
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesT);
-      if (e != cudaSuccess) return e;
-      kern<<<persistent_grid(q), kThreads, kSmemBytesT, s>>>(maps, q);
-      return cudaGetLastError();
+      return tt == 128 ? launch_tma_typed<true, 128>(maps, q, s) : launch_tma_typed<true, 256>(maps, q, s);
     }
     if (e == cudaSuccess)
       e = make_plain_map(&maps.s, p.scales, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.K / 32, p.N, 16, kTileW);
     if (e == cudaSuccess)
       e = make_plain_map(&maps.b, p.biases, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.K / 32, p.N, 16, kTileW);
     if (e != cudaSuccess) return e;
-    auto kern = qgemm_tma_kernel<false>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesT);
-    if (e != cudaSuccess) return e;
-    kern<<<persistent_grid(p), kThreads, kSmemBytesT, s>>>(maps, p);
-    return cudaGetLastError();
+    return tt == 128 ? launch_tma_typed<false, 128>(maps, p, s) : launch_tma_typed<false, 256>(maps, p, s);
   }
   CUtensorMap map;
   cudaError_t e = make_x_map(&map, x, p.M, p.K, kTileT);
