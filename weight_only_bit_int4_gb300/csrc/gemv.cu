@@ -904,8 +904,9 @@ __global__ void __launch_bounds__(KS * 32) gemv_ks_kernel(const __grid_constant_
     }
   };
 
+  // Chunks go through the loop in pairs; DEPTH - 2 chunks are in flight ahead of a pair.
 #pragma unroll
-  for (int i = 0; i < DEPTH - 1; ++i) {
+  for (int i = 0; i < DEPTH - 2; ++i) {
     if (i < nch) issue(i);
     cp_async_commit();
   }
@@ -955,11 +956,7 @@ __global__ void __launch_bounds__(KS * 32) gemv_ks_kernel(const __grid_constant_
 #pragma unroll
   for (int u = 0; u < MT2; ++u) acc[u][0] = acc[u][1] = 0.f;
 
-  for (int c = 0; c < nch; ++c) {
-    if (c + DEPTH - 1 < nch) issue(c + DEPTH - 1);
-    cp_async_commit();
-    cp_async_wait<DEPTH - 1>();
-    __syncwarp();
+  auto process = [&](int c) {
     const uint8_t *sl = ring + (c % DEPTH) * 1024;
     uint4 xb[4][MT2];
     float2 X[MT2];
@@ -1013,7 +1010,23 @@ __global__ void __launch_bounds__(KS * 32) gemv_ks_kernel(const __grid_constant_
         acc[u][h] = v;
       }
     }
+  };
+  int c = 0;
+  for (; c + 1 < nch; c += 2) {
+    if (c + DEPTH - 2 < nch) issue(c + DEPTH - 2);
+    cp_async_commit();
+    if (c + DEPTH - 1 < nch) issue(c + DEPTH - 1);
+    cp_async_commit();
+    cp_async_wait<DEPTH - 2>();
     __syncwarp();
+    process(c);
+    process(c + 1);
+    __syncwarp();
+  }
+  if (c < nch) {   // odd chunk count: the last chunk alone
+    cp_async_wait<0>();
+    __syncwarp();
+    process(c);
   }
   cp_async_wait<0>();
 
@@ -1256,7 +1269,7 @@ KsPlan make_ks_plan(int M, int N, int K) {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
   }
   const int R = (N + 15) / 16, C = K / 128;
-  const int regs = M <= 2 ? 48 : 80;    // per thread, as compiled (ptxas -v)
+  const int regs = M <= 2 ? 72 : 96;    // per thread, at least what ptxas -v reports
   double best_score = -1e30;
   for (int depth : {4, 8})
     for (int KS : {2, 4, 8})
