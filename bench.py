@@ -311,13 +311,13 @@ def run_ours(args, rank, world, local_rank):
         "decode_shapes": shape_rows,
     }
     t_h, by_h = headline
-    out["roofline"] = {"bound": "hbm", "kernel": "gemv_async_kernel (q4_gemv_ex, static weights)",
+    out["roofline"] = {"bound": "hbm", "kernel": "gemv_ks_kernel (q4_gemv_ex, static weights)",
                        "shape": {"M": HEADLINE[0], "K": HEADLINE[1], "N": HEADLINE[2]},
                        "achieved": round(by_h / t_h / 1e9, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                        "frac": round(by_h / t_h / 1e9 / pk["hbm_gbs"], 3),
                        "frac_vs_8TBs": round(by_h / t_h / 8e12, 3),
                        "peak_source": pk["source"] + " (hbm_gbs, burst copy)",
-                       "traffic": profiled_traffic("gemv_async_kernel_q4_gemv_M1_K4096_N14336.md"),
+                       "traffic": profiled_traffic("gemv_ks_kernel_q4_gemv_M1_K4096_N14336.md"),
                        "algorithmic_bytes_per_launch": by_h}
 
     # ---------------- e2e through the public API with host buffers ----------------

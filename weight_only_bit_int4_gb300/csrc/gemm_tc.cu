@@ -496,19 +496,19 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     const uint8_t *raw_row = smem + L::raw + row * 32 + half * 16;
     const uint8_t *sc_row = smem + L::sc + row * 32;
     const uint8_t *bi_row = smem + L::bi + row * 32;
+    // Step j = i * KB + kb walks (tile i, K block kb); scale tile q = i * SCB + kb / kScKb.
+    // Counters advance incrementally (no divisions per stage).
+    int kb = 0, kk = 0, q = 0, s = 0;
+    uint32_t ph = 0;
     for (int j = 0; j < steps; ++j) {
-      const int i = j / KB, kb = j - i * KB;
-      const int q = i * SCB + kb / kScKb, slot = q & 1;
-      if (kb % kScKb == 0 && !tc::mbar_wait(bar_sc_full + 8 * slot, (q >> 1) & 1, abort_flag, 100)) break;
-      const int s = j % kStages;
-      const uint32_t ph = (j / kStages) & 1;
+      const int slot = q & 1;
+      if (kk == 0 && !tc::mbar_wait(bar_sc_full + 8 * slot, (q >> 1) & 1, abort_flag, 100)) break;
       if (!tc::mbar_wait(bar_full_w + 8 * s, ph, abort_flag, 100)) break;
       RawKb r;
       r.q0 = *reinterpret_cast<const uint4 *>(raw_row + s * kRawBytes);
       r.q1 = r.q0;
-      const int kk = kb % kScKb;
       if constexpr (LUT) {
-        r.s = *reinterpret_cast<const uint32_t *>(sc_row + slot * kScBytes + 4 * (kk / p.lut_kb_per_block));
+        r.s = *reinterpret_cast<const uint32_t *>(sc_row + slot * kScBytes + 4 * (kk >> (p.lut_kb_per_block - 1)));
         r.b = 0;
       } else {
         r.s = *reinterpret_cast<const uint32_t *>(sc_row + slot * kScBytes + 4 * kk);
@@ -530,6 +530,12 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(bar_full_a + 8 * s);
       if (kk == kScKb - 1 || kb == KB - 1) tc::mbar_arrive(bar_sc_empty + 8 * slot);
+      if (++s == kStages) { s = 0; ph ^= 1u; }
+      if (++kb == KB) {          // next tile: its scale tiles start a new group
+        kb = 0; kk = 0; ++q;
+      } else if (++kk == kScKb) {
+        kk = 0; ++q;
+      }
     }
   } else {
     // ---------------- epilogue: TMEM -> bf16 y ----------------
