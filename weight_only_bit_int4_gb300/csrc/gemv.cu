@@ -371,9 +371,6 @@ __device__ __forceinline__ void cp_async(uint32_t dst, const void *src, int byte
   else
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // INT4 weights enter the MMA as fma(128 + q, s, c_hi) in bf16, where c = b - 128 s (exact
 // in fp32) splits as c_hi + c_lo, c_hi = bf16(c): the rounded value is that of q*s + b - c_lo,

@@ -438,6 +438,173 @@ cudaError_t launch_q4_0_route(const uint32_t *ids, int n_rows, int n_experts, ui
   return launch_route_internal(ids, n_rows, n_experts, htpe, nullptr, hids, n_invalid, s);
 }
 
+// ---------------------------------------------------------------------------------------
+// Mat-vec form on the tensor cores (K % 256 == 0, 16-byte aligned expert slabs).
+//
+// A CTA owns routed row r = token * top_k + slot and 16 weight rows of expert ids[r]; its
+// KS warps take consecutive K slices.  Each warp streams its slice as chunks of 8 Q4_0
+// blocks per row (144 bytes, 16-byte aligned because K % 256 == 0) through a private
+// cp.async ring, and stages its slice of x rounded to bf16 together with the per-block sums
+// of those bf16 values.
+//
+// The product follows the M <= 4 INT4 decode kernel: with one token, B column j of an
+// m16n8k16 step carries x on the k-slots of Q4_0 block j (j < 4) and zeros elsewhere, so
+// the tensor core forms D = sum (128 + q) * x per (row, block) exactly; the codes enter as
+// bf16 128 + q with one LOP3.  Then, in fp32,
+//     sum_k (q - 8) d x_k = d * D - 136 * d * X,   X = sum of the block's bf16 x,
+// which is the block's contribution with its terms regrouped.  Word m of a block's qs
+// holds elements 4m..4m+3 (low nibbles) and 4m+16..4m+19 (high nibbles); the decode pairs
+// are (4m, 4m+2), (4m+16, 4m+18), (4m+1, 4m+3), (4m+17, 4m+19) and x is staged in that order.
+// ---------------------------------------------------------------------------------------
+constexpr int kMvcDepth = 4;                   // chunk stages per warp
+constexpr int kMvcRow = 144;                   // bytes per weight row per chunk (8 blocks)
+constexpr int kMvcChunk = 16 * kMvcRow;        // 2304 bytes per chunk stage
+
+__host__ __device__ inline size_t mvc_warp_bytes(int maxc) {
+  return (size_t)kMvcDepth * kMvcChunk + (size_t)maxc * 8 * 64 + (size_t)maxc * 8 * 4;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+template <int KS>
+__global__ void __launch_bounds__(KS * 32) q4_0_mv_mma_kernel(const __grid_constant__ MvParams p, int maxc) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int g = lane / 4, t = lane % 4;
+  const size_t wb = mvc_warp_bytes(maxc);
+  uint8_t *ring = smem + (size_t)warp * wb;
+  uint8_t *xs = ring + kMvcDepth * kMvcChunk;                          // [maxc * 8 blocks][4][16 B]
+  float *xsum = reinterpret_cast<float *>(xs + (size_t)maxc * 8 * 64);  // [maxc * 8]
+  float *red = reinterpret_cast<float *>(smem + (size_t)KS * wb);       // [KS][16]
+  const uint32_t ring_s = smem_u32(ring);
+  const int C = p.K / 256;
+  const int c_begin = (int)(((long long)warp * C) / KS);
+  const int c_end = (int)(((long long)(warp + 1) * C) / KS);
+  const int nch = c_end - c_begin;
+  const int row0 = blockIdx.x * 16;
+  const size_t row_bytes = (size_t)(p.K / 32) * 18;
+
+  for (int r = blockIdx.y; r < p.n_rows; r += gridDim.y) {
+    const uint32_t e = __ldg(p.ids + r);
+    if (e >= (uint32_t)p.E) {   // routed to no expert: zero row, and record it
+      if (threadIdx.x < 16 && row0 + (int)threadIdx.x < p.N) p.out[(size_t)r * p.N + row0 + threadIdx.x] = 0.f;
+      if (threadIdx.x == 0 && blockIdx.x == 0) raise_device_error(Q4MM_DEVERR_BAD_EXPERT);
+      continue;
+    }
+    const uint8_t *wexp = p.w + (size_t)e * p.expert_stride;
+    auto issue = [&](int c) {
+      const uint32_t slot = ring_s + (uint32_t)((c % kMvcDepth) * kMvcChunk);
+      const size_t col0 = (size_t)(c_begin + c) * kMvcRow;
+      for (int i = lane; i < 16 * 9; i += 32) {   // 16 rows x 9 pieces of 16 bytes
+        const int rr = i / 9, pc = i - rr * 9;
+        const int grow = row0 + rr;
+        const bool ok = grow < p.N;
+        cp_async16(slot + (uint32_t)(rr * kMvcRow + pc * 16), wexp + (ok ? (size_t)grow * row_bytes + col0 + pc * 16 : 0),
+                   ok ? 16u : 0u);
+      }
+    };
+#pragma unroll
+    for (int i = 0; i < kMvcDepth - 1; ++i) {
+      if (i < nch) issue(i);
+      cp_async_commit();
+    }
+
+    // x slice: item (block, m) -> 16 bytes of bf16 pairs in decode order; block sums.
+    const float *xr = p.x + (size_t)(r / p.top_k) * p.K + (size_t)c_begin * 256;
+    for (int it = lane; it < nch * 8 * 4; it += 32) {   // 4 consecutive lanes share a block
+      const int blk = it >> 2, m = it & 3;
+      const float4 lo = __ldg(reinterpret_cast<const float4 *>(xr + blk * 32 + 4 * m));
+      const float4 hi = __ldg(reinterpret_cast<const float4 *>(xr + blk * 32 + 16 + 4 * m));
+      const uint32_t p0 = pack_bf16x2(lo.x, lo.z), p1 = pack_bf16x2(hi.x, hi.z);
+      const uint32_t p2 = pack_bf16x2(lo.y, lo.w), p3 = pack_bf16x2(hi.y, hi.w);
+      *reinterpret_cast<uint4 *>(xs + (size_t)blk * 64 + m * 16) = make_uint4(p0, p1, p2, p3);
+      float sum = 0.f;
+      const uint32_t pv[4] = {p0, p2, p1, p3};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sum += __uint_as_float(pv[i] << 16) + __uint_as_float(pv[i] & 0xFFFF0000u);
+      sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+      sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+      if (m == 0) xsum[blk] = sum;
+    }
+    __syncwarp();
+
+    const bool bl = g == t;   // B column g = block g of the sub-chunk (one token: g < 4)
+    float acc[2] = {0.f, 0.f};
+    for (int c = 0; c < nch; ++c) {
+      if (c + kMvcDepth - 1 < nch) issue(c + kMvcDepth - 1);
+      cp_async_commit();
+      cp_async_wait<kMvcDepth - 1>();
+      __syncwarp();
+      const uint8_t *slot = ring + (c % kMvcDepth) * kMvcChunk;
+#pragma unroll
+      for (int sc = 0; sc < 2; ++sc) {   // sub-chunks of 4 blocks; quad lane t decodes block 4 sc + t
+        const int bk = 4 * sc + t;
+        const int off = 18 * bk + 2;                    // qs of block bk within a row
+        const uint32_t sel = (off & 2) ? 0x5432u : 0x3210u;
+        uint32_t qs[2][4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t *u = reinterpret_cast<const uint32_t *>(slot + (g + 8 * h) * kMvcRow + (off & ~3));
+          uint32_t v[5];
+#pragma unroll
+          for (int i = 0; i < 5; ++i) v[i] = u[i];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) qs[h][i] = prmt(v[i], v[i + 1], sel);
+        }
+        uint4 xb[4];
+        const uint8_t *xl = xs + (size_t)(c * 8 + bk) * 64;
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          xb[m] = bl ? *reinterpret_cast<const uint4 *>(xl + m * 16) : make_uint4(0, 0, 0, 0);
+        float D[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const uint32_t w0 = qs[0][m], w1 = qs[1][m];
+          constexpr uint32_t kMask = 0x000F000Fu, kMagic = 0x43004300u;   // bf16 128 + q
+          const uint32_t a0[4] = {and_or(w0, kMask, kMagic), and_or(w1, kMask, kMagic),
+                                  and_or(w0 >> 4, kMask, kMagic), and_or(w1 >> 4, kMask, kMagic)};
+          const uint32_t a1[4] = {and_or(w0 >> 8, kMask, kMagic), and_or(w1 >> 8, kMask, kMagic),
+                                  and_or(w0 >> 12, kMask, kMagic), and_or(w1 >> 12, kMask, kMagic)};
+          mma_bf16_16816(D, a0, xb[m].x, xb[m].y);
+          mma_bf16_16816(D, a1, xb[m].z, xb[m].w);
+        }
+        // columns 2t, 2t+1 = blocks 4 sc + 2t, +1 for t < 2; zero columns for t >= 2
+        const int ba = 4 * sc + 2 * (t & 1);
+        const float2 X = *reinterpret_cast<const float2 *>(xsum + c * 8 + ba);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint8_t *rowp = slot + (g + 8 * h) * kMvcRow;
+          const float da = f16_bits_to_float(*reinterpret_cast<const uint16_t *>(rowp + 18 * ba));
+          const float db = f16_bits_to_float(*reinterpret_cast<const uint16_t *>(rowp + 18 * (ba + 1)));
+          float a = acc[h];
+          a = __fmaf_rn(da, D[2 * h], a);
+          a = __fmaf_rn(-136.f * da, X.x, a);
+          a = __fmaf_rn(db, D[2 * h + 1], a);
+          a = __fmaf_rn(-136.f * db, X.y, a);
+          acc[h] = t < 2 ? a : 0.f;
+        }
+      }
+      __syncwarp();
+    }
+    cp_async_wait<0>();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float v = acc[h] + __shfl_xor_sync(0xFFFFFFFFu, acc[h], 1);
+      if (t == 0) red[warp * 16 + g + 8 * h] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < 16) {
+      float v = red[threadIdx.x];
+#pragma unroll
+      for (int w = 1; w < KS; ++w) v += red[w * 16 + threadIdx.x];
+      if (row0 + (int)threadIdx.x < p.N) p.out[(size_t)r * p.N + row0 + threadIdx.x] = v;
+    }
+    __syncthreads();   // ring, x and red are reused by the next routed row
+  }
+}
+
 cudaError_t launch_q4_0_mv(const float *x, const uint8_t *w, const uint32_t *ids, float *out,
                            int n_tokens, int top_k, int N, int K, int n_experts,
                            uint64_t expert_stride, cudaStream_t s) {
@@ -445,6 +612,20 @@ cudaError_t launch_q4_0_mv(const float *x, const uint8_t *w, const uint32_t *ids
   p.x = x; p.w = w; p.ids = ids; p.order = nullptr; p.n_order = nullptr; p.out = out;
   p.n_rows = n_tokens * top_k; p.top_k = top_k; p.N = N; p.K = K; p.E = n_experts;
   p.expert_stride = expert_stride;
+  if (K % 256 == 0 && expert_stride % 16 == 0 && (reinterpret_cast<uintptr_t>(w) & 15) == 0) {
+    const int C = K / 256;
+    const int ks = C >= 4 ? 4 : (C >= 2 ? 2 : 1);
+    const int maxc = (C + ks - 1) / ks;
+    const size_t smem = (size_t)ks * mvc_warp_bytes(maxc) + (size_t)ks * 16 * 4;
+    if (smem <= 227 * 1024) {
+      dim3 grid((unsigned)((N + 15) / 16), (unsigned)(p.n_rows < 65535 ? p.n_rows : 65535), 1);
+      auto kern = ks == 4 ? q4_0_mv_mma_kernel<4> : ks == 2 ? q4_0_mv_mma_kernel<2> : q4_0_mv_mma_kernel<1>;
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      kern<<<grid, ks * 32, smem, s>>>(p, maxc);
+      return cudaGetLastError();
+    }
+  }
   const int rows_cta = kMvWarps * kMvRowsPerWarp;
   dim3 grid((unsigned)((N + rows_cta - 1) / rows_cta), (unsigned)(p.n_rows < 65535 ? p.n_rows : 65535), 1);
   q4_0_mv_kernel<<<grid, kMvWarps * 32, 0, s>>>(p);
