@@ -75,21 +75,27 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-// Four nibbles (lo or hi halves of four qs bytes) as (q - 8) * d in fp16, natural-order
-// pairs.  (code | 0x6400) is the fp16 value 1024 + q; subtracting 1032 gives q - 8 exactly.
-__device__ __forceinline__ uint2 q4_0_pairs(uint32_t word, bool hi, uint32_t d2) {
+// K order inside every 32-element Q4_0 block, shared by the decoded weight tile and the
+// gathered x rows: 16-byte chunk m (m = 0..3) holds elements
+//   4m, 4m+2, 4m+1, 4m+3, 4m+16, 4m+18, 4m+17, 4m+19,
+// which are the pairs that qs word m (bytes 4m..4m+3; low nibbles 4m.., high nibbles
+// 4m+16..) yields with one mask each.  A dot product is indifferent to the order of k as
+// long as both operands use the same one.
+//
+// qs word m as one 16-byte chunk of (q - 8) * d in fp16.  (code | 0x6400) is the fp16 value
+// 1024 + q; subtracting 1032 gives q - 8 exactly, and the product with d is rounded once.
+__device__ __forceinline__ uint4 q4_0_chunk(uint32_t word, uint32_t d2) {
   constexpr uint32_t kMask = 0x000F000Fu, kMagic = 0x64006400u, kOff = 0x64086408u;   // 1024, 1032
-  uint32_t t01 = prmt(word, 0u, 0x4140u), t23 = prmt(word, 0u, 0x4342u);
-  if (hi) {
-    t01 >>= 4;
-    t23 >>= 4;
+  const uint32_t c[4] = {and_or(word, kMask, kMagic), and_or(word >> 8, kMask, kMagic),
+                         and_or(word >> 4, kMask, kMagic), and_or(word >> 12, kMask, kMagic)};
+  uint32_t r[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t q;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(q) : "r"(c[i]), "r"(kOff));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r[i]) : "r"(q), "r"(d2));
   }
-  uint32_t q01, q23, r01, r23;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(q01) : "r"(and_or(t01, kMask, kMagic)), "r"(kOff));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(q23) : "r"(and_or(t23, kMask, kMagic)), "r"(kOff));
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r01) : "r"(q01), "r"(d2));
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r23) : "r"(q23), "r"(d2));
-  return make_uint2(r01, r23);
+  return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -269,14 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, 100)) { ok = false; break; }
         uint8_t *a_tile = smem + SmemL::a + s * kABytes;
 #pragma unroll
-        for (int sub = 0; sub < 4; ++sub) {
-          const bool hi = sub >= 2;
-          const int wq = 2 * (sub & 1);
-          const uint2 p0 = q4_0_pairs(qs[wq], hi, d2);
-          const uint2 p1 = q4_0_pairs(qs[wq + 1], hi, d2);
-          *reinterpret_cast<uint4 *>(a_tile + tc::sw128_offset((uint32_t)tp, (uint32_t)(4 * half + sub))) =
-              make_uint4(p0.x, p0.y, p1.x, p1.y);
-        }
+        for (int m = 0; m < 4; ++m)
+          *reinterpret_cast<uint4 *>(a_tile + tc::sw128_offset((uint32_t)tp, (uint32_t)(4 * half + m))) =
+              q4_0_chunk(qs[m], d2);
         tc::fence_proxy_async_smem();
         tc::mbar_arrive(bar_full_a + 8 * s);
       }
@@ -316,24 +317,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// xs[p] = fp16(x[hids[p] / top_k]) for p < number of valid routed rows.
+// xs[p] = fp16(x[hids[p] / top_k]) for p < number of valid routed rows, each 32-element
+// block laid out in the chunk order of q4_0_chunk.  Item = (row, block, chunk m): two float4
+// loads (elements 4m.. and 16+4m..) and one 16-byte store.  A CTA takes four rows at a time,
+// so each thread has four items' loads in flight.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const float *__restrict__ x, const int32_t *__restrict__ hids,
                                                           const uint32_t *__restrict__ n_valid, int top_k, int K,
                                                           uint16_t *__restrict__ xs, int n_rows) {
-  const int nv = (int)*n_valid;
-  for (int pos = blockIdx.x; pos < nv && pos < n_rows; pos += gridDim.x) {
-    const float4 *src = reinterpret_cast<const float4 *>(x + (size_t)(hids[pos] / top_k) * K);
-    uint2 *dst = reinterpret_cast<uint2 *>(xs + (size_t)pos * K);
-    bool out_of_range = false;
-    for (int k4 = threadIdx.x; k4 < K / 4; k4 += blockDim.x) {
-      const float4 f = __ldg(src + k4);
-      const float m = fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w)));
-      out_of_range |= !(m <= 65504.f);
-      __half2 h01 = __floats2half2_rn(f.x, f.y), h23 = __floats2half2_rn(f.z, f.w);
-      dst[k4] = make_uint2(*reinterpret_cast<uint32_t *>(&h01), *reinterpret_cast<uint32_t *>(&h23));
+  const int nv = min((int)*n_valid, n_rows);
+  const int per_row = K / 8;   // items per row: K / 32 blocks x 4 chunks
+  bool out_of_range = false;
+  for (int pos0 = blockIdx.x * 4; pos0 < nv; pos0 += gridDim.x * 4) {
+    const float *src[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) src[u] = pos0 + u < nv ? x + (size_t)(hids[pos0 + u] / top_k) * K : nullptr;
+    for (int i = threadIdx.x; i < per_row; i += blockDim.x) {
+      const int off = (i >> 2) * 32 + 4 * (i & 3);
+      float4 lo[4], hi[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (src[u] != nullptr) {
+          lo[u] = __ldg(reinterpret_cast<const float4 *>(src[u] + off));
+          hi[u] = __ldg(reinterpret_cast<const float4 *>(src[u] + off + 16));
+        }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (src[u] != nullptr) {
+          const float4 a = lo[u], b = hi[u];
+          const float mx = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                                 fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+          out_of_range |= !(mx <= 65504.f);
+          __half2 h0 = __floats2half2_rn(a.x, a.z), h1 = __floats2half2_rn(a.y, a.w);
+          __half2 h2 = __floats2half2_rn(b.x, b.z), h3 = __floats2half2_rn(b.y, b.w);
+          *reinterpret_cast<uint4 *>(xs + (size_t)(pos0 + u) * K + (size_t)i * 8) =
+              make_uint4(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
+                         *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
+        }
     }
-    if (out_of_range) raise_device_error(Q4MM_DEVERR_F16_RANGE);
   }
+  if (out_of_range) raise_device_error(Q4MM_DEVERR_F16_RANGE);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -364,8 +386,7 @@ cudaError_t launch_q4_0_mm_tc(const float *x, const uint8_t *w, float *out, int 
   int sms = 148, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
 
-  gather_rows_kernel<<<(unsigned)(n_rows < 4 * sms ? n_rows : 4 * sms), 256, 0, s>>>(x, hids, offs + n_experts, top_k,
-                                                                                    K, xs, n_rows);
+  gather_rows_kernel<<<(unsigned)(4 * sms), 256, 0, s>>>(x, hids, offs + n_experts, top_k, K, xs, n_rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
