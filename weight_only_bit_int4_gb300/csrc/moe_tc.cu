@@ -157,16 +157,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int raw_issued = 0;
       const int boxes_per_item = KB / 4;
+      // The item's expert and row tile are read once per item, and the next item's block
+      // entry is loaded one item ahead, so no global load sits between two box issues.
+      int i = 0, bq = 0;
+      int4 cur = my_items > 0 ? p.blk[item_of(0) / n_tiles] : make_int4(0, 0, 0, 0);
+      int4 nxt = my_items > 1 ? p.blk[item_of(1) / n_tiles] : cur;
       for (int q = 0; q < my_items * boxes_per_item; ++q) {
-        const int i = q / boxes_per_item, bq = q - i * boxes_per_item;
+        if (bq == boxes_per_item) {
+          bq = 0;
+          ++i;
+          cur = nxt;
+          if (i + 1 < my_items) nxt = p.blk[item_of(i + 1) / n_tiles];
+        }
         const int w = item_of(i);
-        const int e = p.blk[w / n_tiles].x;
+        const int e = cur.x;
         const int n0 = (w % n_tiles) * kTW;
         const int slot = q % kRawSlots;
         if (!tc::mbar_wait(bar_raw_empty + 8 * slot, ((q / kRawSlots) & 1) ^ 1, abort_flag)) break;
         tc::mbar_arrive_expect_tx(bar_raw_full + 8 * slot, kRawBytes);
         tma_load_3d(sR + slot * kRawBytes, &maps.w, bq * (int)kRawRow, n0, e, bar_raw_full + 8 * slot);
         ++raw_issued;
+        ++bq;
       }
       if (*abort_flag) {
         for (int q = (raw_issued > kRawSlots ? raw_issued - kRawSlots : 0); q < raw_issued; ++q) {
@@ -179,13 +190,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- x TMA: the block's gathered rows, every K block ----------------
     if (lane == 0) {
       int issued = 0;
-      int cur_i = -1;
-      int4 bi = make_int4(0, 0, 0, 0);
-      for (int j = 0; j < steps; ++j) {
-        const int i = j / KB, kb = j - i * KB;
-        if (i != cur_i) {
-          cur_i = i;
-          bi = p.blk[item_of(i) / n_tiles];
+      int i = 0, kb = 0;
+      int4 bi = my_items > 0 ? p.blk[item_of(0) / n_tiles] : make_int4(0, 0, 0, 0);
+      int4 bnext = my_items > 1 ? p.blk[item_of(1) / n_tiles] : bi;   // one item ahead
+      for (int j = 0; j < steps; ++j, ++kb) {
+        if (kb == KB) {
+          kb = 0;
+          ++i;
+          bi = bnext;
+          if (i + 1 < my_items) bnext = p.blk[item_of(i + 1) / n_tiles];
         }
         const int s = j % kStages;
         const uint32_t ph = (j / kStages) & 1;
@@ -208,9 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       bool ok = true;
+      int cnt_next = my_items > 0 ? p.blk[item_of(0) / n_tiles].z : 0;   // one item ahead
       for (int i = 0; i < my_items && ok; ++i) {
         const int ab = i & 1;
-        const int cnt = p.blk[item_of(i) / n_tiles].z;
+        const int cnt = cnt_next;
+        if (i + 1 < my_items) cnt_next = p.blk[item_of(i + 1) / n_tiles].z;
         const uint32_t idesc = tc::idesc_f16_f32(kTW, ((cnt + 15) / 16) * 16);
         ok = tc::mbar_wait(bar_acc_empty + 8 * ab, ((i >> 1) & 1) ^ 1, abort_flag);
         if (!ok) break;
