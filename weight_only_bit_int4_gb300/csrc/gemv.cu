@@ -1052,6 +1052,219 @@ __global__ void __launch_bounds__(KS * 32) gemv_ks_kernel(const __grid_constant_
   if (gridDim.y > 1) cluster_sum_store<16>(p, red);
 }
 
+// ---------------------------------------------------------------------------------------
+// LUT4, 1 <= M <= 4, K % 512 == 0, block in {32, 64, 128}: the K-split kernel with a
+// codebook decode.  Byte j of a row holds elements 2j (high nibble) and 2j+1 (low nibble),
+// so one byte is one bf16 pair in natural k order: the CTA builds a table of the 256 pairs
+// (bf16(book[hi]), bf16(book[lo])), replicated 16 times so that the 32 lanes of a lookup
+// fall on distinct banks except for lanes l and l+16, and each code byte costs one byte
+// extract, one address multiply-add and one shared load.  x is staged in natural order.
+// The block scales (f32, one per `block` consecutive k) arrive in 4-chunk blocks like the
+// INT4 scales, and the group-column product applies them after the tensor core:
+// sum_k book[q_k] s x_k = s * sum_k bf16(book[q_k]) x_k per group (LUT4 has no bias).
+// ---------------------------------------------------------------------------------------
+constexpr int kLutCopies = 16;
+constexpr int kLutTableBytes = 256 * kLutCopies * 4;   // 16 KB
+
+__host__ __device__ constexpr int lks_sb_slots(int depth) { return (depth + 2) / 4 + 1; }
+__host__ __device__ inline int lks_row_pitch(int block) { return 2048 / block + 16; }   // scale bytes + pad
+__host__ __device__ inline size_t lks_warp_bytes(int depth, int M, int maxc, int block) {
+  return (size_t)depth * 1024 + (size_t)lks_sb_slots(depth) * 16 * lks_row_pitch(block) +
+         (size_t)M * (maxc * 256 + 64);
+}
+
+template <int MT2, int KS, int DEPTH>
+__global__ void __launch_bounds__(KS * 32) gemv_lks_kernel(const __grid_constant__ GemvParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int kSlots = lks_sb_slots(DEPTH);
+  const int block = p.lut_block_shift_div * 32;
+  const int P = lks_row_pitch(block);
+  const int maxc = p.max_chunks_per_cta;
+  const int XS = maxc * 256 + 64;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int g = lane / 4, t = lane % 4;
+  uint32_t *ltab = reinterpret_cast<uint32_t *>(smem);
+  const size_t wbytes = lks_warp_bytes(DEPTH, p.M, maxc, block);
+  uint8_t *wbase = smem + kLutTableBytes + (size_t)warp * wbytes;
+  uint8_t *ring = wbase;
+  uint8_t *sbr = wbase + DEPTH * 1024;
+  uint8_t *xs = sbr + kSlots * 16 * P;
+  float *red = reinterpret_cast<float *>(smem + kLutTableBytes + (size_t)KS * wbytes);   // [KS][M][16]
+
+  const int splits = (int)gridDim.y * KS;
+  const int sp = (int)blockIdx.y * KS + warp;
+  const int c_begin = (int)(((long long)sp * p.chunks) / splits);
+  const int c_end = (int)(((long long)(sp + 1) * p.chunks) / splits);
+  const int nch = c_end - c_begin;
+  const int row0 = blockIdx.x * 16;
+  const int spr = p.lut_blocks_per_row;            // scales per row
+  const int sblk = 512 / block;                    // scales per 4-chunk block
+  const int cpr = 128 / block;                     // 16-byte copies per row per 4-chunk block
+
+  const uint8_t *wsrc[2];
+  bool live[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int row = row0 + g + 8 * h;
+    live[h] = row < p.N;
+    wsrc[h] = p.w + (live[h] ? (size_t)row * (size_t)(p.K / 2) : 0) + (size_t)c_begin * 64 + t * 16;
+  }
+  const uint32_t ring_s = smem_u32(ring), sb_s = smem_u32(sbr);
+  const int blk0 = c_begin / 4;
+  const float *scales = static_cast<const float *>(p.scales);
+  auto issue = [&](int c) {
+    const uint32_t slot = ring_s + (uint32_t)((c % DEPTH) * 1024);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      cp_async(slot + h * 512 + lane * 16, wsrc[h] + (size_t)c * 64, 16, live[h] ? 16u : 0u);
+    const int a = c_begin + c;
+    if (c == 0 || (a & 3) == 0) {   // scales of chunks 4(a/4) .. +3, 16 rows
+      const int b = a >> 2;
+      const uint32_t sslot = sb_s + (uint32_t)(((b - blk0) % kSlots) * 16 * P);
+      for (int i = lane; i < 16 * cpr; i += 32) {
+        const int r = i / cpr, pc = i - r * cpr;
+        const int row = row0 + r;
+        const bool ok = row < p.N;
+        cp_async(sslot + (uint32_t)(r * P + pc * 16), scales + (ok ? (size_t)row * spr + (size_t)b * sblk + pc * 4 : 0),
+                 16, ok ? 16u : 0u);
+      }
+    }
+  };
+
+  // Pair table: entry (byte, copy) at ltab[byte * 16 + copy].
+  for (int i = threadIdx.x; i < 256 * kLutCopies; i += KS * 32) {
+    const int byte = i / kLutCopies;
+    ltab[i] = pack_bf16x2(p.book[byte >> 4], p.book[byte & 15]);
+  }
+  // Chunks go through the loop in pairs; DEPTH - 2 chunks are in flight ahead of a pair.
+#pragma unroll
+  for (int i = 0; i < DEPTH - 2; ++i) {
+    if (i < nch) issue(i);
+    cp_async_commit();
+  }
+  // Weights are in flight; x may be the previous kernel's output, and y may still be read by it.
+  griddep_launch_dependents();
+  griddep_wait();
+  for (int it = lane; it < p.M * nch * 16; it += 32) {   // this warp's x slice, 16 bytes a piece
+    const int tok = it / (nch * 16), rem = it - tok * (nch * 16);
+    *reinterpret_cast<uint4 *>(xs + (size_t)tok * XS + rem * 16) =
+        __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)tok * p.K + (size_t)c_begin * 128) + rem);
+  }
+  __syncthreads();   // the table is shared by the CTA; x and rings are per warp
+
+  bool bl[MT2], al[MT2];
+  const uint8_t *xl[MT2];
+#pragma unroll
+  for (int u = 0; u < MT2; ++u) {
+    const int tb = 2 * u + g / 4;
+    bl[u] = (g & 3) == t && tb < p.M;
+    xl[u] = xs + (size_t)(bl[u] ? tb : 0) * XS + t * 64;
+    al[u] = 2 * u + t / 2 < p.M;
+  }
+  const uint32_t tab_lane = smem_u32(ltab) + (uint32_t)(lane & (kLutCopies - 1)) * 4u;
+  float acc[MT2][2];
+#pragma unroll
+  for (int u = 0; u < MT2; ++u) acc[u][0] = acc[u][1] = 0.f;
+
+  auto process = [&](int c) {
+    const uint8_t *sl = ring + (c % DEPTH) * 1024;
+    uint4 xb[4][MT2];
+#pragma unroll
+    for (int u = 0; u < MT2; ++u)
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        xb[q][u] = bl[u] ? *reinterpret_cast<const uint4 *>(xl[u] + c * 256 + q * 16) : make_uint4(0, 0, 0, 0);
+    const uint4 q0 = *reinterpret_cast<const uint4 *>(sl + lane * 16);
+    const uint4 q1 = *reinterpret_cast<const uint4 *>(sl + 512 + lane * 16);
+    const int a = c_begin + c;
+    const uint8_t *sc = sbr + ((a >> 2) - blk0) % kSlots * 16 * P;
+    // groups 2(t&1), 2(t&1)+1 of this chunk -> scale indices within the 4-chunk block
+    const int ga = (a & 3) * 4 + 2 * (t & 1);
+    const int ia = (ga * 32) / block, ib = ((ga + 1) * 32) / block;
+    float sa[2], sbv[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float *srow = reinterpret_cast<const float *>(sc + (g + 8 * h) * P);
+      sa[h] = srow[ia];
+      sbv[h] = srow[ib];
+    }
+    float D[MT2][4];
+#pragma unroll
+    for (int u = 0; u < MT2; ++u) D[u][0] = D[u][1] = D[u][2] = D[u][3] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t w0 = q == 0 ? q0.x : q == 1 ? q0.y : q == 2 ? q0.z : q0.w;
+      const uint32_t w1 = q == 0 ? q1.x : q == 1 ? q1.y : q == 2 ? q1.z : q1.w;
+      uint32_t v[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t sel = 0x4440u | (uint32_t)j;   // byte j, zero-extended
+        const uint32_t b0 = prmt(w0, 0u, sel), b1 = prmt(w1, 0u, sel);
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v[2 * j]) : "r"(tab_lane + b0 * (kLutCopies * 4u)));
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v[2 * j + 1]) : "r"(tab_lane + b1 * (kLutCopies * 4u)));
+      }
+      // step 2q: k-slots (2t, 2t+1) <- byte 4q, (2t+8, 2t+9) <- byte 4q+1; step 2q+1: bytes 4q+2, 4q+3
+      const uint32_t a0[4] = {v[0], v[1], v[2], v[3]};
+      const uint32_t a1[4] = {v[4], v[5], v[6], v[7]};
+#pragma unroll
+      for (int u = 0; u < MT2; ++u) {
+        mma_bf16_16816(D[u], a0, xb[q][u].x, xb[q][u].y);
+        mma_bf16_16816(D[u], a1, xb[q][u].z, xb[q][u].w);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int u = 0; u < MT2; ++u) {
+        float v = acc[u][h];
+        v = __fmaf_rn(sa[h], D[u][2 * h], v);
+        v = __fmaf_rn(sbv[h], D[u][2 * h + 1], v);
+        acc[u][h] = v;
+      }
+  };
+  int c = 0;
+  for (; c + 1 < nch; c += 2) {
+    if (c + DEPTH - 2 < nch) issue(c + DEPTH - 2);
+    cp_async_commit();
+    if (c + DEPTH - 1 < nch) issue(c + DEPTH - 1);
+    cp_async_commit();
+    cp_async_wait<DEPTH - 2>();
+    __syncwarp();
+    process(c);
+    process(c + 1);
+    __syncwarp();
+  }
+  if (c < nch) {
+    cp_async_wait<0>();
+    __syncwarp();
+    process(c);
+  }
+  cp_async_wait<0>();
+
+#pragma unroll
+  for (int u = 0; u < MT2; ++u)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float v = acc[u][h] + __shfl_xor_sync(0xFFFFFFFFu, acc[u][h], 1);
+      if ((t & 1) == 0 && al[u]) red[(warp * p.M + 2 * u + t / 2) * 16 + g + 8 * h] = v;
+    }
+  __syncthreads();
+  for (int i = threadIdx.x; i < p.M * 16; i += KS * 32) {
+    float v = red[i];
+#pragma unroll
+    for (int w = 1; w < KS; ++w) v += red[w * p.M * 16 + i];
+    red[i] = v;
+    if (gridDim.y == 1) {
+      const int row = row0 + (i & 15);
+      if (row < p.N) {
+        __nv_bfloat16 hb = __float2bfloat16_rn(v);
+        p.y[(size_t)(i >> 4) * p.N + row] = *reinterpret_cast<uint16_t *>(&hb);
+      }
+    }
+  }
+  if (gridDim.y > 1) cluster_sum_store<16>(p, red);
+}
+
 struct Plan {
   int MT, RT, S, max_chunks;
   size_t smem;
@@ -1339,9 +1552,101 @@ cudaError_t launch_ks(const GemvParams &p, const KsPlan &pl, cudaStream_t s, boo
   return launch_ks_typed<MT2, 8, 8>(p, pl, s, overlap);
 }
 
+// Plans for gemv_lks_kernel: the K-split plan search with the codebook table in each CTA.
+KsPlan make_lks_plan(int M, int N, int K, int block) {
+  KsPlan best;
+  int sms = 152, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
+  }
+  const int R = (N + 15) / 16, C = K / 128;
+  const int regs = M <= 2 ? 80 : 104;   // at least what ptxas -v reports
+  double best_score = -1e30;
+  for (int depth : {4, 8})
+    for (int KS : {2, 4, 8})
+      for (int S : {1, 2, 4, 8}) {
+        if (KS * S > C) continue;
+        const int maxc = (C + KS * S - 1) / (KS * S);
+        const size_t smem = (size_t)kLutTableBytes + (size_t)KS * lks_warp_bytes(depth, M, maxc, block) +
+                            (size_t)KS * M * 16 * 4;
+        if (smem > 227 * 1024) continue;
+        int per_sm = (int)((228 * 1024) / (smem + 1024));
+        per_sm = std::min(per_sm, 2048 / (KS * 32));
+        per_sm = std::min(per_sm, 65536 / (KS * 32 * regs));
+        per_sm = std::min(per_sm, 32);
+        if (per_sm < 1) continue;
+        const long long ctas = (long long)R * S;
+        const long long need = (ctas + sms - 1) / sms;
+        if (need > per_sm) continue;
+        const double balance = (double)ctas / (double)(need * sms);
+        const double warps = (double)need * KS;
+        const double stages_kb = warps * (depth - 1);
+        double score = balance * std::min(1.0, warps / 12.0) * std::min(1.0, stages_kb / 48.0);
+        score -= (S > 1 ? 0.15 : 0.0) + 0.01 * S;
+        score += depth == 8 ? 0.01 : 0.0;
+        if (maxc < 4) score -= 0.04 * (4 - maxc);
+        if (score > best_score) {
+          best_score = score;
+          best.KS = KS; best.S = S; best.depth = depth; best.maxc = maxc; best.smem = smem;
+        }
+      }
+  return best;
+}
+
+template <int MT2, int KS, int DEPTH>
+cudaError_t launch_lks_typed(const GemvParams &p, const KsPlan &pl, cudaStream_t s, bool overlap) {
+  auto kern = gemv_lks_kernel<MT2, KS, DEPTH>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((p.N + 15) / 16), (unsigned)pl.S, 1);
+  cfg.blockDim = dim3(KS * 32, 1, 1);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pl.S > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 1;
+    attr[n].val.clusterDim.y = (unsigned)pl.S;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (overlap) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = (unsigned)n;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int MT2>
+cudaError_t launch_lks(const GemvParams &p, const KsPlan &pl, cudaStream_t s, bool overlap) {
+  if (pl.depth == 4) {
+    if (pl.KS == 2) return launch_lks_typed<MT2, 2, 4>(p, pl, s, overlap);
+    if (pl.KS == 4) return launch_lks_typed<MT2, 4, 4>(p, pl, s, overlap);
+    return launch_lks_typed<MT2, 8, 4>(p, pl, s, overlap);
+  }
+  if (pl.KS == 2) return launch_lks_typed<MT2, 2, 8>(p, pl, s, overlap);
+  if (pl.KS == 4) return launch_lks_typed<MT2, 4, 8>(p, pl, s, overlap);
+  return launch_lks_typed<MT2, 8, 8>(p, pl, s, overlap);
+}
+
 template <bool LUT>
 cudaError_t launch_any(GemvParams &p, cudaStream_t s, bool overlap) {
   p.chunks = (p.K / 32 + 3) / 4;
+  if (LUT && p.M <= 4 && p.K % 512 == 0 &&
+      (p.lut_block_shift_div == 1 || p.lut_block_shift_div == 2 || p.lut_block_shift_div == 4) &&
+      (reinterpret_cast<uintptr_t>(p.scales) & 15u) == 0) {
+    const KsPlan kp = make_lks_plan(p.M, p.N, p.K, p.lut_block_shift_div * 32);
+    if (kp.KS > 0) {
+      p.max_chunks_per_cta = kp.maxc;
+      return p.M <= 2 ? launch_lks<1>(p, kp, s, overlap) : launch_lks<2>(p, kp, s, overlap);
+    }
+  }
   if (!LUT && p.M <= 4 && p.K % 256 == 0) {
     const KsPlan kp = make_ks_plan(p.M, p.N, p.K);
     if (kp.KS > 0) {
