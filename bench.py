@@ -58,6 +58,20 @@ def profiled_traffic(summary: str):
         return None
 
 
+def max_over_ranks(seconds: float, device) -> float:
+    """The slowest rank's time: every rank's timed region ends when the last one's does."""
+    import torch
+    t = torch.tensor([seconds], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_step: int, steps: int, world: int, seconds: float) -> float:
+    """Whole-job GB/s: every rank (an independent replica) processes bytes_per_step each
+    step, and the job takes the slowest rank's time."""
+    return bytes_per_step * steps * world / seconds / 1e9
+
+
 def decode_shapes():
     return [(M, K, N) for (K, N) in DECODE_KN for M in DECODE_M]
 
@@ -269,9 +283,7 @@ def run_ours(args, rank, world, local_rank):
     elapsed = e0.elapsed_time(e1) / 1e3
     if world > 1:
         torch.distributed.barrier()
-        t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed = float(t.item())
+        elapsed = max_over_ranks(elapsed, dev)
     # per-shape and headline-kernel timings (same run, same clock sampling)
     shape_rows = []
     headline = None
@@ -293,7 +305,7 @@ def run_ours(args, rank, world, local_rank):
             headline = (t, by)
     clocks = sampler.stop()
 
-    value = step_bytes * args.steps * world / elapsed / 1e9
+    value = job_throughput(step_bytes, args.steps, world, elapsed)
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
