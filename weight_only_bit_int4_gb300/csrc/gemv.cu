@@ -482,8 +482,9 @@ __global__ void __launch_bounds__(kThreads) gemv_async_kernel(const __grid_const
     }
   };
 
+  // Chunks go through the loop in pairs; kD - 2 chunks are in flight ahead of a pair.
 #pragma unroll
-  for (int i = 0; i < kD - 1; ++i) {
+  for (int i = 0; i < kD - 2; ++i) {
     if (i < nch) issue(i);
     cp_async_commit();
   }
@@ -510,11 +511,7 @@ __global__ void __launch_bounds__(kThreads) gemv_async_kernel(const __grid_const
   const uint8_t *ring_ptr = ring + warp * kD * kStage;
   const int xsum_stride = p.max_chunks_per_cta * 4;
 
-  for (int c = 0; c < nch; ++c) {
-    if (c + kD - 1 < nch) issue(c + kD - 1);
-    cp_async_commit();
-    cp_async_wait<kD - 1>();
-    __syncwarp();
+  auto process = [&](int c) {
     const uint8_t *slot = ring_ptr + (c % kD) * kStage;
     uint4 xb[4][MT];
 #pragma unroll
@@ -597,7 +594,23 @@ __global__ void __launch_bounds__(kThreads) gemv_async_kernel(const __grid_const
         for (int mt = 0; mt < MT; ++mt) mma_bf16_16816(acc[rt][mt], ac, xs_b[mt], 0u);
       }
     }
+  };
+  int c = 0;
+  for (; c + 1 < nch; c += 2) {
+    if (c + kD - 2 < nch) issue(c + kD - 2);
+    cp_async_commit();
+    if (c + kD - 1 < nch) issue(c + kD - 1);
+    cp_async_commit();
+    cp_async_wait<kD - 2>();
     __syncwarp();
+    process(c);
+    process(c + 1);
+    __syncwarp();
+  }
+  if (c < nch) {   // odd chunk count: the last chunk alone
+    cp_async_wait<0>();
+    __syncwarp();
+    process(c);
   }
   cp_async_wait<0>();
   cluster_reduce_store<MT, RT>(p, red, acc, warp, g, t);
