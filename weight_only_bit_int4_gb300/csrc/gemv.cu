@@ -717,8 +717,9 @@ __global__ void __launch_bounds__(kThreads) gemv_gc_kernel(const __grid_constant
     }
   };
 
+  // Chunks go through the loop in pairs; kDepth - 2 chunks are in flight ahead of a pair.
 #pragma unroll
-  for (int i = 0; i < kDepth - 1; ++i) {
+  for (int i = 0; i < kDepth - 2; ++i) {
     if (i < nch) issue(i);
     cp_async_commit();
   }
@@ -754,11 +755,7 @@ __global__ void __launch_bounds__(kThreads) gemv_gc_kernel(const __grid_constant
     for (int u = 0; u < MT2; ++u) acc[rt][u][0] = acc[rt][u][1] = 0.f;
   const uint8_t *ring_ptr = ring + warp * kDepth * kStage;
 
-  for (int c = 0; c < nch; ++c) {
-    if (c + kDepth - 1 < nch) issue(c + kDepth - 1);
-    cp_async_commit();
-    cp_async_wait<kDepth - 1>();
-    __syncwarp();
+  auto process = [&](int c) {
     const uint8_t *slot = ring_ptr + (c % kDepth) * kStage;
     uint4 xb[4][MT2];
     float2 X[MT2];
@@ -823,7 +820,23 @@ __global__ void __launch_bounds__(kThreads) gemv_gc_kernel(const __grid_constant
         }
       }
     }
+  };
+  int c = 0;
+  for (; c + 1 < nch; c += 2) {
+    if (c + kDepth - 2 < nch) issue(c + kDepth - 2);
+    cp_async_commit();
+    if (c + kDepth - 1 < nch) issue(c + kDepth - 1);
+    cp_async_commit();
+    cp_async_wait<kDepth - 2>();
     __syncwarp();
+    process(c);
+    process(c + 1);
+    __syncwarp();
+  }
+  if (c < nch) {   // odd chunk count: the last chunk alone
+    cp_async_wait<0>();
+    __syncwarp();
+    process(c);
   }
   cp_async_wait<0>();
 
