@@ -979,21 +979,49 @@ __global__ void __launch_bounds__(KS * 32) gemv_ks_kernel(const __grid_constant_
 #pragma unroll
   for (int u = 0; u < MT2; ++u) acc[u][0] = acc[u][1] = 0.f;
 
-  auto process = [&](int c) {
-    const uint8_t *sl = ring + (c % DEPTH) * 1024;
-    uint4 xb[4][MT2];
-    float2 X[MT2];
+  // Scale-block read cursor: slot of chunk c's block and c's position in it, advanced per
+  // processed chunk (chunks are processed in order).
+  int rd_slot = 0, rd_pos = c_begin & 3;
+  // B fragments and group sums of the two chunks of a pair.  With one token tile, lanes
+  // that carry no x keep them at zero for the whole loop and only the carrying lanes load
+  // (no per-chunk selects); with two tiles that would cost too many registers, so the
+  // fragments are rebuilt per chunk.
+  uint4 xbuf[2][4][MT2];
+  float2 Xbuf[2][MT2];
+#pragma unroll
+  for (int pi = 0; pi < 2; ++pi)
 #pragma unroll
     for (int u = 0; u < MT2; ++u) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        xb[q][u] = bl[u] ? *reinterpret_cast<const uint4 *>(xl[u] + c * 256 + q * 64) : make_uint4(0, 0, 0, 0);
-      X[u] = al[u] ? *reinterpret_cast<const float2 *>(xsl[u] + c * 4) : make_float2(0.f, 0.f);
+      for (int q = 0; q < 4; ++q) xbuf[pi][q][u] = make_uint4(0, 0, 0, 0);
+      Xbuf[pi][u] = make_float2(0.f, 0.f);
+    }
+  auto process = [&](int c, int pi) {
+    const uint8_t *sl = ring + (c % DEPTH) * 1024;
+    uint4 (&xb)[4][MT2] = xbuf[pi];
+    float2 (&X)[MT2] = Xbuf[pi];
+#pragma unroll
+    for (int u = 0; u < MT2; ++u) {
+      if constexpr (MT2 == 1) {
+        if (bl[u]) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) xb[q][u] = *reinterpret_cast<const uint4 *>(xl[u] + c * 256 + q * 64);
+        }
+        if (al[u]) X[u] = *reinterpret_cast<const float2 *>(xsl[u] + c * 4);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          xb[q][u] = bl[u] ? *reinterpret_cast<const uint4 *>(xl[u] + c * 256 + q * 64) : make_uint4(0, 0, 0, 0);
+        X[u] = al[u] ? *reinterpret_cast<const float2 *>(xsl[u] + c * 4) : make_float2(0.f, 0.f);
+      }
     }
     const uint4 q0 = *reinterpret_cast<const uint4 *>(sl + lane * 16);
     const uint4 q1 = *reinterpret_cast<const uint4 *>(sl + 512 + lane * 16);
-    const int a = c_begin + c;
-    const uint8_t *sc = sbr + ((a >> 2) - blk0) % kSlots * kSbSlot + g * kSbRow + (a & 3) * 8 + 4 * (t & 1);
+    const uint8_t *sc = sbr + rd_slot * kSbSlot + g * kSbRow + rd_pos * 8 + 4 * (t & 1);
+    if (++rd_pos == 4) {
+      rd_pos = 0;
+      rd_slot = rd_slot + 1 == kSlots ? 0 : rd_slot + 1;
+    }
     uint32_t su[2], bu[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -1042,14 +1070,14 @@ __global__ void __launch_bounds__(KS * 32) gemv_ks_kernel(const __grid_constant_
     cp_async_commit();
     cp_async_wait<DEPTH - 2>();
     __syncwarp();
-    process(c);
-    process(c + 1);
+    process(c, 0);
+    process(c + 1, 1);
     __syncwarp();
   }
   if (c < nch) {   // odd chunk count: the last chunk alone
     cp_async_wait<0>();
     __syncwarp();
-    process(c);
+    process(c, 0);
   }
   cp_async_wait<0>();
 
@@ -1505,7 +1533,7 @@ KsPlan make_ks_plan(int M, int N, int K) {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
   }
   const int R = (N + 15) / 16, C = K / 128;
-  const int regs = M <= 2 ? 72 : 96;    // per thread, at least what ptxas -v reports
+  const int regs = M <= 2 ? 80 : 104;   // per thread, at least what ptxas -v reports
   double best_score = -1e30;
   for (int depth : {4, 8})
     for (int KS : {2, 4, 8})

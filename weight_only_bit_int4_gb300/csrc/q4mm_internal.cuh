@@ -147,9 +147,11 @@ __device__ __forceinline__ Int4Pairs int4_word_to_bf16_pairs(uint32_t word, uint
 // Warp-level tensor-core MMA (m16n8k16, bf16 inputs, fp32 accumulate) for the small-M
 // decode kernels, where the weight fragment is built in registers straight from HBM.
 // --------------------------------------------------------------------------------------
+// Not volatile: the MMA has no effect beyond its outputs, so the compiler may interleave
+// independent accumulation chains (e.g. two chunks processed together).
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
                                                uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
