@@ -135,9 +135,12 @@ def test_q4_gemv_static_weights_first_link_matches_oracle():
 
 
 # ---------------------------------------------------------------- prefill GEMM (tensor cores)
-# (512, 4096, 256) and (300, 4096, 256) have few 256-token tiles and run 128-token tiles.
+# (512, 4096, 256) and (300, 4096, 256) have few 256-token tiles and run 128-token tiles;
+# (512, 1024, 2048) and (300, 512, 4096) split K over a cluster (S = 4 with 128-token tiles,
+# S = 8 with a ragged token tile) and sum the partial tiles in distributed shared memory.
 @pytest.mark.parametrize("M,N,K", [(16, 256, 512), (256, 128, 64), (300, 200, 96), (17, 130, 1024),
-                                   (600, 384, 2048), (513, 256, 160), (512, 4096, 256), (300, 4096, 256)])
+                                   (600, 384, 2048), (513, 256, 160), (512, 4096, 256), (300, 4096, 256),
+                                   (512, 1024, 2048), (300, 512, 4096)])
 def test_q4_gemm_parity(M, N, K):
     # config-0 data (no outlier columns) at tile-spanning sizes with ragged M, N and K tails;
     # the outlier-column activations of the prefill configuration are checked at its own
@@ -150,7 +153,8 @@ def test_q4_gemm_parity(M, N, K):
     assert q.device_errors() == 0
 
 
-@pytest.mark.parametrize("M,K,N", [(512, 4096, 14336), (2048, 14336, 4096), (8192, 4096, 6144)])
+@pytest.mark.parametrize("M,K,N", [(512, 4096, 14336), (2048, 14336, 4096), (8192, 4096, 6144),
+                                   (512, 14336, 4096)])
 def test_q4_gemm_full_size_sampled(M, K, N):
     x, w, s, b = _case(2000 + M, M, N, K, outliers=0.01)
     y = poisoned_bf16(M, N)

@@ -27,7 +27,7 @@ def _case(seed, M, N, K, block=64, transpose=1):
 @pytest.mark.parametrize("M,N,K,block", [(1, 256, 512, 64), (16, 200, 96, 32), (5, 130, 1024, 128),
                                          (512, 256, 512, 64), (40, 300, 640, 64), (129, 128, 256, 64),
                                          (3, 130, 1024, 128), (2, 200, 2048, 32), (4, 1000, 512, 64),
-                                         (1, 72, 4096, 128), (2, 4104, 1024, 64)])
+                                         (1, 72, 4096, 128), (2, 4104, 1024, 64), (300, 512, 2048, 64)])
 def test_lut4_fast_paths(M, N, K, block):
     x, packed, scales, book = _case(60 + M, M, N, K, block)
     ref = oracle.lut4_matmul(x, packed, scales, book, M, N, K, block, 1)

@@ -54,6 +54,8 @@ struct TcGemmParams {
   int lut_blocks_per_row;  // LUT4: K / block
   int lut_kb_per_block;    // LUT4: block / 64
   int lut_sc_box;          // LUT4 TMA path: f32 scales per 8 K blocks (8 for block 64, 4 for 128)
+  int ksplit;              // TMA path: 1 = persistent tiles; S > 1 = each tile's K split over a
+                           // cluster of S CTAs (K / 64 a multiple of 8 S), partials summed in DSMEM
   float book[16];
 };
 
@@ -346,7 +348,7 @@ struct TmaMaps {
   CUtensorMap x, w, s, b;
 };
 
-template <bool LUT, int TT>
+template <bool LUT, int TT, bool SPLIT>
 __global__ void __launch_bounds__(kThreadsT, 1)
     qgemm_tma_kernel(const __grid_constant__ TmaMaps maps, const __grid_constant__ TcGemmParams p) {
   using L = SmemLayoutT<TT>;
@@ -375,14 +377,18 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   float *book = reinterpret_cast<float *>(smem + L::book);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int KB = p.K / kBK;
-  const int SCB = (KB + kScKb - 1) / kScKb;      // scale tiles per weight tile
+  // Split mode (ksplit = S > 1): CTA b of the grid owns tile b / S and K blocks
+  // [kb_base, kb_base + KB) of it, kb_base = rank * KB; K-block coordinates add kb_base.
+  const int S = SPLIT ? p.ksplit : 1;
+  const int KB = p.K / kBK / S;
+  const int kb_base = SPLIT ? (int)cluster_ctarank() * KB : 0;
+  const int SCB = (KB + kScKb - 1) / kScKb;      // scale tiles per weight tile (or split)
   const int m_tiles = (p.M + TT - 1) / TT;
   const int n_tiles = (p.N + kTileW - 1) / kTileW;
   const int T = m_tiles * n_tiles;
-  const int my_tiles = (int)blockIdx.x < T ? (T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int my_tiles = SPLIT ? 1 : ((int)blockIdx.x < T ? (T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0);
   const int steps = my_tiles * KB;
-  auto tile_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
+  auto tile_of = [&](int i) { return SPLIT ? (int)blockIdx.x / S : (int)blockIdx.x + i * (int)gridDim.x; };
   const uint32_t sc_tx = LUT ? (uint32_t)(kTileW * p.lut_sc_box * 4) : 2u * kScBytes;
 
   if (threadIdx.x == 0) {
@@ -431,10 +437,11 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           if (!tc::mbar_wait(bar_sc_empty + 8 * slot, ((q >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
           tc::mbar_arrive_expect_tx(bar_sc_full + 8 * slot, sc_tx);
           if (LUT) {
-            tc::tma_load_2d(sS + slot * kScBytes, &maps.s, (kb / kScKb) * p.lut_sc_box, n0, bar_sc_full + 8 * slot);
+            tc::tma_load_2d(sS + slot * kScBytes, &maps.s, ((kb_base + kb) / kScKb) * p.lut_sc_box, n0,
+                            bar_sc_full + 8 * slot);
           } else {
-            tc::tma_load_2d(sS + slot * kScBytes, &maps.s, (kb / kScKb) * 16, n0, bar_sc_full + 8 * slot);
-            tc::tma_load_2d(sBi + slot * kScBytes, &maps.b, (kb / kScKb) * 16, n0, bar_sc_full + 8 * slot);
+            tc::tma_load_2d(sS + slot * kScBytes, &maps.s, ((kb_base + kb) / kScKb) * 16, n0, bar_sc_full + 8 * slot);
+            tc::tma_load_2d(sBi + slot * kScBytes, &maps.b, ((kb_base + kb) / kScKb) * 16, n0, bar_sc_full + 8 * slot);
           }
           ++sc_issued;
         }
@@ -442,9 +449,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         const uint32_t ph = (j / kStages) & 1;
         if (!tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag)) break;
         tc::mbar_arrive_expect_tx(bar_full_w + 8 * s, kRawBytes);
-        tc::tma_load_2d(sR + s * kRawBytes, &maps.w, kb * 32, n0, bar_full_w + 8 * s);
+        tc::tma_load_2d(sR + s * kRawBytes, &maps.w, (kb_base + kb) * 32, n0, bar_full_w + 8 * s);
         tc::mbar_arrive_expect_tx(bar_full_b + 8 * s, kBBytesT);
-        tc::tma_load_2d(sB + s * kBBytesT, &maps.x, kb * kBK, m0, bar_full_b + 8 * s);
+        tc::tma_load_2d(sB + s * kBBytesT, &maps.x, (kb_base + kb) * kBK, m0, bar_full_b + 8 * s);
         ++issued;
       }
       if (*abort_flag) {
@@ -538,8 +545,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       }
     }
   } else {
-    // ---------------- epilogue: TMEM -> bf16 y ----------------
+    // ---------------- epilogue: TMEM -> bf16 y (split mode: fp32 partial tile) ----------------
     const int quarter = warp & 3;
+    float *part = reinterpret_cast<float *>(smem + L::a);   // split mode: [TT tokens][128 rows]
     for (int i = 0; i < my_tiles; ++i) {
       const int ab = i & 1;
       if (!tc::mbar_wait(bar_acc_full + 8 * ab, (i >> 1) & 1, abort_flag)) break;
@@ -552,7 +560,10 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         uint32_t v[32];
         tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * TT + c0), v);
         tc::tmem_ld_wait();
-        if (n < p.N) {
+        if constexpr (SPLIT) {   // all MMAs of the (single) tile are done: the stage buffers are free
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) part[(c0 + jj) * kTileW + quarter * 32 + lane] = __uint_as_float(v[jj]);
+        } else if (n < p.N) {
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
             const int m = m0 + c0 + jj;
@@ -567,6 +578,45 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(bar_acc_empty + 8 * ab);
     }
+  }
+
+  if constexpr (SPLIT) {
+    // Sum the S partial tiles of the cluster in rank order; rank r finishes tokens
+    // [r TT / S, (r + 1) TT / S) of the tile.  Every thread of every CTA passes both
+    // cluster barriers, also after an aborted main loop.
+    __syncwarp();
+    cluster_sync_all();
+    const uint32_t rank = cluster_ctarank();
+    const int t = tile_of(0);
+    const int m0 = (t % m_tiles) * TT, n0 = (t / m_tiles) * kTileW;
+    const int tok_per = TT / S;
+    const uint32_t part_s = smem_u32(smem + L::a);
+    for (int it = threadIdx.x; it < tok_per * (kTileW / 4); it += kThreadsT) {
+      const int tl = (int)rank * tok_per + it / (kTileW / 4);
+      const int r4 = (it % (kTileW / 4)) * 4;
+      const uint32_t off = (uint32_t)((tl * kTileW + r4) * 4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int r = 0; r < S; ++r) {
+        const float4 v = ld_shared_cluster_v4(map_shared_rank(part_s + off, (uint32_t)r));
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      const int m = m0 + tl, n = n0 + r4;
+      if (m < p.M) {
+        uint16_t *dst = p.y + (size_t)m * p.N + n;
+        const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
+        if (n + 3 < p.N && (p.N & 3) == 0) {
+          *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(vals[0], vals[1]), pack_bf16x2(vals[2], vals[3]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (n + j < p.N) {
+              __nv_bfloat16 h = __float2bfloat16_rn(vals[j]);
+              dst[j] = *reinterpret_cast<uint16_t *>(&h);
+            }
+        }
+      }
+    }
+    cluster_sync_all();   // every rank has read every partial before any CTA exits
   }
 
   tc::tc_fence_before();
@@ -630,32 +680,74 @@ unsigned persistent_grid(const TcGemmParams &p, int tt = kTileT) {
   return (unsigned)(tiles < sms ? tiles : sms);
 }
 
-// Tokens per tile.  The dequantising producers bound a tile's time, so a 128-token tile
-// costs about 7/8 of a 256-token one (measured on GB300); 128 is taken when its waves of
-// tiles finish sooner: 7 * waves(128) < 8 * waves(256).
-int pick_token_tile(const TcGemmParams &p) {
+// Tile plan: tokens per tile (TT) and K split (S).  A tile's time is set by its K blocks,
+// the dequantising producers being the bound: a 128-token tile costs about 7/8 of a
+// 256-token one per K block (measured on GB300).  S = 1 runs persistent CTAs over all
+// tiles; S > 1 runs one (tile, K slice) per CTA, S CTAs per cluster, plus the reduction of
+// the partial tiles (about 10 K blocks' time).  Cost = rounds of CTAs x time per CTA; a
+// split is taken only when it is clearly (10 %) cheaper than the best unsplit plan.
+struct TilePlan {
+  int tt, S;
+};
+TilePlan pick_tile_plan(const TcGemmParams &p) {
   const int sms = sm_count();
-  auto waves = [&](int tt) {
-    const long long t = (long long)((p.N + kTileW - 1) / kTileW) * ((p.M + tt - 1) / tt);
-    return (t + sms - 1) / sms;
-  };
-  return 7 * waves(128) < 8 * waves(256) ? 128 : 256;
+  const int KB = p.K / kBK;
+  TilePlan best{256, 1};
+  double best1 = 1e30, bestS = 1e30;
+  TilePlan planS{256, 1};
+  for (int tt : {256, 128}) {
+    const double f = tt == 256 ? 1.0 : 0.875;
+    const long long T = (long long)((p.N + kTileW - 1) / kTileW) * ((p.M + tt - 1) / tt);
+    for (int S : {1, 2, 4, 8}) {
+      if (S > 1 && KB % (8 * S) != 0) continue;
+      const long long ctas = T * S;
+      const long long rounds = (ctas + sms - 1) / sms;
+      const double cost = (double)rounds * ((double)KB / S * f + (S > 1 ? 10.0 : 0.0));
+      if (S == 1 && cost < best1) { best1 = cost; best = TilePlan{tt, 1}; }
+      if (S > 1 && cost < bestS) { bestS = cost; planS = TilePlan{tt, S}; }
+    }
+  }
+  return bestS < 0.9 * best1 ? planS : best;
 }
 
 template <bool LUT, int TT>
-cudaError_t launch_tma_typed(const TmaMaps &maps, const TcGemmParams &q, cudaStream_t s) {
-  auto kern = qgemm_tma_kernel<LUT, TT>;
+cudaError_t launch_tma_typed(const TmaMaps &maps, const TcGemmParams &q, int S, cudaStream_t s) {
+  if (S <= 1) {
+    auto kern = qgemm_tma_kernel<LUT, TT, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes_t<TT>());
+    if (e != cudaSuccess) return e;
+    TcGemmParams q1 = q;
+    q1.ksplit = 1;
+    kern<<<persistent_grid(q1, TT), kThreadsT, smem_bytes_t<TT>(), s>>>(maps, q1);
+    return cudaGetLastError();
+  }
+  auto kern = qgemm_tma_kernel<LUT, TT, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes_t<TT>());
   if (e != cudaSuccess) return e;
-  kern<<<persistent_grid(q, TT), kThreadsT, smem_bytes_t<TT>(), s>>>(maps, q);
-  return cudaGetLastError();
+  TcGemmParams qs = q;
+  qs.ksplit = S;
+  const long long tiles = (long long)((q.N + kTileW - 1) / kTileW) * ((q.M + TT - 1) / TT);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(tiles * S), 1, 1);
+  cfg.blockDim = dim3(kThreadsT, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes_t<TT>();
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, maps, qs);
 }
 
 template <bool LUT>
 cudaError_t launch_tc(const TcGemmParams &p, const void *x, cudaStream_t s) {
   const bool tma_path = p.K % 256 == 0 && (!LUT || p.lut_kb_per_block == 1 || p.lut_kb_per_block == 2);
   if (tma_path) {
-    const int tt = pick_token_tile(p);
+    const TilePlan tp = pick_tile_plan(p);
+    const int tt = tp.tt;
     TmaMaps maps;
     cudaError_t e = make_x_map(&maps.x, x, p.M, p.K, tt);
     if (e == cudaSuccess)
@@ -668,14 +760,14 @@ cudaError_t launch_tc(const TcGemmParams &p, const void *x, cudaStream_t s) {
                            q.lut_sc_box, kTileW);
       maps.b = maps.s;
       if (e != cudaSuccess) return e;
-      return tt == 128 ? launch_tma_typed<true, 128>(maps, q, s) : launch_tma_typed<true, 256>(maps, q, s);
+      return tt == 128 ? launch_tma_typed<true, 128>(maps, q, tp.S, s) : launch_tma_typed<true, 256>(maps, q, tp.S, s);
     }
     if (e == cudaSuccess)
       e = make_plain_map(&maps.s, p.scales, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.K / 32, p.N, 16, kTileW);
     if (e == cudaSuccess)
       e = make_plain_map(&maps.b, p.biases, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.K / 32, p.N, 16, kTileW);
     if (e != cudaSuccess) return e;
-    return tt == 128 ? launch_tma_typed<false, 128>(maps, p, s) : launch_tma_typed<false, 256>(maps, p, s);
+    return tt == 128 ? launch_tma_typed<false, 128>(maps, p, tp.S, s) : launch_tma_typed<false, 256>(maps, p, tp.S, s);
   }
   CUtensorMap map;
   cudaError_t e = make_x_map(&map, x, p.M, p.K, kTileT);
