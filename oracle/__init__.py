@@ -33,6 +33,8 @@ PINS = {
     "lut4_dequant / lut4_matmul": "pinned: the lut4.rs CPU test's worked example (both transposes, exact)",
     "q4_0_matmul_id": "pinned: hand-built block, q=8 zero case, one-hot x, top_k=1 dense reduction, id permutation",
     "q4_0_route": "pinned: hand-written lists and brute-force invariants",
+    "q4_0_matmul_id_swiglu": "pinned: sigmoid(+-ln 3) closed form, zero gate/up, odd part = plain routed "
+                             "matmul, even part = z tanh(z/2) via numpy, per-row independence",
 }
 
 
@@ -81,6 +83,9 @@ def _declare(L: ctypes.CDLL) -> None:
         "oracle_q4_0_matmul_id": ([_P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_uint64, _P], None),
         "oracle_q4_0_matmul_id_rows": ([_P, _P, _P, _I, _I, _I, _I, ctypes.c_uint64, _P, _I, _P], None),
         "oracle_q4_0_route": ([_P, _I, _I, _P, _P, _P], None),
+        "oracle_q4_0_matmul_id_swiglu": ([_P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_uint64, _P], None),
+        "oracle_q4_0_matmul_id_swiglu_rows": ([_P, _P, _P, _P, _I, _I, _I, ctypes.c_uint64, _P, _I, _P],
+                                              None),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -224,6 +229,29 @@ def q4_0_matmul_id_rows(x, w, ids, top_k: int, N: int, K: int, n_experts: int,
     out = np.empty((rows.size, N), np.float64)
     lib().oracle_q4_0_matmul_id_rows(_p(x), _p(w), _p(ids), top_k, N, K, n_experts,
                                      expert_stride, _p(rows), rows.size, _p(out))
+    return out
+
+
+def q4_0_matmul_id_swiglu(gate, up, w, ids, N: int, K: int, n_experts: int,
+                          expert_stride: int) -> np.ndarray:
+    """fp64 [n_rows, N]: out[r] = (silu(gate[r]) * up[r]) . dequant(W[ids[r]])^T; gate and up
+    are [n_rows, K] f32, one row per routed row."""
+    gate, up, w, ids = _c(gate, np.float32), _c(up, np.float32), _c(w, np.uint8), _c(ids, np.uint32)
+    n_rows = ids.size
+    assert gate.size == n_rows * K and up.size == n_rows * K
+    out = np.empty((n_rows, N), np.float64)
+    lib().oracle_q4_0_matmul_id_swiglu(_p(gate), _p(up), _p(w), _p(ids), n_rows, N, K, n_experts,
+                                       expert_stride, _p(out))
+    return out
+
+
+def q4_0_matmul_id_swiglu_rows(gate, up, w, ids, N: int, K: int, n_experts: int,
+                               expert_stride: int, rows) -> np.ndarray:
+    gate, up, w, ids = _c(gate, np.float32), _c(up, np.float32), _c(w, np.uint8), _c(ids, np.uint32)
+    rows = _c(rows, np.int64)
+    out = np.empty((rows.size, N), np.float64)
+    lib().oracle_q4_0_matmul_id_swiglu_rows(_p(gate), _p(up), _p(w), _p(ids), N, K, n_experts,
+                                            expert_stride, _p(rows), rows.size, _p(out))
     return out
 
 

@@ -24,6 +24,8 @@
  *   [P3] mlx-native 0.9.0, src/ops/quantized_matmul_id_ggml.rs -- module doc
  *        (routed-matmul definition), `IdMmScratch` and the map0 stage of
  *        `dispatch_id_mm_for_test` (per-expert routed lists).
+ *        Also `quantized_matmul_id_swiglu_q4_0` (doc comment): the fused SwiGLU
+ *        routed mat-vec.
  *   The Q4_0 block layout itself (fp16 d + 16 bytes of nibbles, low nibbles are
  *   elements 0..15, high nibbles 16..31, value (q-8)*d) is not printed on [P3]; it is
  *   the GGML Q4_0 format as the problem statement gives it.
@@ -364,6 +366,55 @@ void oracle_q4_0_matmul_id_rows(const float *x, const uint8_t *w, const uint32_t
     for (int64_t i = 0; i < count; ++i)
         q4_0_one_row(x, w, ids[rows[i]], rows[i] / top_k, N, K, n_experts, expert_stride,
                      out + i * N);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Fused SwiGLU + routed Q4_0 mat-vec  [P3 quantized_matmul_id_swiglu_q4_0  */
+/* doc]: out[r][n] = sum_k q4_0(W[ids[r]])[n][k] * (silu(gate[r][k]) *      */
+/* up[r][k]).  gate and up hold one row per ROUTED row r (not per token).    */
+/* silu is not spelled out on the page; its plain definition is used:       */
+/* silu(z) = z * sigmoid(z) = z / (1 + exp(-z)), evaluated in fp64.          */
+/* ------------------------------------------------------------------------- */
+
+static double silu(double z)
+{
+    return z / (1.0 + exp(-z));
+}
+
+static void swiglu_one_row(const float *gate, const float *up, const uint8_t *w, uint32_t e,
+                           int64_t r, int64_t N, int64_t K, int64_t n_experts,
+                           uint64_t expert_stride, double *out_row)
+{
+    for (int64_t n = 0; n < N; ++n) {
+        double acc = 0.0;
+        if ((int64_t)e < n_experts) {
+            const uint8_t *row = w + (uint64_t)e * expert_stride + (uint64_t)(n * (K / 32) * 18);
+            for (int64_t k = 0; k < K; ++k) {
+                double h = silu((double)gate[r * K + k]) * (double)up[r * K + k];
+                acc += (double)q4_0_value(row, k) * h;
+            }
+        }
+        out_row[n] = acc;
+    }
+}
+
+void oracle_q4_0_matmul_id_swiglu(const float *gate, const float *up, const uint8_t *w,
+                                  const uint32_t *ids, int64_t n_rows, int64_t N, int64_t K,
+                                  int64_t n_experts, uint64_t expert_stride, double *out)
+{
+    for (int64_t r = 0; r < n_rows; ++r)
+        swiglu_one_row(gate, up, w, ids[r], r, N, K, n_experts, expert_stride, out + r * N);
+}
+
+/* Only the routed rows listed in rows[] (out is [count, N]). */
+void oracle_q4_0_matmul_id_swiglu_rows(const float *gate, const float *up, const uint8_t *w,
+                                       const uint32_t *ids, int64_t N, int64_t K,
+                                       int64_t n_experts, uint64_t expert_stride,
+                                       const int64_t *rows, int64_t count, double *out)
+{
+    for (int64_t i = 0; i < count; ++i)
+        swiglu_one_row(gate, up, w, ids[rows[i]], rows[i], N, K, n_experts, expert_stride,
+                       out + i * N);
 }
 
 /* Per-expert routed lists (the map0 stage): htpe[e] = number of rows r with

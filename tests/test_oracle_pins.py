@@ -296,6 +296,108 @@ def test_q4_0_routing_rows_follow_ids():
     np.testing.assert_array_equal(np.delete(out3, 3, 0), np.delete(out, 3, 0))
 
 
+# ---------------------------------------------------------------------------------------
+# Fused SwiGLU + routed Q4_0 mat-vec (quantized_matmul_id_ggml.rs,
+# quantized_matmul_id_swiglu_q4_0): out[r] = (silu(gate[r]) * up[r]) . dequant(W[ids[r]])^T
+# ---------------------------------------------------------------------------------------
+
+def _dense_rows(w, stride, e, N, K):
+    """Expert e's dequantised rows [N, K] from the (pinned) Q4_0 block decode."""
+    rb = (K // 32) * 18
+    base = e * stride
+    return np.stack([oracle.q4_0_dequant_row(w[base + n * rb:base + (n + 1) * rb], K)
+                     for n in range(N)]).astype(np.float64)
+
+
+def test_swiglu_closed_form_at_plus_minus_ln3():
+    # sigmoid(ln 3) = 3/4 and sigmoid(-ln 3) = 1/4, so silu(ln 3) = 0.75 ln 3 and
+    # silu(-ln 3) = -0.25 ln 3; every other gate entry is 0 and silu(0) = 0.
+    n_exp, N, K = 3, 4, 64
+    w, stride = synth.q4_0_experts(81, n_exp, N, K)
+    ln3 = float(np.log(3.0))
+    gate = np.zeros((2, K), np.float32)
+    up = synth.activations_f32(82, 2, K)
+    k0, k1 = 5, 40
+    gate[:, k0], gate[:, k1] = np.float32(ln3), np.float32(-ln3)
+    up[:, k0], up[:, k1] = 2.0, 4.0
+    ids = np.array([2, 0], np.uint32)
+    out = oracle.q4_0_matmul_id_swiglu(gate, up, w, ids, N, K, n_exp, stride)
+    g = float(np.float32(ln3))   # the stored gate value
+    for r in range(2):
+        Wd = _dense_rows(w, stride, int(ids[r]), N, K)
+        s_pos = g / (1.0 + 1.0 / 3.0 * np.exp(ln3 - g))   # = 0.75 g up to the f32 rounding of ln 3
+        s_neg = -g / (1.0 + 3.0 * np.exp(g - ln3))
+        want = Wd[:, k0] * s_pos * 2.0 + Wd[:, k1] * s_neg * 4.0
+        np.testing.assert_allclose(out[r], want, rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(out[r], Wd[:, k0] * 1.5 * ln3 - Wd[:, k1] * ln3, rtol=1e-6)
+
+
+def test_swiglu_zero_gate_or_zero_up_gives_zero():
+    n_exp, N, K = 2, 5, 96
+    w, stride = synth.q4_0_experts(83, n_exp, N, K)
+    ids = np.array([1, 0, 1], np.uint32)
+    x = synth.activations_f32(84, 3, K)
+    zero = np.zeros_like(x)
+    assert np.all(oracle.q4_0_matmul_id_swiglu(zero, x, w, ids, N, K, n_exp, stride) == 0.0)
+    assert np.all(oracle.q4_0_matmul_id_swiglu(x, zero, w, ids, N, K, n_exp, stride) == 0.0)
+
+
+def _exact_gate_up(seed, T, K):
+    # gate on a 1/16 grid in [-4, 4) and up in {+-1/2, +-1, +-2}: every product gate * up is
+    # exact in f32, so it can be fed to the plain routed matmul as its x.
+    r = synth.u64(seed, 0, 2 * T * K)
+    gate = ((r[:T * K] % np.uint64(128)).astype(np.float32) - 64.0) / 16.0
+    up = np.array([-2.0, -1.0, -0.5, 0.5, 1.0, 2.0], np.float32)[(r[T * K:] % np.uint64(6)).astype(np.int64)]
+    return gate.reshape(T, K), up.reshape(T, K)
+
+
+def test_swiglu_odd_part_is_the_plain_routed_matmul():
+    # silu(z) - silu(-z) = z, so out(gate) - out(-gate) = the routed matmul of x = gate * up.
+    n_exp, N, K, T = 4, 6, 128, 5
+    w, stride = synth.q4_0_experts(85, n_exp, N, K)
+    gate, up = _exact_gate_up(86, T, K)
+    ids = np.array([3, 0, 2, 2, 1], np.uint32)
+    diff = (oracle.q4_0_matmul_id_swiglu(gate, up, w, ids, N, K, n_exp, stride) -
+            oracle.q4_0_matmul_id_swiglu(-gate, up, w, ids, N, K, n_exp, stride))
+    plain = oracle.q4_0_matmul_id(gate * up, w, ids, T, 1, N, K, n_exp, stride)
+    np.testing.assert_allclose(diff, plain, rtol=1e-11, atol=1e-11)
+
+
+def test_swiglu_even_part_is_z_tanh_half_z():
+    # silu(z) + silu(-z) = z tanh(z / 2); with the odd part this fixes silu(z) = z sigmoid(z).
+    n_exp, N, K, T = 3, 4, 64, 3
+    w, stride = synth.q4_0_experts(87, n_exp, N, K)
+    gate, up = _exact_gate_up(88, T, K)
+    ids = np.array([2, 1, 2], np.uint32)
+    summ = (oracle.q4_0_matmul_id_swiglu(gate, up, w, ids, N, K, n_exp, stride) +
+            oracle.q4_0_matmul_id_swiglu(-gate, up, w, ids, N, K, n_exp, stride))
+    g = gate.astype(np.float64)
+    h = g * np.tanh(g / 2.0) * up.astype(np.float64)
+    for r in range(T):
+        want = _dense_rows(w, stride, int(ids[r]), N, K) @ h[r]
+        np.testing.assert_allclose(summ[r], want, rtol=1e-11, atol=1e-11)
+
+
+def test_swiglu_rows_follow_ids_and_inputs():
+    n_exp, N, K, T = 5, 3, 64, 6
+    w, stride = synth.q4_0_experts(89, n_exp, N, K)
+    gate = synth.activations_f32(90, T, K)
+    up = synth.activations_f32(91, T, K)
+    ids = np.array([4, 1, 0, 4, 2, 3], np.uint32)
+    out = oracle.q4_0_matmul_id_swiglu(gate, up, w, ids, N, K, n_exp, stride)
+    # a routed row depends only on its own gate/up row and its own expert
+    perm = np.array([5, 3, 0, 1, 4, 2])
+    outp = oracle.q4_0_matmul_id_swiglu(gate[perm], up[perm], w, ids[perm], N, K, n_exp, stride)
+    np.testing.assert_array_equal(outp, out[perm])
+    rows = np.array([4, 0, 4])
+    np.testing.assert_array_equal(
+        oracle.q4_0_matmul_id_swiglu_rows(gate, up, w, ids, N, K, n_exp, stride, rows), out[rows])
+    ids2 = ids.copy(); ids2[2] = 77   # out of range: zero row, the others unchanged
+    out2 = oracle.q4_0_matmul_id_swiglu(gate, up, w, ids2, N, K, n_exp, stride)
+    assert np.all(out2[2] == 0.0)
+    np.testing.assert_array_equal(np.delete(out2, 2, 0), np.delete(out, 2, 0))
+
+
 def test_q4_0_route_hand_written():
     htpe, hids, bad = oracle.q4_0_route(np.array([3, 0, 3, 1, 0, 3, 7], np.uint32), 4)
     assert list(htpe) == [2, 1, 0, 3]
