@@ -454,7 +454,23 @@ def bench_moe(args, q, synth, to_dev, ring_of, time_graph, dev, pk):
             rows.append({"n_tokens": n_tokens, "mode": {1: "mv", 2: "mm"}[mode], "us": round(t * 1e6, 2),
                          "GB_s": round(by / t / 1e9, 1), "frac_hbm": round(by / t / 1e9 / pk["hbm_gbs"], 3),
                          "TFLOP_s": round(fl / t / 1e12, 2)})
-    return {"experts": E, "top_k": top_k, "N": N, "K": K, "shapes": rows}
+    # Fused SwiGLU routed mat-vec: the down projection of the same MoE (K = 1408 -> N = 2048),
+    # one decode token; gate/up rows per routed row.
+    Nd, Kd, n_tokens = K, N, 1
+    wd, stride_d = synth.q4_0_experts(4300, E, Nd, Kd)
+    ring_d = ring_of((to_dev(wd),), wd.nbytes)
+    ids = synth.routing_ids(4400, n_tokens, top_k, E)
+    idd = to_dev(ids.view(np.int32))
+    gate = to_dev(synth.activations_f32(4500, n_tokens * top_k, Kd))
+    up = to_dev(synth.activations_f32(4501, n_tokens * top_k, Kd))
+    out = torch.empty((n_tokens * top_k, Nd), dtype=torch.float32, device=dev)
+    by = len(np.unique(ids)) * Nd * (Kd // 32) * 18 + 2 * gate.numel() * 4 + out.numel() * 4 + ids.nbytes
+    L = 2 * len(ring_d)
+    t = time_graph(lambda _: [q.q4_0_matmul_id_swiglu(gate, up, ring_d[l % len(ring_d)][0], idd, out, top_k,
+                                                      Nd, Kd, E, stride_d) for l in range(L)], L, replays=5) / L
+    swiglu = {"n_tokens": n_tokens, "N": Nd, "K": Kd, "us": round(t * 1e6, 2), "GB_s": round(by / t / 1e9, 1),
+              "frac_hbm": round(by / t / 1e9 / pk["hbm_gbs"], 3)}
+    return {"experts": E, "top_k": top_k, "N": N, "K": K, "shapes": rows, "swiglu_down_mv": swiglu}
 
 
 # ------------------------------------------------------------------------------------------
@@ -543,6 +559,7 @@ CASES = {
     "lut4_m512": "lut4_matmul M=512 K=N=4096",
     "moe_n1": "q4_0_matmul_id n_tokens=1 (mat-vec)",
     "moe_n512": "q4_0_matmul_id n_tokens=512 (mat-mat)",
+    "swiglu_n1": "q4_0_matmul_id_swiglu n_tokens=1, K=1408 -> N=2048 (fused SwiGLU mat-vec)",
 }
 
 
@@ -576,6 +593,15 @@ def run_case(name: str, launches: int = 3):
         P, S = to_dev(packed), to_dev(scales)
         y = torch.empty((M, N), dtype=torch.int16, device=dev)
         fn = lambda: q.lut4_matmul(x, P, S, book, y, N, K, 64, 1)
+    elif name == "swiglu_n1":
+        E, top_k, N, K = 64, 8, 2048, 1408
+        w, stride = synth.q4_0_experts(4300, E, N, K)
+        ids = synth.routing_ids(4400, 1, top_k, E)
+        gate = to_dev(synth.activations_f32(4500, top_k, K))
+        up = to_dev(synth.activations_f32(4501, top_k, K))
+        Wd, idd = to_dev(w), to_dev(ids.view(np.int32))
+        out = torch.empty((top_k, N), dtype=torch.float32, device=dev)
+        fn = lambda: q.q4_0_matmul_id_swiglu(gate, up, Wd, idd, out, top_k, N, K, E, stride)
     else:
         n_tokens = 1 if name == "moe_n1" else 512
         E, top_k, N, K = 64, 8, 1408, 2048

@@ -186,6 +186,26 @@ q4mm_status q4_0_matmul_id(const float *x, const void *w, const uint32_t *ids, f
                            int64_t n_experts, uint64_t expert_stride, int mode,
                            void *workspace, size_t workspace_bytes, q4mm_stream_t stream);
 
+/* Fused SwiGLU + expert-routed Q4_0 mat-vec (quantized_matmul_id_ggml.rs,
+ * quantized_matmul_id_swiglu_q4_0 and its doc comment): the down projection of a MoE FFN
+ * in one launch, without writing silu(gate) * up to memory.
+ *   gate, up  f32 [n_tokens * top_k, K]: one row per ROUTED row r = token*top_k + slot.
+ *   w, ids    as for q4_0_matmul_id.
+ *   out       f32 [n_tokens * top_k, N];
+ *             out[r][n] = sum_k W[ids[r]][n][k] * silu(gate[r][k]) * up[r][k],
+ *             silu(z) = z / (1 + exp(-z)), formed in fp32.  A row whose id is >= n_experts
+ *             is written as zeros and sets Q4MM_DEVERR_BAD_EXPERT.
+ * Every routed row reads its expert's rows (the mat-vec form, as on the page, for every
+ * n_tokens); the product runs on the tensor cores when K % 128 == 0 and the expert slabs
+ * are 8-byte aligned, else on the fp32 FMA pipes, with the same results to tolerance.
+ * Requirements: n_tokens >= 0 (0 is a no-op), top_k, N, K, n_experts >= 1, K % 32 == 0,
+ * n_experts <= 1024, n_tokens*top_k <= 2^24, expert_stride >= N*(K/32)*18; gate, up, out
+ * 16-byte aligned, ids 4-byte aligned.  No workspace; nothing is allocated. */
+q4mm_status q4_0_matmul_id_swiglu(const float *gate, const float *up, const void *w,
+                                  const uint32_t *ids, float *out, int64_t n_tokens,
+                                  int64_t top_k, int64_t N, int64_t K, int64_t n_experts,
+                                  uint64_t expert_stride, q4mm_stream_t stream);
+
 /* ======================================================================================
  * Allocation-free variant of the mat-mat form (the source pages have no counterpart).
  *

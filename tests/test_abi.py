@@ -26,7 +26,8 @@ def L():
 def test_header_declares_the_hot_path():
     names = _declared_functions()
     for n in ["q4_dequant", "q4_gemv", "q4_gemm", "lut4_matmul", "lut4_dequant", "q4_0_route",
-              "q4_0_matmul_id", "q4_0_matmul_id_workspace_size", "q4mm_status_string"]:
+              "q4_0_matmul_id", "q4_0_matmul_id_workspace_size", "q4_0_matmul_id_swiglu",
+              "q4mm_status_string"]:
         assert n in names
 
 
@@ -79,5 +80,11 @@ def test_moe_argument_checks(L):
     need = L.q4_0_matmul_id_workspace_size(64, 8, 64, 64, 16)
     assert need > 0
     assert L.q4_0_matmul_id(FAKE, FAKE, FAKE, FAKE, 64, 8, 64, 64, 16, 64 * 2 * 18, 2, FAKE, need - 1, None) == 3
+    # fused SwiGLU: null up, K not a multiple of 32, misaligned gate
+    assert L.q4_0_matmul_id_swiglu(FAKE, None, FAKE, FAKE, FAKE, 1, 8, 64, 64, 16, 1 << 20, None) == 1
+    assert L.q4_0_matmul_id_swiglu(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 64, 48, 16, 1 << 20, None) == 1
+    assert L.q4_0_matmul_id_swiglu(FAKE + 4, FAKE, FAKE, FAKE, FAKE, 1, 8, 64, 64, 16, 1 << 20, None) == 2
+    assert L.q4_0_matmul_id_swiglu(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 64, 64, 16, 64 * 2 * 18 - 1, None) == 1
+    assert L.q4_0_matmul_id_swiglu(None, None, None, None, None, 0, 8, 64, 64, 16, 0, None) == 0
     # routing: too many experts
     assert L.q4_0_route(FAKE, 8, 2000, FAKE, FAKE, None, None) == 1

@@ -67,7 +67,8 @@ def _run(x, w, ids, top_k, N, K, E, stride, mode):
 @pytest.mark.parametrize("mode", [1, 2])
 @pytest.mark.parametrize("n_tokens,top_k,E,N,K,pad", [(1, 8, 64, 96, 256, 0), (5, 2, 6, 64, 2048, 48),
                                                       (40, 8, 16, 130, 512, 16), (33, 1, 3, 256, 96, 0),
-                                                      (3, 4, 9, 70, 4096, 0)])
+                                                      (3, 4, 9, 70, 4096, 0), (2, 4, 7, 48, 1408, 8),
+                                                      (3, 2, 5, 40, 384, 0), (2, 2, 3, 20, 128, 0)])
 def test_moe_parity(mode, n_tokens, top_k, E, N, K, pad):
     x, w, stride, ids = _moe_case(100 + n_tokens, n_tokens, top_k, E, N, K, pad)
     ref = oracle.q4_0_matmul_id(x, w, ids, n_tokens, top_k, N, K, E, stride)
@@ -111,3 +112,80 @@ def test_moe_workspace_checks():
     with pytest.raises(q.Q4MMError) as ei:
         q.q4_0_matmul_id(dev(x), dev(w), dev(ids), out, 8, 64, 64, 16, stride, mode=2, workspace=None)
     assert ei.value.status == 3
+
+
+# ---------------------------------------------------------------------------------------
+# Fused SwiGLU + routed Q4_0 mat-vec (quantized_matmul_id_swiglu_q4_0)
+# ---------------------------------------------------------------------------------------
+
+def _swiglu_case(seed, n_tokens, top_k, E, N, K, pad=0):
+    per = N * (K // 32) * 18
+    w, stride = synth.q4_0_experts(seed, E, N, K, expert_stride=per + pad)
+    ids = synth.routing_ids(seed + 1, n_tokens, top_k, E)
+    gate = synth.activations_f32(seed + 2, n_tokens * top_k, K)
+    up = synth.activations_f32(seed + 3, n_tokens * top_k, K)
+    return gate, up, w, stride, ids
+
+
+def _run_swiglu(gate, up, w, ids, top_k, N, K, E, stride):
+    out = torch.full((gate.shape[0], N), float("nan"), dtype=torch.float32, device=DEV)
+    q.q4_0_matmul_id_swiglu(dev(gate), dev(up), dev(w), dev(ids), out, top_k, N, K, E, stride)
+    return out.cpu().numpy().astype(np.float64)
+
+
+# K % 256 == 0 (16-byte copies), K % 128 == 0 with a 4-block tail chunk and 8-byte copies
+# (1408 is the down projection of the 64-expert configuration), K = 128 (one tail chunk),
+# and the fp32 FMA kernel (K % 128 != 0, or an expert stride that is not 8-byte aligned).
+@pytest.mark.parametrize("n_tokens,top_k,E,N,K,pad", [(1, 8, 64, 96, 256, 0), (1, 8, 64, 2048, 1408, 0),
+                                                      (5, 2, 6, 64, 640, 8), (3, 4, 9, 70, 384, 0),
+                                                      (2, 3, 4, 24, 128, 0), (4, 2, 5, 33, 96, 0),
+                                                      (2, 3, 4, 40, 256, 4), (40, 8, 16, 130, 512, 16)])
+def test_swiglu_parity(n_tokens, top_k, E, N, K, pad):
+    gate, up, w, stride, ids = _swiglu_case(300 + n_tokens + K, n_tokens, top_k, E, N, K, pad)
+    ref = oracle.q4_0_matmul_id_swiglu(gate, up, w, ids, N, K, E, stride)
+    got = _run_swiglu(gate, up, w, ids, top_k, N, K, E, stride)
+    assert_within_tolerance(got, ref, f"q4_0_matmul_id_swiglu K={K}")
+
+
+def test_swiglu_saturated_gates():
+    # gates far into both tails: silu(-90) ~ 0 (exp overflows to inf in fp32), silu(90) = 90
+    n_tokens, top_k, E, N, K = 2, 2, 3, 32, 256
+    gate, up, w, stride, ids = _swiglu_case(77, n_tokens, top_k, E, N, K)
+    gate[:, ::3] = -90.0
+    gate[:, 1::7] = 90.0
+    ref = oracle.q4_0_matmul_id_swiglu(gate, up, w, ids, N, K, E, stride)
+    got = _run_swiglu(gate, up, w, ids, top_k, N, K, E, stride)
+    assert_within_tolerance(got, ref, "swiglu saturated gates")
+
+
+@pytest.mark.parametrize("K", [1408, 96])
+def test_swiglu_invalid_id_gives_zero_row(K):
+    n_tokens, top_k, E, N = 3, 4, 6, 48
+    gate, up, w, stride, ids = _swiglu_case(81, n_tokens, top_k, E, N, K)
+    ids = ids.copy()
+    ids[[1, 10]] = 1000
+    ref = oracle.q4_0_matmul_id_swiglu(gate, up, w, ids, N, K, E, stride)
+    got = _run_swiglu(gate, up, w, ids, top_k, N, K, E, stride)
+    assert np.all(got[[1, 10]] == 0.0)
+    assert_within_tolerance(got, ref, "swiglu invalid id")
+    assert q.device_errors() & 0x2
+
+
+@pytest.mark.parametrize("n_tokens", [1, 64])
+def test_swiglu_full_size_sampled(n_tokens):
+    # the down projection of the 64-expert, top-8 configuration: K = 1408 -> N = 2048
+    E, top_k, N, K = 64, 8, 2048, 1408
+    gate, up, w, stride, ids = _swiglu_case(5000 + n_tokens, n_tokens, top_k, E, N, K)
+    got = _run_swiglu(gate, up, w, ids, top_k, N, K, E, stride)
+    assert np.all(np.isfinite(got))
+    rows = np.unique(np.concatenate([np.arange(min(8, n_tokens * top_k)),
+                                     np.random.default_rng(n_tokens).integers(0, n_tokens * top_k, 16)]))
+    ref = oracle.q4_0_matmul_id_swiglu_rows(gate, up, w, ids, N, K, E, stride, rows)
+    assert_within_tolerance(got[rows], ref, f"swiglu full n_tokens={n_tokens}")
+
+
+def test_swiglu_zero_tokens_is_a_no_op():
+    out = torch.full((4, 8), 5.0, dtype=torch.float32, device=DEV)
+    z = torch.empty((0, 64), dtype=torch.float32, device=DEV)
+    q.q4_0_matmul_id_swiglu(z, z, out, out, out, 1, 8, 64, 1, 8 * 2 * 18)
+    assert torch.all(out == 5.0)

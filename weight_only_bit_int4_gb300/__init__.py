@@ -124,6 +124,17 @@ def q4_0_matmul_id(x, w, ids, out, top_k: int, N: int, K: int, n_experts: int,
         mode, _ptr(workspace), ws_bytes, _stream(stream)))
 
 
+def q4_0_matmul_id_swiglu(gate, up, w, ids, out, top_k: int, N: int, K: int, n_experts: int,
+                          expert_stride: int, stream=None) -> None:
+    """out[r, N] f32 = (silu(gate[r]) * up[r]) . dequant_q4_0(W[ids[r]])^T for every routed row
+    r; gate and up are [n_tokens*top_k, K] f32 (one row per routed row)."""
+    n_rows, K_ = gate.shape
+    assert K_ == K and n_rows % top_k == 0
+    _check("q4_0_matmul_id_swiglu", lib().q4_0_matmul_id_swiglu(
+        _ptr(gate), _ptr(up), _ptr(w), _ptr(ids), _ptr(out), n_rows // top_k, top_k, N, K, n_experts,
+        expert_stride, _stream(stream)))
+
+
 def q4_0_matmul_id_noalloc(x, w, ids, out, top_k: int, N: int, K: int, n_experts: int,
                            expert_stride: int, stream=None) -> None:
     """Mat-mat form of q4_0_matmul_id for callers that cannot provide (or allocate) a

@@ -26,6 +26,7 @@ SIGNATURES = {
     "q4_0_matmul_id_workspace_size": ([_I, _I, _I, _I, _I], ctypes.c_size_t),
     "q4_0_matmul_id": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_uint64, _S, _P,
                         ctypes.c_size_t, _P], _S),
+    "q4_0_matmul_id_swiglu": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_uint64, _P], _S),
     "q4_0_matmul_id_noalloc": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_uint64, _P], _S),
 }
 

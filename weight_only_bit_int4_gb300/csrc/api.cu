@@ -223,4 +223,25 @@ q4mm_status q4_0_matmul_id(const float *x, const void *w, const uint32_t *ids, f
                                   (int)n_experts, expert_stride, s));
 }
 
+q4mm_status q4_0_matmul_id_swiglu(const float *gate, const float *up, const void *w,
+                                  const uint32_t *ids, float *out, int64_t n_tokens, int64_t top_k,
+                                  int64_t N, int64_t K, int64_t n_experts, uint64_t expert_stride,
+                                  q4mm_stream_t stream) {
+  if (n_tokens == 0) return Q4MM_OK;
+  if (!gate || !up || !w || !ids || !out) return Q4MM_ERR_INVALID_ARG;
+  if (n_tokens < 0 || top_k < 1 || N < 1 || K < 32 || K % 32 != 0 || n_experts < 1 ||
+      n_experts > 1024 || N > kMaxDim || K > kMaxDim)
+    return Q4MM_ERR_INVALID_ARG;
+  if (n_tokens * top_k > (int64_t(1) << 24)) return Q4MM_ERR_INVALID_ARG;
+  const uint64_t per_expert = (uint64_t)N * (uint64_t)(K / 32) * 18u;
+  if (expert_stride < per_expert) return Q4MM_ERR_INVALID_ARG;
+  if (!aligned(gate, 16) || !aligned(up, 16) || !aligned(out, 16) || !aligned(ids, 4))
+    return Q4MM_ERR_UNSUPPORTED;
+  q4mm_status st = check_device();
+  if (st != Q4MM_OK) return st;
+  return from_cuda(launch_q4_0_swiglu_mv(gate, up, static_cast<const uint8_t *>(w), ids, out,
+                                         (int)(n_tokens * top_k), (int)N, (int)K, (int)n_experts,
+                                         expert_stride, (cudaStream_t)stream));
+}
+
 }  // extern "C"

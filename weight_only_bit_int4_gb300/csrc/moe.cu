@@ -184,7 +184,8 @@ constexpr int kMvRowsPerWarp = 8;
 constexpr int kMvSegBlocks = 64;   // K segment: 64 blocks = 2048 values = 1152 bytes
 
 struct MvParams {
-  const float *x;
+  const float *x;           // x [n_tokens, K]; the SwiGLU form: gate [n_rows, K]
+  const float *up;          // the SwiGLU form: up [n_rows, K] (nullptr otherwise)
   const uint8_t *w;
   const uint32_t *ids;
   const int32_t *order;     // routed rows to visit (nullptr: row i is routed row i)
@@ -198,6 +199,21 @@ __device__ __forceinline__ float f16_bits_to_float(uint16_t h) {
   return __half2float(*reinterpret_cast<const __half *>(&h));
 }
 
+// The vector a routed row multiplies: x itself, or silu(gate) * up in fp32 (SwiGLU form).
+__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
+
+template <bool SWIGLU>
+__device__ __forceinline__ float4 mv_input4(const float *xr, const float *ur, int off) {
+  const float4 g = __ldg(reinterpret_cast<const float4 *>(xr + off));
+  if constexpr (!SWIGLU) {
+    return g;
+  } else {
+    const float4 u = __ldg(reinterpret_cast<const float4 *>(ur + off));
+    return make_float4(silu_f32(g.x) * u.x, silu_f32(g.y) * u.y, silu_f32(g.z) * u.z, silu_f32(g.w) * u.w);
+  }
+}
+
+template <bool SWIGLU>
 __global__ void __launch_bounds__(kMvWarps * 32) q4_0_mv_kernel(const __grid_constant__ MvParams p) {
   __shared__ __align__(16) uint8_t wrow[kMvWarps][kMvSegBlocks * 18];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -214,7 +230,8 @@ __global__ void __launch_bounds__(kMvWarps * 32) q4_0_mv_kernel(const __grid_con
     continue;
   }
   const uint8_t *wexp = p.w + (size_t)e * p.expert_stride;
-  const float *xr = p.x + (size_t)tok * p.K;
+  const float *xr = p.x + (SWIGLU ? (size_t)r : (size_t)tok) * p.K;
+  const float *ur = SWIGLU ? p.up + (size_t)r * p.K : nullptr;
   const size_t row_bytes = (size_t)nblk * 18;
   float acc[kMvRowsPerWarp];
 #pragma unroll
@@ -228,10 +245,9 @@ __global__ void __launch_bounds__(kMvWarps * 32) q4_0_mv_kernel(const __grid_con
     for (int h = 0; h < 2; ++h) {
       const int b = sb + lane + 32 * h;
       if (lane + 32 * h < seg_blocks) {
-        const float4 *src = reinterpret_cast<const float4 *>(xr + (size_t)b * 32);
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-          const float4 f = __ldg(src + v);
+          const float4 f = mv_input4<SWIGLU>(xr, ur, b * 32 + 4 * v);
           xv[h][4 * v] = f.x; xv[h][4 * v + 1] = f.y; xv[h][4 * v + 2] = f.z; xv[h][4 * v + 3] = f.w;
         }
       } else {
@@ -439,13 +455,14 @@ cudaError_t launch_q4_0_route(const uint32_t *ids, int n_rows, int n_experts, ui
 }
 
 // ---------------------------------------------------------------------------------------
-// Mat-vec form on the tensor cores (K % 256 == 0, 16-byte aligned expert slabs).
+// Mat-vec form on the tensor cores (K % 128 == 0, 8-byte aligned rows).
 //
 // A CTA owns routed row r = token * top_k + slot and 16 weight rows of expert ids[r]; its
-// KS warps take consecutive K slices.  Each warp streams its slice as chunks of 8 Q4_0
-// blocks per row (144 bytes, 16-byte aligned because K % 256 == 0) through a private
-// cp.async ring, and stages its slice of x rounded to bf16 together with the per-block sums
-// of those bf16 values.
+// KS warps take consecutive K slices.  Each warp streams its slice as chunks of up to 8
+// Q4_0 blocks per row (144 bytes; the last chunk of a row holds 4 blocks when K % 256 != 0)
+// through a private cp.async ring -- 16-byte copies when every row is 16-byte aligned
+// (K % 256 == 0), else 8-byte copies -- and stages its slice of x rounded to bf16 together
+// with the per-block sums of those bf16 values.
 //
 // The product follows the M <= 4 INT4 decode kernel: with one token, B column j of an
 // m16n8k16 step carries x on the k-slots of Q4_0 block j (j < 4) and zeros elsewhere, so
@@ -455,34 +472,47 @@ cudaError_t launch_q4_0_route(const uint32_t *ids, int n_rows, int n_experts, ui
 // which is the block's contribution with its terms regrouped.  Word m of a block's qs
 // holds elements 4m..4m+3 (low nibbles) and 4m+16..4m+19 (high nibbles); the decode pairs
 // are (4m, 4m+2), (4m+16, 4m+18), (4m+1, 4m+3), (4m+17, 4m+19) and x is staged in that order.
+//
+// SWIGLU (quantized_matmul_id_swiglu_q4_0): the vector of routed row r is
+// silu(gate[r][k]) * up[r][k], formed in fp32 while x is staged; gate and up have one row
+// per routed row.  Everything after the staging is the same.
 // ---------------------------------------------------------------------------------------
-constexpr int kMvcDepth = 4;                   // chunk stages per warp
+constexpr int kMvcDepth = 4;                   // chunk stages per warp (at most)
 constexpr int kMvcRow = 144;                   // bytes per weight row per chunk (8 blocks)
 constexpr int kMvcChunk = 16 * kMvcRow;        // 2304 bytes per chunk stage
 
+__host__ __device__ inline int mvc_depth(int maxc) { return maxc < kMvcDepth ? maxc : kMvcDepth; }
 __host__ __device__ inline size_t mvc_warp_bytes(int maxc) {
-  return (size_t)kMvcDepth * kMvcChunk + (size_t)maxc * 8 * 64 + (size_t)maxc * 8 * 4;
+  return (size_t)mvc_depth(maxc) * kMvcChunk + (size_t)maxc * 8 * 64 + (size_t)maxc * 8 * 4;
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+template <int PIECE>
+__device__ __forceinline__ void cp_async_piece(uint32_t dst, const void *src, uint32_t src_bytes) {
+  if constexpr (PIECE == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 
-template <int KS>
+template <int KS, bool SWIGLU, int PIECE>
 __global__ void __launch_bounds__(KS * 32) q4_0_mv_mma_kernel(const __grid_constant__ MvParams p, int maxc) {
   extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int kPiecesFull = kMvcRow / PIECE;   // copies per row of an 8-block chunk
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int g = lane / 4, t = lane % 4;
+  const int depth = mvc_depth(maxc);
   const size_t wb = mvc_warp_bytes(maxc);
   uint8_t *ring = smem + (size_t)warp * wb;
-  uint8_t *xs = ring + kMvcDepth * kMvcChunk;                          // [maxc * 8 blocks][4][16 B]
+  uint8_t *xs = ring + (size_t)depth * kMvcChunk;                      // [maxc * 8 blocks][4][16 B]
   float *xsum = reinterpret_cast<float *>(xs + (size_t)maxc * 8 * 64);  // [maxc * 8]
   float *red = reinterpret_cast<float *>(smem + (size_t)KS * wb);       // [KS][16]
   const uint32_t ring_s = smem_u32(ring);
-  const int C = p.K / 256;
+  const int S4 = p.K / 128;                       // 4-block sub-chunks per row
+  const int C = (S4 + 1) / 2;                     // chunks of (up to) 8 blocks
   const int c_begin = (int)(((long long)warp * C) / KS);
   const int c_end = (int)(((long long)(warp + 1) * C) / KS);
   const int nch = c_end - c_begin;
+  const int nblk_w = min(8 * nch, p.K / 32 - 8 * c_begin);   // blocks in this warp's slice
   const int row0 = blockIdx.x * 16;
   const size_t row_bytes = (size_t)(p.K / 32) * 18;
 
@@ -496,13 +526,15 @@ __global__ void __launch_bounds__(KS * 32) q4_0_mv_mma_kernel(const __grid_const
     const uint8_t *wexp = p.w + (size_t)e * p.expert_stride;
     auto issue = [&](int c) {
       const uint32_t slot = ring_s + (uint32_t)((c % kMvcDepth) * kMvcChunk);
-      const size_t col0 = (size_t)(c_begin + c) * kMvcRow;
-      for (int i = lane; i < 16 * 9; i += 32) {   // 16 rows x 9 pieces of 16 bytes
-        const int rr = i / 9, pc = i - rr * 9;
+      const int a = c_begin + c;
+      const int pieces = 2 * a + 1 < S4 ? kPiecesFull : kPiecesFull / 2;   // 4-block tail chunk
+      const size_t col0 = (size_t)a * kMvcRow;
+      for (int i = lane; i < 16 * pieces; i += 32) {
+        const int rr = i / pieces, pc = i - rr * pieces;
         const int grow = row0 + rr;
         const bool ok = grow < p.N;
-        cp_async16(slot + (uint32_t)(rr * kMvcRow + pc * 16), wexp + (ok ? (size_t)grow * row_bytes + col0 + pc * 16 : 0),
-                   ok ? 16u : 0u);
+        cp_async_piece<PIECE>(slot + (uint32_t)(rr * kMvcRow + pc * PIECE),
+                              wexp + (ok ? (size_t)grow * row_bytes + col0 + pc * PIECE : 0), ok ? (uint32_t)PIECE : 0u);
       }
     };
 #pragma unroll
@@ -512,21 +544,27 @@ __global__ void __launch_bounds__(KS * 32) q4_0_mv_mma_kernel(const __grid_const
     }
 
     // x slice: item (block, m) -> 16 bytes of bf16 pairs in decode order; block sums.
-    const float *xr = p.x + (size_t)(r / p.top_k) * p.K + (size_t)c_begin * 256;
-    for (int it = lane; it < nch * 8 * 4; it += 32) {   // 4 consecutive lanes share a block
+    const size_t xrow = SWIGLU ? (size_t)r : (size_t)(r / p.top_k);
+    const float *xr = p.x + xrow * p.K + (size_t)c_begin * 256;
+    const float *ur = SWIGLU ? p.up + xrow * p.K + (size_t)c_begin * 256 : nullptr;
+    for (int it = lane; it < ((nblk_w * 4 + 31) & ~31); it += 32) {   // 4 consecutive lanes share a block
       const int blk = it >> 2, m = it & 3;
-      const float4 lo = __ldg(reinterpret_cast<const float4 *>(xr + blk * 32 + 4 * m));
-      const float4 hi = __ldg(reinterpret_cast<const float4 *>(xr + blk * 32 + 16 + 4 * m));
+      const bool in = blk < nblk_w;
+      float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+      if (in) {
+        lo = mv_input4<SWIGLU>(xr, ur, blk * 32 + 4 * m);
+        hi = mv_input4<SWIGLU>(xr, ur, blk * 32 + 16 + 4 * m);
+      }
       const uint32_t p0 = pack_bf16x2(lo.x, lo.z), p1 = pack_bf16x2(hi.x, hi.z);
       const uint32_t p2 = pack_bf16x2(lo.y, lo.w), p3 = pack_bf16x2(hi.y, hi.w);
-      *reinterpret_cast<uint4 *>(xs + (size_t)blk * 64 + m * 16) = make_uint4(p0, p1, p2, p3);
+      if (in) *reinterpret_cast<uint4 *>(xs + (size_t)blk * 64 + m * 16) = make_uint4(p0, p1, p2, p3);
       float sum = 0.f;
       const uint32_t pv[4] = {p0, p2, p1, p3};
 #pragma unroll
       for (int i = 0; i < 4; ++i) sum += __uint_as_float(pv[i] << 16) + __uint_as_float(pv[i] & 0xFFFF0000u);
       sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
       sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-      if (m == 0) xsum[blk] = sum;
+      if (in && m == 0) xsum[blk] = sum;
     }
     __syncwarp();
 
@@ -538,8 +576,8 @@ __global__ void __launch_bounds__(KS * 32) q4_0_mv_mma_kernel(const __grid_const
       cp_async_wait<kMvcDepth - 1>();
       __syncwarp();
       const uint8_t *slot = ring + (c % kMvcDepth) * kMvcChunk;
-#pragma unroll
-      for (int sc = 0; sc < 2; ++sc) {   // sub-chunks of 4 blocks; quad lane t decodes block 4 sc + t
+      const int nsub = 2 * (c_begin + c) + 1 < S4 ? 2 : 1;
+      for (int sc = 0; sc < nsub; ++sc) {   // sub-chunks of 4 blocks; quad lane t decodes block 4 sc + t
         const int bk = 4 * sc + t;
         const int off = 18 * bk + 2;                    // qs of block bk within a row
         const uint32_t sel = (off & 2) ? 0x5432u : 0x3210u;
@@ -605,31 +643,57 @@ __global__ void __launch_bounds__(KS * 32) q4_0_mv_mma_kernel(const __grid_const
   }
 }
 
+template <bool SWIGLU, int PIECE>
+cudaError_t launch_mv_mma_typed(const MvParams &p, int ks, int maxc, size_t smem, cudaStream_t s) {
+  dim3 grid((unsigned)((p.N + 15) / 16), (unsigned)(p.n_rows < 65535 ? p.n_rows : 65535), 1);
+  auto kern = ks == 4 ? q4_0_mv_mma_kernel<4, SWIGLU, PIECE>
+            : ks == 2 ? q4_0_mv_mma_kernel<2, SWIGLU, PIECE> : q4_0_mv_mma_kernel<1, SWIGLU, PIECE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, ks * 32, smem, s>>>(p, maxc);
+  return cudaGetLastError();
+}
+
+// Tensor-core mat-vec when the rows allow it (K % 128 == 0; 16-byte copies need K % 256 == 0
+// and 16-byte aligned slabs, 8-byte copies 8-byte aligned ones), else the fp32 FMA kernel.
+template <bool SWIGLU>
+cudaError_t launch_mv_any(const MvParams &p, cudaStream_t s) {
+  const uintptr_t wa = reinterpret_cast<uintptr_t>(p.w);
+  const bool a16 = p.K % 256 == 0 && p.expert_stride % 16 == 0 && (wa & 15) == 0;
+  const bool a8 = p.K % 128 == 0 && p.expert_stride % 8 == 0 && (wa & 7) == 0;
+  if (a16 || a8) {
+    const int C = (p.K / 128 + 1) / 2;
+    const int ks = C >= 4 ? 4 : (C >= 2 ? 2 : 1);
+    const int maxc = (C + ks - 1) / ks;
+    const size_t smem = (size_t)ks * mvc_warp_bytes(maxc) + (size_t)ks * 16 * 4;
+    if (smem <= 227 * 1024)
+      return a16 ? launch_mv_mma_typed<SWIGLU, 16>(p, ks, maxc, smem, s)
+                 : launch_mv_mma_typed<SWIGLU, 8>(p, ks, maxc, smem, s);
+  }
+  const int rows_cta = kMvWarps * kMvRowsPerWarp;
+  dim3 grid((unsigned)((p.N + rows_cta - 1) / rows_cta), (unsigned)(p.n_rows < 65535 ? p.n_rows : 65535), 1);
+  q4_0_mv_kernel<SWIGLU><<<grid, kMvWarps * 32, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_q4_0_mv(const float *x, const uint8_t *w, const uint32_t *ids, float *out,
                            int n_tokens, int top_k, int N, int K, int n_experts,
                            uint64_t expert_stride, cudaStream_t s) {
   MvParams p{};
-  p.x = x; p.w = w; p.ids = ids; p.order = nullptr; p.n_order = nullptr; p.out = out;
+  p.x = x; p.up = nullptr; p.w = w; p.ids = ids; p.order = nullptr; p.n_order = nullptr; p.out = out;
   p.n_rows = n_tokens * top_k; p.top_k = top_k; p.N = N; p.K = K; p.E = n_experts;
   p.expert_stride = expert_stride;
-  if (K % 256 == 0 && expert_stride % 16 == 0 && (reinterpret_cast<uintptr_t>(w) & 15) == 0) {
-    const int C = K / 256;
-    const int ks = C >= 4 ? 4 : (C >= 2 ? 2 : 1);
-    const int maxc = (C + ks - 1) / ks;
-    const size_t smem = (size_t)ks * mvc_warp_bytes(maxc) + (size_t)ks * 16 * 4;
-    if (smem <= 227 * 1024) {
-      dim3 grid((unsigned)((N + 15) / 16), (unsigned)(p.n_rows < 65535 ? p.n_rows : 65535), 1);
-      auto kern = ks == 4 ? q4_0_mv_mma_kernel<4> : ks == 2 ? q4_0_mv_mma_kernel<2> : q4_0_mv_mma_kernel<1>;
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      kern<<<grid, ks * 32, smem, s>>>(p, maxc);
-      return cudaGetLastError();
-    }
-  }
-  const int rows_cta = kMvWarps * kMvRowsPerWarp;
-  dim3 grid((unsigned)((N + rows_cta - 1) / rows_cta), (unsigned)(p.n_rows < 65535 ? p.n_rows : 65535), 1);
-  q4_0_mv_kernel<<<grid, kMvWarps * 32, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_mv_any<false>(p, s);
+}
+
+cudaError_t launch_q4_0_swiglu_mv(const float *gate, const float *up, const uint8_t *w, const uint32_t *ids,
+                                  float *out, int n_rows, int N, int K, int n_experts, uint64_t expert_stride,
+                                  cudaStream_t s) {
+  MvParams p{};
+  p.x = gate; p.up = up; p.w = w; p.ids = ids; p.order = nullptr; p.n_order = nullptr; p.out = out;
+  p.n_rows = n_rows; p.top_k = 1; p.N = N; p.K = K; p.E = n_experts;
+  p.expert_stride = expert_stride;
+  return launch_mv_any<true>(p, s);
 }
 
 // Mat-mat form, first version: route, then visit routed rows expert by expert so that
@@ -655,12 +719,12 @@ cudaError_t launch_q4_0_mm(const float *x, const uint8_t *w, const uint32_t *ids
   if (tc_ok)
     return launch_q4_0_mm_tc(x, w, out, n_tokens, top_k, N, K, n_experts, expert_stride, workspace, s);
   MvParams p{};
-  p.x = x; p.w = w; p.ids = ids; p.order = hids; p.n_order = offs + n_experts; p.out = out;
+  p.x = x; p.up = nullptr; p.w = w; p.ids = ids; p.order = hids; p.n_order = offs + n_experts; p.out = out;
   p.n_rows = n_rows; p.top_k = top_k; p.N = N; p.K = K; p.E = n_experts;
   p.expert_stride = expert_stride;
   const int rows_cta = kMvWarps * kMvRowsPerWarp;
   dim3 grid((unsigned)((N + rows_cta - 1) / rows_cta), (unsigned)(n_rows < 65535 ? n_rows : 65535), 1);
-  q4_0_mv_kernel<<<grid, kMvWarps * 32, 0, s>>>(p);
+  q4_0_mv_kernel<false><<<grid, kMvWarps * 32, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -231,6 +231,10 @@ cudaError_t launch_q4_0_mv(const float *x, const uint8_t *w, const uint32_t *ids
                            int n_tokens, int top_k, int N, int K, int n_experts,
                            uint64_t expert_stride, cudaStream_t s);
 
+cudaError_t launch_q4_0_swiglu_mv(const float *gate, const float *up, const uint8_t *w, const uint32_t *ids,
+                                  float *out, int n_rows, int N, int K, int n_experts, uint64_t expert_stride,
+                                  cudaStream_t s);
+
 cudaError_t launch_q4_0_mm(const float *x, const uint8_t *w, const uint32_t *ids, float *out,
                            int n_tokens, int top_k, int N, int K, int n_experts,
                            uint64_t expert_stride, void *workspace, cudaStream_t s);
