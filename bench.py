@@ -419,14 +419,21 @@ def bench_lut4(args, q, synth, to_dev, ring_of, time_graph, dev, pk):
         x = to_dev(synth.activations_bf16(3100 + M, M, K))
         y = torch.empty((M, N), dtype=torch.int16, device=dev)
         L = 2 * len(ring)
-        t = time_graph(lambda _: [q.lut4_matmul(x, *ring[l % len(ring)], book, y, N, K, 64, 1)
+        # Static weights (lut4_matmul_ex, Q4MM_GEMV_STATIC_WEIGHTS) as in the decode step; the
+        # flag only changes the decode-kernel (M <= 16) launches.
+        t = time_graph(lambda _: [q.lut4_matmul(x, *ring[l % len(ring)], book, y, N, K, 64, 1, static_weights=True)
                                   for l in range(L)], L, replays=10) / L
         by = packed.nbytes + scales.nbytes + 64 + 2 * M * K + 2 * M * N
         fl = 2.0 * M * N * K
-        rows.append({"M": M, "K": K, "N": N, "us": round(t * 1e6, 3), "GB_s": round(by / t / 1e9, 1),
-                     "frac_hbm": round(by / t / 1e9 / pk["hbm_gbs"], 3),
-                     "TFLOP_s": round(fl / t / 1e12, 2),
-                     "frac_bf16_burst": round(fl / t / 1e12 / pk["bf16_tflops"], 3)})
+        row = {"M": M, "K": K, "N": N, "us": round(t * 1e6, 3), "GB_s": round(by / t / 1e9, 1),
+               "frac_hbm": round(by / t / 1e9 / pk["hbm_gbs"], 3),
+               "TFLOP_s": round(fl / t / 1e12, 2),
+               "frac_bf16_burst": round(fl / t / 1e12 / pk["bf16_tflops"], 3)}
+        if M <= 16:
+            tp = time_graph(lambda _: [q.lut4_matmul(x, *ring[l % len(ring)], book, y, N, K, 64, 1)
+                                       for l in range(L)], L, replays=10) / L
+            row["us_plain_launch"] = round(tp * 1e6, 3)
+        rows.append(row)
     return {"shapes": rows}
 
 

@@ -139,6 +139,16 @@ q4mm_status lut4_matmul(const uint16_t *x, const uint8_t *packed, const float *s
                         const float *book, uint16_t *y, int64_t M, int64_t N, int64_t K,
                         int64_t block, int transpose, q4mm_stream_t stream);
 
+/* lut4_matmul with launch flags (lut4_matmul is lut4_matmul_ex with flags = 0).
+ * Q4MM_GEMV_STATIC_WEIGHTS: the promise and effect described at q4_gemv_ex, for packed and
+ *   scales (the codebook is copied into the launch).  It changes only calls served by the
+ *   decode kernels (M <= 16 on the fast layout); other calls launch as with flags = 0.
+ *   Results are bit-identical to flags = 0.
+ * Unknown flag bits: Q4MM_ERR_INVALID_ARG. */
+q4mm_status lut4_matmul_ex(const uint16_t *x, const uint8_t *packed, const float *scales,
+                           const float *book, uint16_t *y, int64_t M, int64_t N, int64_t K,
+                           int64_t block, int transpose, uint32_t flags, q4mm_stream_t stream);
+
 /* Standalone LUT4 decode (lut4.rs lookup4 decode kernel): out [rows, cols] of out_dtype,
  * out[f] = fl32(book[code(f)] * scales[f / block]) (F32 bit for bit; BF16/F16 rounded to
  * nearest even). */

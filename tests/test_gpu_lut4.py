@@ -76,12 +76,12 @@ def test_lut4_dequant_bit_exact(rows, cols, block):
             np.testing.assert_array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), conv(ref))
 
 
-@pytest.mark.parametrize("M", [1, 512])
-def test_lut4_full_size_sampled(M):
+@pytest.mark.parametrize("M,static_weights", [(1, False), (1, True), (512, False)])
+def test_lut4_full_size_sampled(M, static_weights):
     N = K = 4096
     x, packed, scales, book = _case(3000 + M, M, N, K)
     y = poisoned_bf16(M, N)
-    q.lut4_matmul(dev(x), dev(packed), dev(scales), book, y, N, K, 64, 1)
+    q.lut4_matmul(dev(x), dev(packed), dev(scales), book, y, N, K, 64, 1, static_weights=static_weights)
     got = bf16_out(y)
     assert np.all(np.isfinite(got))
     rng = np.random.default_rng(M)
@@ -89,3 +89,44 @@ def test_lut4_full_size_sampled(M):
     ni = rng.integers(0, N, 600)
     ref = oracle.lut4_matmul_at(x, packed, scales, book, N, K, 64, 1, mi, ni)
     assert_within_tolerance(got[mi, ni], ref, f"lut4 full M={M}")
+
+
+def _lut4_chain(M, D, layers, static_weights, graph=False):
+    """`layers` dependent D x D LUT4 decode matmuls on one stream, each reading the previous
+    call's output; two weight sets alternate.  Returns every activation as host uint16."""
+    sets = []
+    for i in range(2):
+        packed, scales, book = synth.lut4_weights(720 + i, D, D, 64)
+        sets.append((dev(packed), dev(scales), book))
+    x0 = dev(synth.activations_bf16(730, M, D))
+    bufs = [poisoned_bf16(M, D) for _ in range(layers + 1)]
+    bufs[0].copy_(x0)
+
+    def calls():
+        for i in range(layers):
+            P, S, book = sets[i % 2]
+            q.lut4_matmul(bufs[i], P, S, book, bufs[i + 1], D, D, 64, 1, static_weights=static_weights)
+
+    if graph:
+        st = torch.cuda.Stream()
+        st.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            calls()
+        torch.cuda.synchronize()
+        g.replay()
+    else:
+        calls()
+    torch.cuda.synchronize()
+    return [b.cpu().numpy().view(np.uint16).copy() for b in bufs]
+
+
+@pytest.mark.parametrize("M,D", [(1, 4096), (3, 1024), (8, 512)])
+def test_lut4_static_weights_chain_is_bit_identical(M, D):
+    """Overlapped launches (Q4MM_GEMV_STATIC_WEIGHTS) read x only after the producing call has
+    finished: a read-after-write chain gives exactly the plain launches' bits, also in a graph."""
+    plain = _lut4_chain(M, D, 5, False)
+    for graph in (False, True):
+        over = _lut4_chain(M, D, 5, True, graph=graph)
+        for a, b_ in zip(plain, over):
+            np.testing.assert_array_equal(a, b_)

@@ -89,12 +89,18 @@ def _book_ptr(book):
 
 
 def lut4_matmul(x, packed, scales, book, y, N: int, K: int, block: int, transpose: int,
-                stream=None) -> None:
-    """y[M, N] = x[M, K] . W^T with W[n][k] = fl32(book[code] * scale) (see q4mm.h)."""
+                stream=None, static_weights: bool = False) -> None:
+    """y[M, N] = x[M, K] . W^T with W[n][k] = fl32(book[code] * scale) (see q4mm.h).
+    static_weights=True: lut4_matmul_ex with Q4MM_GEMV_STATIC_WEIGHTS (see q4_gemv)."""
     M = x.shape[0]
     keep, bp = _book_ptr(book)
-    _check("lut4_matmul", lib().lut4_matmul(_ptr(x), _ptr(packed), _ptr(scales), bp, _ptr(y), M, N,
-                                            K, block, int(transpose), _stream(stream)))
+    if static_weights:
+        _check("lut4_matmul_ex", lib().lut4_matmul_ex(_ptr(x), _ptr(packed), _ptr(scales), bp, _ptr(y), M, N,
+                                                      K, block, int(transpose), GEMV_STATIC_WEIGHTS,
+                                                      _stream(stream)))
+    else:
+        _check("lut4_matmul", lib().lut4_matmul(_ptr(x), _ptr(packed), _ptr(scales), bp, _ptr(y), M, N,
+                                                K, block, int(transpose), _stream(stream)))
     del keep
 
 

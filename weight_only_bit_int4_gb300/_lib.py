@@ -21,6 +21,7 @@ SIGNATURES = {
     "q4_gemv_ex": ([_P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_uint32, _P], _S),
     "q4_gemm": ([_P, _P, _P, _P, _P, _I, _I, _I, _P], _S),
     "lut4_matmul": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _S, _P], _S),
+    "lut4_matmul_ex": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _S, ctypes.c_uint32, _P], _S),
     "lut4_dequant": ([_P, _P, _P, _I, _I, _I, _P, _S, _P], _S),
     "q4_0_route": ([_P, _I, _I, _P, _P, _P, _P], _S),
     "q4_0_matmul_id_workspace_size": ([_I, _I, _I, _I, _I], ctypes.c_size_t),

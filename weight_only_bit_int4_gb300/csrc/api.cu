@@ -138,6 +138,13 @@ static q4mm_status check_lut4(const uint8_t *packed, const float *scales, const 
 q4mm_status lut4_matmul(const uint16_t *x, const uint8_t *packed, const float *scales,
                         const float *book, uint16_t *y, int64_t M, int64_t N, int64_t K,
                         int64_t block, int transpose, q4mm_stream_t stream) {
+  return lut4_matmul_ex(x, packed, scales, book, y, M, N, K, block, transpose, 0u, stream);
+}
+
+q4mm_status lut4_matmul_ex(const uint16_t *x, const uint8_t *packed, const float *scales,
+                           const float *book, uint16_t *y, int64_t M, int64_t N, int64_t K,
+                           int64_t block, int transpose, uint32_t flags, q4mm_stream_t stream) {
+  if ((flags & ~Q4MM_GEMV_STATIC_WEIGHTS) != 0u) return Q4MM_ERR_INVALID_ARG;
   if (M == 0) return Q4MM_OK;
   if (M < 0 || M > kMaxDim || (transpose != 0 && transpose != 1)) return Q4MM_ERR_INVALID_ARG;
   const int64_t rows = transpose ? N : K, cols = transpose ? K : N;
@@ -150,7 +157,8 @@ q4mm_status lut4_matmul(const uint16_t *x, const uint8_t *packed, const float *s
   const bool fast = transpose == 1 && K % 32 == 0 && block % 32 == 0 && K % block == 0 &&
                     aligned(x, 16) && aligned(packed, 16) && aligned(y, 16);
   if (fast && M <= 16)
-    return from_cuda(launch_lut4_gemv(x, packed, scales, book, y, (int)M, (int)N, (int)K, (int)block, s));
+    return from_cuda(launch_lut4_gemv(x, packed, scales, book, y, (int)M, (int)N, (int)K, (int)block, s,
+                                      (flags & Q4MM_GEMV_STATIC_WEIGHTS) != 0u));
   if (fast && K % 64 == 0 && block % 64 == 0) {
     cudaError_t e = launch_lut4_gemm(x, packed, scales, book, y, (int)M, (int)N, (int)K, (int)block, s);
     if (e != cudaErrorNotSupported) return from_cuda(e);

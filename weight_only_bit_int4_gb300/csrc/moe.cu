@@ -494,6 +494,20 @@ __device__ __forceinline__ void cp_async_piece(uint32_t dst, const void *src, ui
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 
+// One chunk of 16 weight rows into a ring stage: PIECES copies of PIECE bytes per row
+// (compile-time counts, so the row/piece split of an item index is a multiply, not a divide).
+template <int PIECES, int PIECE>
+__device__ __forceinline__ void mv_copy_rows(uint32_t slot, const uint8_t *src, size_t row_bytes, int row0,
+                                             int N, int lane) {
+#pragma unroll 1
+  for (int i = lane; i < 16 * PIECES; i += 32) {
+    const int rr = i / PIECES, pc = i - rr * PIECES;
+    const bool ok = row0 + rr < N;
+    cp_async_piece<PIECE>(slot + (uint32_t)(rr * kMvcRow + pc * PIECE),
+                          ok ? src + (size_t)(row0 + rr) * row_bytes + pc * PIECE : src, ok ? (uint32_t)PIECE : 0u);
+  }
+}
+
 template <int KS, bool SWIGLU, int PIECE>
 __global__ void __launch_bounds__(KS * 32) q4_0_mv_mma_kernel(const __grid_constant__ MvParams p, int maxc) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -527,15 +541,11 @@ __global__ void __launch_bounds__(KS * 32) q4_0_mv_mma_kernel(const __grid_const
     auto issue = [&](int c) {
       const uint32_t slot = ring_s + (uint32_t)((c % kMvcDepth) * kMvcChunk);
       const int a = c_begin + c;
-      const int pieces = 2 * a + 1 < S4 ? kPiecesFull : kPiecesFull / 2;   // 4-block tail chunk
-      const size_t col0 = (size_t)a * kMvcRow;
-      for (int i = lane; i < 16 * pieces; i += 32) {
-        const int rr = i / pieces, pc = i - rr * pieces;
-        const int grow = row0 + rr;
-        const bool ok = grow < p.N;
-        cp_async_piece<PIECE>(slot + (uint32_t)(rr * kMvcRow + pc * PIECE),
-                              wexp + (ok ? (size_t)grow * row_bytes + col0 + pc * PIECE : 0), ok ? (uint32_t)PIECE : 0u);
-      }
+      const uint8_t *src = wexp + (size_t)a * kMvcRow;
+      if (2 * a + 1 < S4)
+        mv_copy_rows<kPiecesFull, PIECE>(slot, src, row_bytes, row0, p.N, lane);
+      else   // 4-block tail chunk
+        mv_copy_rows<kPiecesFull / 2, PIECE>(slot, src, row_bytes, row0, p.N, lane);
     };
 #pragma unroll
     for (int i = 0; i < kMvcDepth - 1; ++i) {
@@ -645,11 +655,11 @@ __global__ void __launch_bounds__(KS * 32) q4_0_mv_mma_kernel(const __grid_const
 
 template <bool SWIGLU, int PIECE>
 cudaError_t launch_mv_mma_typed(const MvParams &p, int ks, int maxc, size_t smem, cudaStream_t s) {
-  dim3 grid((unsigned)((p.N + 15) / 16), (unsigned)(p.n_rows < 65535 ? p.n_rows : 65535), 1);
   auto kern = ks == 4 ? q4_0_mv_mma_kernel<4, SWIGLU, PIECE>
             : ks == 2 ? q4_0_mv_mma_kernel<2, SWIGLU, PIECE> : q4_0_mv_mma_kernel<1, SWIGLU, PIECE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((p.N + 15) / 16), (unsigned)(p.n_rows < 65535 ? p.n_rows : 65535), 1);
   kern<<<grid, ks * 32, smem, s>>>(p, maxc);
   return cudaGetLastError();
 }
