@@ -339,6 +339,7 @@ def run_ours(args, rank, world, local_rank):
         out["prefill"] = bench_prefill(args, q, synth, to_dev, time_graph, dev, pk)
         out["lut4"] = bench_lut4(args, q, synth, to_dev, ring_of, time_graph, dev, pk)
         out["moe"] = bench_moe(args, q, synth, to_dev, ring_of, time_graph, dev, pk)
+        out["dispatch"] = bench_dispatch(q, synth, to_dev, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
     return out
@@ -407,6 +408,32 @@ def bench_prefill(args, q, synth, to_dev, time_graph, dev, pk):
             "aggregate_TFLOP_s": round(tot_f / tot_t / 1e12, 1),
             "aggregate_frac_bf16_burst": round(tot_f / tot_t / 1e12 / pk["bf16_tflops"], 3),
             "x": "bf16 N(0,1), 1% columns x20, seeded torch generator on device"}
+
+
+def bench_dispatch(q, synth, to_dev, dev, calls: int = 3000):
+    """Host time per call on the smallest decode shape (M=16, K=512, N=256, whose kernel is
+    shorter than its launch): the direct entry point, which plans every call, against a
+    dispatch record planned once.  Python -> ctypes -> C ABI both ways; the calls are
+    enqueued without synchronising, and the device is drained before and after."""
+    import torch
+    M, K, N = 16, 512, 256
+    w, s, b = synth.int4_weights(1000, N, K)
+    W = (to_dev(w), to_dev(s), to_dev(b))
+    x = to_dev(synth.activations_bf16(1001, M, K))
+    y = torch.empty((M, N), dtype=torch.int16, device=dev)
+    rec = q.q4_gemv_record(M, N, K)
+    res = {"shape": {"M": M, "K": K, "N": N}, "calls": calls}
+    for name, fn in (("direct_us", lambda: q.q4_gemv(x, *W, y)), ("record_us", lambda: rec.gemv(x, *W, y))):
+        for _ in range(50):
+            fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(calls):
+            fn()
+        res[name] = round((time.perf_counter() - t0) / calls * 1e6, 2)
+        torch.cuda.synchronize()
+    rec.close()
+    return res
 
 
 def bench_lut4(args, q, synth, to_dev, ring_of, time_graph, dev, pk):

@@ -217,6 +217,51 @@ q4mm_status q4_0_matmul_id_swiglu(const float *gate, const float *up, const void
                                   uint64_t expert_stride, q4mm_stream_t stream);
 
 /* ======================================================================================
+ * Dispatch records: plan a decode call once, replay it with new pointers.
+ *
+ * The counterpart of the pages' pre-baked decode dispatches (quantized_matmul_id_ggml.rs,
+ * `build_q6k_id_nr2_m1_record` and `build_q8_0_id_decode_record`: bake the load-time-
+ * immutable parts of a per-token call -- kernel, launch geometry, parameter block -- once,
+ * so each token's dispatch only binds buffers).  A record holds the planned kernel, grid,
+ * cluster shape, shared-memory size and launch attributes of one call shape; creating it
+ * also performs the kernel's one-time attribute set-up, so the first replay may be inside a
+ * stream capture.  A replay launches exactly the kernel the direct call would launch, with
+ * bit-identical results.
+ *
+ *   - Creation allocates one small HOST object (no device memory); free it with
+ *     q4mm_record_free.  A record may be replayed any number of times, from any host thread,
+ *     on any stream of the device that was current at creation (else Q4MM_ERR_DEVICE).
+ *   - Replays check pointers (null: Q4MM_ERR_INVALID_ARG; alignment: Q4MM_ERR_UNSUPPORTED)
+ *     but not buffer sizes: the buffers must have the recorded shape.
+ * ====================================================================================*/
+typedef struct q4mm_record q4mm_record;
+
+/* Record q4_gemv_ex(M, N, K, flags): 1 <= M <= 16, K % 32 == 0, flags as for q4_gemv_ex. */
+q4mm_status q4_gemv_record(int64_t M, int64_t N, int64_t K, uint32_t flags, q4mm_record **out);
+/* Replay: the q4_gemv_ex call the record was made for, on x, w, scales, biases, y (each
+ * 16-byte aligned, with the recorded shape). */
+q4mm_status q4_gemv_record_launch(const q4mm_record *rec, const uint16_t *x, const uint32_t *w,
+                                  const uint16_t *scales, const uint16_t *biases, uint16_t *y,
+                                  q4mm_stream_t stream);
+
+/* Record the routed Q4_0 mat-vec: q4_0_matmul_id in mode 1 (swiglu = 0) or
+ * q4_0_matmul_id_swiglu (swiglu = 1), with the argument rules of those calls.  The plan
+ * assumes the weight pointer of every replay is 16-byte aligned when K % 256 == 0 and
+ * expert_stride % 16 == 0, else 8-byte aligned when K % 128 == 0 and expert_stride % 8 == 0;
+ * a replay whose w breaks that returns Q4MM_ERR_UNSUPPORTED (the direct calls accept it). */
+q4mm_status q4_0_matmul_id_mv_record(int64_t n_tokens, int64_t top_k, int64_t N, int64_t K,
+                                     int64_t n_experts, uint64_t expert_stride, int swiglu,
+                                     q4mm_record **out);
+/* Replay: x is x [n_tokens, K] (swiglu = 0; up must be NULL) or gate [n_tokens*top_k, K]
+ * with up [n_tokens*top_k, K] (swiglu = 1). */
+q4mm_status q4_0_matmul_id_mv_record_launch(const q4mm_record *rec, const float *x, const float *up,
+                                            const void *w, const uint32_t *ids, float *out,
+                                            q4mm_stream_t stream);
+
+/* Release a record (NULL is a no-op).  Launches already enqueued are unaffected. */
+void q4mm_record_free(q4mm_record *rec);
+
+/* ======================================================================================
  * Allocation-free variant of the mat-mat form (the source pages have no counterpart).
  *
  * For callers that cannot obtain device memory at the moment of the call -- code running

@@ -90,3 +90,19 @@ def test_moe_argument_checks(L):
     assert L.q4_0_matmul_id_swiglu(None, None, None, None, None, 0, 8, 64, 64, 16, 0, None) == 0
     # routing: too many experts
     assert L.q4_0_route(FAKE, 8, 2000, FAKE, FAKE, None, None) == 1
+
+
+def test_record_argument_checks(L):
+    out = ctypes.c_void_p(123)
+    # bad shapes and flags are refused before any device work, and *out is cleared
+    assert L.q4_gemv_record(0, 64, 64, 0, ctypes.byref(out)) == 1 and out.value is None
+    assert L.q4_gemv_record(17, 64, 64, 0, ctypes.byref(out)) == 1
+    assert L.q4_gemv_record(1, 64, 48, 0, ctypes.byref(out)) == 1
+    assert L.q4_gemv_record(1, 64, 64, 0x2, ctypes.byref(out)) == 1
+    assert L.q4_gemv_record(1, 64, 64, 0, None) == 1
+    assert L.q4_0_matmul_id_mv_record(1, 8, 64, 64, 16, 64 * 2 * 18 - 1, 0, ctypes.byref(out)) == 1
+    assert L.q4_0_matmul_id_mv_record(1, 8, 64, 64, 16, 1 << 20, 2, ctypes.byref(out)) == 1
+    # launching without a record, and freeing NULL
+    assert L.q4_gemv_record_launch(None, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 1
+    assert L.q4_0_matmul_id_mv_record_launch(None, FAKE, None, FAKE, FAKE, FAKE, None) == 1
+    L.q4mm_record_free(None)

@@ -149,3 +149,46 @@ def q4_0_matmul_id_noalloc(x, w, ids, out, top_k: int, N: int, K: int, n_experts
     _check("q4_0_matmul_id_noalloc", lib().q4_0_matmul_id_noalloc(
         _ptr(x), _ptr(w), _ptr(ids), _ptr(out), n_tokens, top_k, N, K, n_experts, expert_stride,
         _stream(stream)))
+
+
+class Record:
+    """A dispatch record (q4mm.h): one decode call planned once, replayed with new tensors.
+    Owns the library's host-side record and frees it when garbage-collected or closed."""
+
+    def __init__(self, kind: str, handle: int):
+        self.kind = kind
+        self._h = handle
+
+    def close(self) -> None:
+        if self._h:
+            lib().q4mm_record_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def gemv(self, x, w, scales, biases, y, stream=None) -> None:
+        _check("q4_gemv_record_launch", lib().q4_gemv_record_launch(
+            self._h, _ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(y), _stream(stream)))
+
+    def matmul_id_mv(self, x, w, ids, out, up=None, stream=None) -> None:
+        _check("q4_0_matmul_id_mv_record_launch", lib().q4_0_matmul_id_mv_record_launch(
+            self._h, _ptr(x), _ptr(up), _ptr(w), _ptr(ids), _ptr(out), _stream(stream)))
+
+
+def q4_gemv_record(M: int, N: int, K: int, static_weights: bool = False) -> Record:
+    h = ctypes.c_void_p()
+    _check("q4_gemv_record", lib().q4_gemv_record(M, N, K, GEMV_STATIC_WEIGHTS if static_weights else 0,
+                                                  ctypes.byref(h)))
+    return Record("gemv", h.value)
+
+
+def q4_0_matmul_id_mv_record(n_tokens: int, top_k: int, N: int, K: int, n_experts: int,
+                             expert_stride: int, swiglu: bool = False) -> Record:
+    h = ctypes.c_void_p()
+    _check("q4_0_matmul_id_mv_record", lib().q4_0_matmul_id_mv_record(
+        n_tokens, top_k, N, K, n_experts, expert_stride, int(swiglu), ctypes.byref(h)))
+    return Record("swiglu" if swiglu else "mv", h.value)

@@ -11,6 +11,8 @@
 
 #include <stdint.h>
 
+#include <new>
+
 using namespace q4mm;
 
 namespace {
@@ -250,6 +252,111 @@ q4mm_status q4_0_matmul_id_swiglu(const float *gate, const float *up, const void
   return from_cuda(launch_q4_0_swiglu_mv(gate, up, static_cast<const uint8_t *>(w), ids, out,
                                          (int)(n_tokens * top_k), (int)N, (int)K, (int)n_experts,
                                          expert_stride, (cudaStream_t)stream));
+}
+
+// ------------------------------------------------------------------------------------------
+// Dispatch records
+// ------------------------------------------------------------------------------------------
+struct q4mm_record {
+  int kind;      // kRecGemv, kRecMv or kRecSwiglu
+  int device;    // the device current at creation; launches need it current again
+  int w_align;   // alignment the weight pointer of every launch must keep
+  void *impl;
+};
+
+namespace {
+constexpr int kRecGemv = 1, kRecMv = 2, kRecSwiglu = 3;
+
+q4mm_status check_record(const q4mm_record *rec, int kind) {
+  if (!rec || rec->kind != kind) return Q4MM_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return Q4MM_ERR_CUDA;
+  return dev == rec->device ? Q4MM_OK : Q4MM_ERR_DEVICE;
+}
+}  // namespace
+
+q4mm_status q4_gemv_record(int64_t M, int64_t N, int64_t K, uint32_t flags, q4mm_record **out) {
+  if (!out) return Q4MM_ERR_INVALID_ARG;
+  *out = nullptr;
+  if ((flags & ~Q4MM_GEMV_STATIC_WEIGHTS) != 0u) return Q4MM_ERR_INVALID_ARG;
+  if (M < 1 || M > 16 || N < 1 || N > kMaxDim || K < 32 || K > kMaxDim || K % 32 != 0) return Q4MM_ERR_INVALID_ARG;
+  q4mm_status st = check_device();
+  if (st != Q4MM_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return Q4MM_ERR_CUDA;
+  void *impl = nullptr;
+  if (record_q4_gemv((int)M, (int)N, (int)K, (flags & Q4MM_GEMV_STATIC_WEIGHTS) != 0u, &impl) != cudaSuccess)
+    return Q4MM_ERR_CUDA;
+  q4mm_record *rec = new (std::nothrow) q4mm_record{kRecGemv, dev, 16, impl};
+  if (!rec) {
+    free_q4_gemv_record(impl);
+    return Q4MM_ERR_CUDA;
+  }
+  *out = rec;
+  return Q4MM_OK;
+}
+
+q4mm_status q4_gemv_record_launch(const q4mm_record *rec, const uint16_t *x, const uint32_t *w,
+                                  const uint16_t *scales, const uint16_t *biases, uint16_t *y,
+                                  q4mm_stream_t stream) {
+  q4mm_status st = check_record(rec, kRecGemv);
+  if (st != Q4MM_OK) return st;
+  if (!x || !w || !scales || !biases || !y) return Q4MM_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(scales, 16) || !aligned(biases, 16) || !aligned(y, 16))
+    return Q4MM_ERR_UNSUPPORTED;
+  return from_cuda(replay_q4_gemv(rec->impl, x, w, scales, biases, y, (cudaStream_t)stream));
+}
+
+q4mm_status q4_0_matmul_id_mv_record(int64_t n_tokens, int64_t top_k, int64_t N, int64_t K,
+                                     int64_t n_experts, uint64_t expert_stride, int swiglu,
+                                     q4mm_record **out) {
+  if (!out) return Q4MM_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (swiglu != 0 && swiglu != 1) return Q4MM_ERR_INVALID_ARG;
+  if (n_tokens < 1 || top_k < 1 || N < 1 || K < 32 || K % 32 != 0 || n_experts < 1 || n_experts > 1024 ||
+      N > kMaxDim || K > kMaxDim || n_tokens * top_k > (int64_t(1) << 24))
+    return Q4MM_ERR_INVALID_ARG;
+  if (expert_stride < (uint64_t)N * (uint64_t)(K / 32) * 18u) return Q4MM_ERR_INVALID_ARG;
+  q4mm_status st = check_device();
+  if (st != Q4MM_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return Q4MM_ERR_CUDA;
+  void *impl = nullptr;
+  int w_align = 1;
+  if (record_q4_0_mv((int)(n_tokens * top_k), swiglu ? 1 : (int)top_k, (int)N, (int)K, (int)n_experts,
+                     expert_stride, swiglu != 0, &w_align, &impl) != cudaSuccess)
+    return Q4MM_ERR_CUDA;
+  q4mm_record *rec = new (std::nothrow) q4mm_record{swiglu ? kRecSwiglu : kRecMv, dev, w_align, impl};
+  if (!rec) {
+    free_q4_0_mv_record(impl);
+    return Q4MM_ERR_CUDA;
+  }
+  *out = rec;
+  return Q4MM_OK;
+}
+
+q4mm_status q4_0_matmul_id_mv_record_launch(const q4mm_record *rec, const float *x, const float *up,
+                                            const void *w, const uint32_t *ids, float *out,
+                                            q4mm_stream_t stream) {
+  if (!rec || (rec->kind != kRecMv && rec->kind != kRecSwiglu)) return Q4MM_ERR_INVALID_ARG;
+  q4mm_status st = check_record(rec, rec->kind);
+  if (st != Q4MM_OK) return st;
+  const bool swiglu = rec->kind == kRecSwiglu;
+  if (!x || !w || !ids || !out || (swiglu && !up) || (!swiglu && up)) return Q4MM_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(ids, 4) || (swiglu && !aligned(up, 16)) ||
+      !aligned(w, (uintptr_t)rec->w_align))
+    return Q4MM_ERR_UNSUPPORTED;
+  return from_cuda(replay_q4_0_mv(rec->impl, x, up, static_cast<const uint8_t *>(w), ids, out,
+                                  (cudaStream_t)stream));
+}
+
+void q4mm_record_free(q4mm_record *rec) {
+  if (!rec) return;
+  if (rec->kind == kRecGemv)
+    free_q4_gemv_record(rec->impl);
+  else
+    free_q4_0_mv_record(rec->impl);
+  delete rec;
 }
 
 }  // extern "C"

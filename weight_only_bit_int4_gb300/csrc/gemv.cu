@@ -21,6 +21,8 @@
 //     no atomics).
 #include "q4mm_internal.cuh"
 
+#include <new>
+
 #include <algorithm>
 
 namespace q4mm {
@@ -1319,6 +1321,28 @@ __global__ void __launch_bounds__(KS * 32) gemv_lks_kernel(const __grid_constant
   if (gridDim.y > 1) cluster_sum_store<16>(p, red);
 }
 
+// A planned decode launch kept for replay (a dispatch record): the kernel, its launch
+// configuration and attributes, and the shape part of its parameters.  Recording runs the
+// same planning and per-kernel attribute set-up as a call, then stops short of the launch.
+struct LaunchSpec {
+  const void *fn = nullptr;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[2]{};
+  GemvParams params{};
+};
+
+template <typename Kern>
+cudaError_t launch_or_record(const cudaLaunchConfig_t &cfg, Kern kern, const GemvParams &p, LaunchSpec *rec) {
+  if (rec == nullptr) return cudaLaunchKernelEx(&cfg, kern, p);
+  rec->fn = reinterpret_cast<const void *>(kern);
+  rec->cfg = cfg;
+  rec->cfg.numAttrs = cfg.numAttrs < 2 ? cfg.numAttrs : 2;
+  for (unsigned i = 0; i < rec->cfg.numAttrs; ++i) rec->attr[i] = cfg.attrs[i];
+  rec->cfg.attrs = nullptr;   // re-pointed at rec->attr by each replay
+  rec->params = p;
+  return cudaSuccess;
+}
+
 struct Plan {
   int MT, RT, S, max_chunks;
   size_t smem;
@@ -1372,7 +1396,7 @@ Plan make_plan(int M, int N, int K) {
 }
 
 template <int MT, int RT, bool LUT>
-cudaError_t launch_typed(const GemvParams &p, const Plan &pl, cudaStream_t s, bool overlap) {
+cudaError_t launch_typed(const GemvParams &p, const Plan &pl, cudaStream_t s, bool overlap, LaunchSpec *rec) {
   auto kern = gemv_kernel<MT, RT, LUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   if (e != cudaSuccess) return e;
@@ -1391,7 +1415,7 @@ cudaError_t launch_typed(const GemvParams &p, const Plan &pl, cudaStream_t s, bo
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  return launch_or_record(cfg, kern, p, rec);
 }
 
 size_t async_smem_bytes(int M, int MT, int RT, int max_chunks, bool sb) {
@@ -1463,7 +1487,7 @@ Plan make_async_plan(int M, int N, int K, bool gc, bool sb) {
 }
 
 template <int MT, int RT, bool LUT>
-cudaError_t launch_async_typed(const GemvParams &p, const Plan &pl, cudaStream_t s, bool overlap) {
+cudaError_t launch_async_typed(const GemvParams &p, const Plan &pl, cudaStream_t s, bool overlap, LaunchSpec *rec) {
   auto kern = gemv_async_kernel<MT, RT, LUT, false>;
   if constexpr (!LUT) {
     if (p.K % 256 == 0) kern = gemv_async_kernel<MT, RT, false, true>;
@@ -1484,7 +1508,7 @@ cudaError_t launch_async_typed(const GemvParams &p, const Plan &pl, cudaStream_t
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  return launch_or_record(cfg, kern, p, rec);
 }
 
 size_t gc_smem_bytes(int M, int RT, int max_chunks) {   // the larger of the two layouts (SB)
@@ -1493,7 +1517,7 @@ size_t gc_smem_bytes(int M, int RT, int max_chunks) {   // the larger of the two
 }
 
 template <int MT2, int RT>
-cudaError_t launch_gc_typed(const GemvParams &p, const Plan &pl, cudaStream_t s, bool overlap) {
+cudaError_t launch_gc_typed(const GemvParams &p, const Plan &pl, cudaStream_t s, bool overlap, LaunchSpec *rec) {
   const bool sb = p.K % 256 == 0 && (reinterpret_cast<uintptr_t>(p.scales) & 15u) == 0 &&
                   (reinterpret_cast<uintptr_t>(p.biases) & 15u) == 0;
   auto kern = sb ? gemv_gc_kernel<MT2, RT, true> : gemv_gc_kernel<MT2, RT, false>;
@@ -1514,7 +1538,7 @@ cudaError_t launch_gc_typed(const GemvParams &p, const Plan &pl, cudaStream_t s,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  return launch_or_record(cfg, kern, p, rec);
 }
 
 struct KsPlan {
@@ -1566,7 +1590,7 @@ KsPlan make_ks_plan(int M, int N, int K) {
 }
 
 template <int MT2, int KS, int DEPTH>
-cudaError_t launch_ks_typed(const GemvParams &p, const KsPlan &pl, cudaStream_t s, bool overlap) {
+cudaError_t launch_ks_typed(const GemvParams &p, const KsPlan &pl, cudaStream_t s, bool overlap, LaunchSpec *rec) {
   auto kern = gemv_ks_kernel<MT2, KS, DEPTH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   if (e != cudaSuccess) return e;
@@ -1591,19 +1615,19 @@ cudaError_t launch_ks_typed(const GemvParams &p, const KsPlan &pl, cudaStream_t 
   }
   cfg.attrs = attr;
   cfg.numAttrs = (unsigned)n;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  return launch_or_record(cfg, kern, p, rec);
 }
 
 template <int MT2>
-cudaError_t launch_ks(const GemvParams &p, const KsPlan &pl, cudaStream_t s, bool overlap) {
+cudaError_t launch_ks(const GemvParams &p, const KsPlan &pl, cudaStream_t s, bool overlap, LaunchSpec *rec) {
   if (pl.depth == 4) {
-    if (pl.KS == 2) return launch_ks_typed<MT2, 2, 4>(p, pl, s, overlap);
-    if (pl.KS == 4) return launch_ks_typed<MT2, 4, 4>(p, pl, s, overlap);
-    return launch_ks_typed<MT2, 8, 4>(p, pl, s, overlap);
+    if (pl.KS == 2) return launch_ks_typed<MT2, 2, 4>(p, pl, s, overlap, rec);
+    if (pl.KS == 4) return launch_ks_typed<MT2, 4, 4>(p, pl, s, overlap, rec);
+    return launch_ks_typed<MT2, 8, 4>(p, pl, s, overlap, rec);
   }
-  if (pl.KS == 2) return launch_ks_typed<MT2, 2, 8>(p, pl, s, overlap);
-  if (pl.KS == 4) return launch_ks_typed<MT2, 4, 8>(p, pl, s, overlap);
-  return launch_ks_typed<MT2, 8, 8>(p, pl, s, overlap);
+  if (pl.KS == 2) return launch_ks_typed<MT2, 2, 8>(p, pl, s, overlap, rec);
+  if (pl.KS == 4) return launch_ks_typed<MT2, 4, 8>(p, pl, s, overlap, rec);
+  return launch_ks_typed<MT2, 8, 8>(p, pl, s, overlap, rec);
 }
 
 // Plans for gemv_lks_kernel: the K-split plan search with the codebook table in each CTA.
@@ -1649,7 +1673,7 @@ KsPlan make_lks_plan(int M, int N, int K, int block) {
 }
 
 template <int MT2, int KS, int DEPTH>
-cudaError_t launch_lks_typed(const GemvParams &p, const KsPlan &pl, cudaStream_t s, bool overlap) {
+cudaError_t launch_lks_typed(const GemvParams &p, const KsPlan &pl, cudaStream_t s, bool overlap, LaunchSpec *rec) {
   auto kern = gemv_lks_kernel<MT2, KS, DEPTH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   if (e != cudaSuccess) return e;
@@ -1674,23 +1698,23 @@ cudaError_t launch_lks_typed(const GemvParams &p, const KsPlan &pl, cudaStream_t
   }
   cfg.attrs = attr;
   cfg.numAttrs = (unsigned)n;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  return launch_or_record(cfg, kern, p, rec);
 }
 
 template <int MT2>
-cudaError_t launch_lks(const GemvParams &p, const KsPlan &pl, cudaStream_t s, bool overlap) {
+cudaError_t launch_lks(const GemvParams &p, const KsPlan &pl, cudaStream_t s, bool overlap, LaunchSpec *rec) {
   if (pl.depth == 4) {
-    if (pl.KS == 2) return launch_lks_typed<MT2, 2, 4>(p, pl, s, overlap);
-    if (pl.KS == 4) return launch_lks_typed<MT2, 4, 4>(p, pl, s, overlap);
-    return launch_lks_typed<MT2, 8, 4>(p, pl, s, overlap);
+    if (pl.KS == 2) return launch_lks_typed<MT2, 2, 4>(p, pl, s, overlap, rec);
+    if (pl.KS == 4) return launch_lks_typed<MT2, 4, 4>(p, pl, s, overlap, rec);
+    return launch_lks_typed<MT2, 8, 4>(p, pl, s, overlap, rec);
   }
-  if (pl.KS == 2) return launch_lks_typed<MT2, 2, 8>(p, pl, s, overlap);
-  if (pl.KS == 4) return launch_lks_typed<MT2, 4, 8>(p, pl, s, overlap);
-  return launch_lks_typed<MT2, 8, 8>(p, pl, s, overlap);
+  if (pl.KS == 2) return launch_lks_typed<MT2, 2, 8>(p, pl, s, overlap, rec);
+  if (pl.KS == 4) return launch_lks_typed<MT2, 4, 8>(p, pl, s, overlap, rec);
+  return launch_lks_typed<MT2, 8, 8>(p, pl, s, overlap, rec);
 }
 
 template <bool LUT>
-cudaError_t launch_any(GemvParams &p, cudaStream_t s, bool overlap) {
+cudaError_t launch_any(GemvParams &p, cudaStream_t s, bool overlap, LaunchSpec *rec = nullptr) {
   p.chunks = (p.K / 32 + 3) / 4;
   if (LUT && p.M <= 4 && p.K % 512 == 0 &&
       (p.lut_block_shift_div == 1 || p.lut_block_shift_div == 2 || p.lut_block_shift_div == 4) &&
@@ -1698,14 +1722,14 @@ cudaError_t launch_any(GemvParams &p, cudaStream_t s, bool overlap) {
     const KsPlan kp = make_lks_plan(p.M, p.N, p.K, p.lut_block_shift_div * 32);
     if (kp.KS > 0) {
       p.max_chunks_per_cta = kp.maxc;
-      return p.M <= 2 ? launch_lks<1>(p, kp, s, overlap) : launch_lks<2>(p, kp, s, overlap);
+      return p.M <= 2 ? launch_lks<1>(p, kp, s, overlap, rec) : launch_lks<2>(p, kp, s, overlap, rec);
     }
   }
   if (!LUT && p.M <= 4 && p.K % 256 == 0) {
     const KsPlan kp = make_ks_plan(p.M, p.N, p.K);
     if (kp.KS > 0) {
       p.max_chunks_per_cta = kp.maxc;
-      return p.M <= 2 ? launch_ks<1>(p, kp, s, overlap) : launch_ks<2>(p, kp, s, overlap);
+      return p.M <= 2 ? launch_ks<1>(p, kp, s, overlap, rec) : launch_ks<2>(p, kp, s, overlap, rec);
     }
   }
   const bool lut_ok = !LUT || (p.lut_block_shift_div == 1 || p.lut_block_shift_div == 2 ||
@@ -1717,20 +1741,20 @@ cudaError_t launch_any(GemvParams &p, cudaStream_t s, bool overlap) {
       p.max_chunks_per_cta = pa.max_chunks;
       if (!LUT && p.M <= 4) {
         if (p.M <= 2)
-          return pa.RT == 2 ? launch_gc_typed<1, 2>(p, pa, s, overlap) : launch_gc_typed<1, 1>(p, pa, s, overlap);
-        return pa.RT == 2 ? launch_gc_typed<2, 2>(p, pa, s, overlap) : launch_gc_typed<2, 1>(p, pa, s, overlap);
+          return pa.RT == 2 ? launch_gc_typed<1, 2>(p, pa, s, overlap, rec) : launch_gc_typed<1, 1>(p, pa, s, overlap, rec);
+        return pa.RT == 2 ? launch_gc_typed<2, 2>(p, pa, s, overlap, rec) : launch_gc_typed<2, 1>(p, pa, s, overlap, rec);
       }
       if (pa.MT == 1)
-        return pa.RT == 2 ? launch_async_typed<1, 2, LUT>(p, pa, s, overlap) : launch_async_typed<1, 1, LUT>(p, pa, s, overlap);
-      return pa.RT == 2 ? launch_async_typed<2, 2, LUT>(p, pa, s, overlap) : launch_async_typed<2, 1, LUT>(p, pa, s, overlap);
+        return pa.RT == 2 ? launch_async_typed<1, 2, LUT>(p, pa, s, overlap, rec) : launch_async_typed<1, 1, LUT>(p, pa, s, overlap, rec);
+      return pa.RT == 2 ? launch_async_typed<2, 2, LUT>(p, pa, s, overlap, rec) : launch_async_typed<2, 1, LUT>(p, pa, s, overlap, rec);
     }
   }
   const Plan pl = make_plan(p.M, p.N, p.K);
   p.max_chunks_per_cta = pl.max_chunks;
   if (pl.MT == 1) {
-    return pl.RT == 2 ? launch_typed<1, 2, LUT>(p, pl, s, overlap) : launch_typed<1, 1, LUT>(p, pl, s, overlap);
+    return pl.RT == 2 ? launch_typed<1, 2, LUT>(p, pl, s, overlap, rec) : launch_typed<1, 1, LUT>(p, pl, s, overlap, rec);
   }
-  return pl.RT == 2 ? launch_typed<2, 2, LUT>(p, pl, s, overlap) : launch_typed<2, 1, LUT>(p, pl, s, overlap);
+  return pl.RT == 2 ? launch_typed<2, 2, LUT>(p, pl, s, overlap, rec) : launch_typed<2, 1, LUT>(p, pl, s, overlap, rec);
 }
 
 }  // namespace
@@ -1747,6 +1771,40 @@ cudaError_t launch_q4_gemv(const uint16_t *x, const uint32_t *w, const uint16_t 
   p.M = M; p.N = N; p.K = K;
   return launch_any<false>(p, s, overlap);
 }
+
+// Dispatch records for q4_gemv: plan once (kernel choice, grid, cluster, shared memory,
+// the kernel's attribute set-up), then replay with new pointers.
+cudaError_t record_q4_gemv(int M, int N, int K, bool overlap, void **out) {
+  GemvParams p{};
+  p.M = M; p.N = N; p.K = K;
+  LaunchSpec *rec = new (std::nothrow) LaunchSpec();
+  if (rec == nullptr) return cudaErrorMemoryAllocation;
+  const cudaError_t e = launch_any<false>(p, nullptr, overlap, rec);
+  if (e != cudaSuccess || rec->fn == nullptr) {
+    delete rec;
+    return e != cudaSuccess ? e : cudaErrorInvalidValue;
+  }
+  *out = rec;
+  return cudaSuccess;
+}
+
+cudaError_t replay_q4_gemv(const void *record, const uint16_t *x, const uint32_t *w, const uint16_t *scales,
+                           const uint16_t *biases, uint16_t *y, cudaStream_t s) {
+  const LaunchSpec *rec = static_cast<const LaunchSpec *>(record);
+  GemvParams p = rec->params;
+  p.x = x;
+  p.w = reinterpret_cast<const uint8_t *>(w);
+  p.scales = scales;
+  p.biases = biases;
+  p.y = y;
+  cudaLaunchConfig_t cfg = rec->cfg;
+  cfg.attrs = const_cast<cudaLaunchAttribute *>(rec->attr);
+  cfg.stream = s;
+  void *args[] = {&p};
+  return cudaLaunchKernelExC(&cfg, rec->fn, args);
+}
+
+void free_q4_gemv_record(void *record) { delete static_cast<LaunchSpec *>(record); }
 
 cudaError_t launch_lut4_gemv(const uint16_t *x, const uint8_t *packed, const float *scales,
                              const float *book, uint16_t *y, int M, int N, int K, int block,

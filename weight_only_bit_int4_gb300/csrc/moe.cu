@@ -13,6 +13,8 @@
 //    reused across the 32 weight rows.
 #include "q4mm_internal.cuh"
 
+#include <new>
+
 namespace q4mm {
 
 size_t q4_0_mm_workspace_bytes(int64_t n_tokens, int64_t top_k, int64_t N, int64_t K,
@@ -653,21 +655,46 @@ __global__ void __launch_bounds__(KS * 32) q4_0_mv_mma_kernel(const __grid_const
   }
 }
 
+// A planned mat-vec launch: kernel, grid, shared memory and the shape part of the
+// parameters (also kept as a dispatch record and replayed with new pointers).
+struct MvSpec {
+  const void *fn = nullptr;
+  dim3 grid, block;
+  size_t smem = 0;
+  int maxc = 0;          // tensor-core kernel: chunks per warp (its second argument)
+  bool mma = false;
+  int w_align = 4;       // alignment the weight pointer must keep for this kernel
+  MvParams params{};
+};
+
+cudaError_t run_mv_spec(const MvSpec &sp, const MvParams &p, cudaStream_t s) {
+  MvParams pp = p;
+  int maxc = sp.maxc;
+  void *args[] = {&pp, &maxc};
+  return cudaLaunchKernel(sp.fn, sp.grid, sp.block, args, sp.smem, s);
+}
+
 template <bool SWIGLU, int PIECE>
-cudaError_t launch_mv_mma_typed(const MvParams &p, int ks, int maxc, size_t smem, cudaStream_t s) {
+cudaError_t plan_mv_mma_typed(const MvParams &p, int ks, int maxc, size_t smem, MvSpec *sp) {
   auto kern = ks == 4 ? q4_0_mv_mma_kernel<4, SWIGLU, PIECE>
             : ks == 2 ? q4_0_mv_mma_kernel<2, SWIGLU, PIECE> : q4_0_mv_mma_kernel<1, SWIGLU, PIECE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((p.N + 15) / 16), (unsigned)(p.n_rows < 65535 ? p.n_rows : 65535), 1);
-  kern<<<grid, ks * 32, smem, s>>>(p, maxc);
-  return cudaGetLastError();
+  sp->fn = reinterpret_cast<const void *>(kern);
+  sp->grid = dim3((unsigned)((p.N + 15) / 16), (unsigned)(p.n_rows < 65535 ? p.n_rows : 65535), 1);
+  sp->block = dim3(ks * 32);
+  sp->smem = smem;
+  sp->maxc = maxc;
+  sp->mma = true;
+  sp->w_align = PIECE;
+  sp->params = p;
+  return cudaSuccess;
 }
 
 // Tensor-core mat-vec when the rows allow it (K % 128 == 0; 16-byte copies need K % 256 == 0
 // and 16-byte aligned slabs, 8-byte copies 8-byte aligned ones), else the fp32 FMA kernel.
 template <bool SWIGLU>
-cudaError_t launch_mv_any(const MvParams &p, cudaStream_t s) {
+cudaError_t plan_mv_any(const MvParams &p, MvSpec *sp) {
   const uintptr_t wa = reinterpret_cast<uintptr_t>(p.w);
   const bool a16 = p.K % 256 == 0 && p.expert_stride % 16 == 0 && (wa & 15) == 0;
   const bool a8 = p.K % 128 == 0 && p.expert_stride % 8 == 0 && (wa & 7) == 0;
@@ -677,13 +704,28 @@ cudaError_t launch_mv_any(const MvParams &p, cudaStream_t s) {
     const int maxc = (C + ks - 1) / ks;
     const size_t smem = (size_t)ks * mvc_warp_bytes(maxc) + (size_t)ks * 16 * 4;
     if (smem <= 227 * 1024)
-      return a16 ? launch_mv_mma_typed<SWIGLU, 16>(p, ks, maxc, smem, s)
-                 : launch_mv_mma_typed<SWIGLU, 8>(p, ks, maxc, smem, s);
+      return a16 ? plan_mv_mma_typed<SWIGLU, 16>(p, ks, maxc, smem, sp)
+                 : plan_mv_mma_typed<SWIGLU, 8>(p, ks, maxc, smem, sp);
   }
   const int rows_cta = kMvWarps * kMvRowsPerWarp;
-  dim3 grid((unsigned)((p.N + rows_cta - 1) / rows_cta), (unsigned)(p.n_rows < 65535 ? p.n_rows : 65535), 1);
-  q4_0_mv_kernel<SWIGLU><<<grid, kMvWarps * 32, 0, s>>>(p);
-  return cudaGetLastError();
+  sp->fn = reinterpret_cast<const void *>(q4_0_mv_kernel<SWIGLU>);
+  sp->grid = dim3((unsigned)((p.N + rows_cta - 1) / rows_cta), (unsigned)(p.n_rows < 65535 ? p.n_rows : 65535), 1);
+  sp->block = dim3(kMvWarps * 32);
+  sp->smem = 0;
+  sp->maxc = 0;
+  sp->mma = false;
+  sp->w_align = 1;
+  sp->params = p;
+  return cudaSuccess;
+}
+
+template <bool SWIGLU>
+cudaError_t launch_mv_any(const MvParams &p, cudaStream_t s) {
+  MvSpec sp;
+  const cudaError_t e = plan_mv_any<SWIGLU>(p, &sp);
+  if (e != cudaSuccess) return e;
+  const cudaError_t e2 = run_mv_spec(sp, p, s);
+  return e2 != cudaSuccess ? e2 : cudaGetLastError();
 }
 
 cudaError_t launch_q4_0_mv(const float *x, const uint8_t *w, const uint32_t *ids, float *out,
@@ -737,5 +779,37 @@ cudaError_t launch_q4_0_mm(const float *x, const uint8_t *w, const uint32_t *ids
   q4_0_mv_kernel<false><<<grid, kMvWarps * 32, 0, s>>>(p);
   return cudaGetLastError();
 }
+
+// Dispatch records for the routed mat-vec (quantized_matmul_id_ggml.rs pre-bakes its decode
+// mat-vec dispatches the same way): planned for a shape, an expert stride and a weight
+// alignment, replayed with new pointers.  *w_align reports the alignment every replayed
+// weight pointer must keep (the kernel choice depends on it).
+cudaError_t record_q4_0_mv(int n_rows, int top_k, int N, int K, int n_experts, uint64_t expert_stride,
+                           bool swiglu, int *w_align, void **out) {
+  MvParams p{};
+  p.w = nullptr;   // planned as if 16-byte aligned; replay checks the pointer against w_align
+  p.n_rows = n_rows; p.top_k = top_k; p.N = N; p.K = K; p.E = n_experts;
+  p.expert_stride = expert_stride;
+  MvSpec *sp = new (std::nothrow) MvSpec();
+  if (sp == nullptr) return cudaErrorMemoryAllocation;
+  const cudaError_t e = swiglu ? plan_mv_any<true>(p, sp) : plan_mv_any<false>(p, sp);
+  if (e != cudaSuccess) {
+    delete sp;
+    return e;
+  }
+  *w_align = sp->w_align;
+  *out = sp;
+  return cudaSuccess;
+}
+
+cudaError_t replay_q4_0_mv(const void *record, const float *x, const float *up, const uint8_t *w,
+                           const uint32_t *ids, float *out, cudaStream_t s) {
+  const MvSpec *sp = static_cast<const MvSpec *>(record);
+  MvParams p = sp->params;
+  p.x = x; p.up = up; p.w = w; p.ids = ids; p.out = out; p.order = nullptr; p.n_order = nullptr;
+  return run_mv_spec(*sp, p, s);
+}
+
+void free_q4_0_mv_record(void *record) { delete static_cast<MvSpec *>(record); }
 
 }  // namespace q4mm

@@ -204,6 +204,18 @@ cudaError_t launch_q4_gemv(const uint16_t *x, const uint32_t *w, const uint16_t 
                            const uint16_t *biases, uint16_t *y, int M, int N, int K,
                            cudaStream_t s, bool overlap = false);
 
+// Dispatch records (plan once, replay with new pointers).  The record is a host object
+// owned by the caller of record_*; replay_* launches exactly what the planned call would.
+cudaError_t record_q4_gemv(int M, int N, int K, bool overlap, void **out);
+cudaError_t replay_q4_gemv(const void *record, const uint16_t *x, const uint32_t *w, const uint16_t *scales,
+                           const uint16_t *biases, uint16_t *y, cudaStream_t s);
+void free_q4_gemv_record(void *record);
+cudaError_t record_q4_0_mv(int n_rows, int top_k, int N, int K, int n_experts, uint64_t expert_stride,
+                           bool swiglu, int *w_align, void **out);
+cudaError_t replay_q4_0_mv(const void *record, const float *x, const float *up, const uint8_t *w,
+                           const uint32_t *ids, float *out, cudaStream_t s);
+void free_q4_0_mv_record(void *record);
+
 cudaError_t launch_lut4_gemv(const uint16_t *x, const uint8_t *packed, const float *scales,
                              const float *book, uint16_t *y, int M, int N, int K, int block,
                              cudaStream_t s, bool overlap = false);
