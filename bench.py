@@ -339,7 +339,7 @@ def run_ours(args, rank, world, local_rank):
         out["prefill"] = bench_prefill(args, q, synth, to_dev, time_graph, dev, pk)
         out["lut4"] = bench_lut4(args, q, synth, to_dev, ring_of, time_graph, dev, pk)
         out["moe"] = bench_moe(args, q, synth, to_dev, ring_of, time_graph, dev, pk)
-        out["dispatch"] = bench_dispatch(q, synth, to_dev, dev)
+        out["dispatch"] = bench_dispatch(q, synth, to_dev, dev, calls=10 if eager else 3000)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
     return out
@@ -424,7 +424,7 @@ def bench_dispatch(q, synth, to_dev, dev, calls: int = 3000):
     rec = q.q4_gemv_record(M, N, K)
     res = {"shape": {"M": M, "K": K, "N": N}, "calls": calls}
     for name, fn in (("direct_us", lambda: q.q4_gemv(x, *W, y)), ("record_us", lambda: rec.gemv(x, *W, y))):
-        for _ in range(50):
+        for _ in range(min(50, calls)):
             fn()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
