@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libq4mm (declared in include/q4mm.h): host-side argument checks,
-// then launches on the caller's stream.  Nothing here allocates or synchronises (except
-// q4mm_device_errors, a diagnostics call).
+// then launches on the caller's stream.  Nothing here allocates device memory or
+// synchronises (except q4mm_device_errors, a diagnostics call); dispatch records are small
+// host objects.
 //
 // The checks mirror the pages' own gates: quant_fastkernel.rs `eligible` (group size 32,
 // K a multiple of 32, bf16 activations/scales/biases, uint32 weights) and

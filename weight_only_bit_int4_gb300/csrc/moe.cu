@@ -7,10 +7,13 @@
 // of byte j, element 16+j its high nibble; value = (q - 8) * d.
 //
 //  * q4_0_route: the map0 stage of `dispatch_id_mm_for_test` -- per-expert routed counts and
-//    ascending routed-row lists -- as a deterministic stable counting sort in one CTA.
-//  * mat-vec (`dispatch_id_mv`, `kernel_mul_mv_id_q4_0_f32`): one CTA per (routed row,
-//    32 weight rows); fp32 FMA on CUDA cores; the token's x row is held in registers and
-//    reused across the 32 weight rows.
+//    ascending routed-row lists, deterministic: one CTA per expert when the ids fit in shared
+//    memory, else a stable counting sort in one CTA.
+//  * mat-vec (`dispatch_id_mv`, `kernel_mul_mv_id_q4_0_f32`), and its fused SwiGLU form
+//    (`quantized_matmul_id_swiglu_q4_0`): on the tensor cores when K % 128 == 0 (one CTA per
+//    (routed row, 16 weight rows), K split over its warps), else fp32 FMA on CUDA cores (one
+//    CTA per (routed row, 32 weight rows)).
+//  * dispatch records of the mat-vec (plan once, replay with new pointers).
 #include "q4mm_internal.cuh"
 
 #include <new>

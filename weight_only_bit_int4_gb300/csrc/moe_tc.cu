@@ -18,7 +18,7 @@
 // Operands are fp16 (fp32 accumulation): Q4_0's d is already fp16, so (q - 8) * d is formed
 // with one fp16 multiply (a single rounding of the exact product), and x is rounded from fp32
 // to fp16 once in the gather.  Values |x| > 65504 would overflow; the gather flags them in
-// the device error word (Q4MM_DEVERR_F16_RANGE).  The mat-vec form stays in fp32 throughout.
+// the device error word (Q4MM_DEVERR_F16_RANGE).  The mat-vec form rounds x to bf16 instead.
 #include "tc_common.cuh"
 
 #include <cudaTypedefs.h>
