@@ -711,6 +711,15 @@ TilePlan pick_tile_plan(const TcGemmParams &p) {
 }
 
 template <bool LUT, int TT>
+cudaError_t set_tma_smem(int S) {
+  if (S <= 1)
+    return cudaFuncSetAttribute(qgemm_tma_kernel<LUT, TT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_bytes_t<TT>());
+  return cudaFuncSetAttribute(qgemm_tma_kernel<LUT, TT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem_bytes_t<TT>());
+}
+
+template <bool LUT, int TT>
 cudaError_t launch_tma_typed(const TmaMaps &maps, const TcGemmParams &q, int S, cudaStream_t s) {
   if (S <= 1) {
     auto kern = qgemm_tma_kernel<LUT, TT, false>;
@@ -745,9 +754,14 @@ cudaError_t launch_tma_typed(const TmaMaps &maps, const TcGemmParams &q, int S, 
 template <bool LUT>
 cudaError_t launch_tc(const TcGemmParams &p, const void *x, cudaStream_t s) {
   const bool tma_path = p.K % 256 == 0 && (!LUT || p.lut_kb_per_block == 1 || p.lut_kb_per_block == 2);
+  // The kernel's attribute set-up comes first: it makes the device's primary context
+  // current on this host thread, which the tensor-map encoding (a driver call) needs when
+  // this is the thread's first CUDA work.
   if (tma_path) {
     const TilePlan tp = pick_tile_plan(p);
     const int tt = tp.tt;
+    cudaError_t ea = tt == 128 ? set_tma_smem<LUT, 128>(tp.S) : set_tma_smem<LUT, 256>(tp.S);
+    if (ea != cudaSuccess) return ea;
     TmaMaps maps;
     cudaError_t e = make_x_map(&maps.x, x, p.M, p.K, tt);
     if (e == cudaSuccess)
@@ -769,11 +783,11 @@ cudaError_t launch_tc(const TcGemmParams &p, const void *x, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     return tt == 128 ? launch_tma_typed<false, 128>(maps, p, tp.S, s) : launch_tma_typed<false, 256>(maps, p, tp.S, s);
   }
-  CUtensorMap map;
-  cudaError_t e = make_x_map(&map, x, p.M, p.K, kTileT);
-  if (e != cudaSuccess) return e;
   auto kern = qgemm_tc_kernel<LUT>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  CUtensorMap map;
+  e = make_x_map(&map, x, p.M, p.K, kTileT);
   if (e != cudaSuccess) return e;
   kern<<<persistent_grid(p), kThreads, kSmemBytes, s>>>(map, p);
   return cudaGetLastError();
