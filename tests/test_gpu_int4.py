@@ -210,3 +210,30 @@ def test_q4_gemm_matches_bf16_operand_model(M, N, K):
     got = bf16_out(y)
     ulp = np.ldexp(1.0, np.floor(np.log2(np.maximum(np.abs(model), 1e-30))).astype(int) - 7)
     assert np.all(np.abs(got - model) <= ulp + 1e-30)
+
+
+# ---------------------------------------------------------------- smallest legal shapes
+@pytest.mark.parametrize("M,N,K", [(1, 1, 32), (16, 1, 32), (1, 3, 32), (5, 17, 64), (16, 1, 256), (2, 1, 4096)])
+def test_q4_gemv_tiny_shapes(M, N, K):
+    x, w, s, b = _case(90 + M + N, M, N, K)
+    ref = oracle.q4_matmul(x, w, s, b, M, N, K)
+    y = poisoned_bf16(M, N)
+    q.q4_gemv(dev(x), dev(w), dev(s), dev(b), y)
+    assert_within_tolerance(bf16_out(y), ref, f"q4_gemv tiny M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(17, 1, 32), (1, 1, 32), (17, 3, 256), (129, 5, 64), (33, 130, 256)])
+def test_q4_gemm_tiny_shapes(M, N, K):
+    x, w, s, b = _case(95 + M + N, M, N, K)
+    ref = oracle.q4_matmul(x, w, s, b, M, N, K)
+    y = poisoned_bf16(M, N)
+    q.q4_gemm(dev(x), dev(w), dev(s), dev(b), y)
+    assert_within_tolerance(bf16_out(y), ref, f"q4_gemm tiny M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("N,K", [(1, 32), (3, 64), (1, 256)])
+def test_q4_dequant_tiny_shapes(N, K):
+    w, s, b = synth.int4_weights(97 + N, N, K)
+    out = torch.empty(N, K, dtype=torch.float32, device=DEV)
+    q.q4_dequant(dev(w), dev(s), dev(b), out)
+    np.testing.assert_array_equal(out.cpu().numpy().view(np.uint32), oracle.q4_dequant(w, s, b, N, K).view(np.uint32))

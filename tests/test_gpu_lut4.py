@@ -130,3 +130,13 @@ def test_lut4_static_weights_chain_is_bit_identical(M, D):
         over = _lut4_chain(M, D, 5, True, graph=graph)
         for a, b_ in zip(plain, over):
             np.testing.assert_array_equal(a, b_)
+
+
+@pytest.mark.parametrize("M,N,K,block", [(1, 1, 512, 64), (1, 1, 32, 32), (17, 1, 64, 64), (3, 2, 512, 128),
+                                         (1, 1, 2, 2), (20, 1, 128, 64)])
+def test_lut4_tiny_shapes(M, N, K, block):
+    x, packed, scales, book = _case(80 + M + K, M, N, K, block)
+    ref = oracle.lut4_matmul(x, packed, scales, book, M, N, K, block, 1)
+    y = poisoned_bf16(M, N)
+    q.lut4_matmul(dev(x), dev(packed), dev(scales), book, y, N, K, block, 1)
+    assert_within_tolerance(bf16_out(y), ref, f"lut4 tiny M={M} N={N} K={K} block={block}")

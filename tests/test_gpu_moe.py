@@ -189,3 +189,20 @@ def test_swiglu_zero_tokens_is_a_no_op():
     z = torch.empty((0, 64), dtype=torch.float32, device=DEV)
     q.q4_0_matmul_id_swiglu(z, z, out, out, out, 1, 8, 64, 1, 8 * 2 * 18)
     assert torch.all(out == 5.0)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("n_tokens,top_k,E,N,K", [(1, 1, 1, 1, 32), (2, 1, 2, 1, 256), (1, 2, 3, 5, 32), (33, 2, 2, 3, 256)])
+def test_moe_tiny_shapes(mode, n_tokens, top_k, E, N, K):
+    x, w, stride, ids = _moe_case(60 + n_tokens + K, n_tokens, top_k, E, N, K)
+    ref = oracle.q4_0_matmul_id(x, w, ids, n_tokens, top_k, N, K, E, stride)
+    got = _run(x, w, ids, top_k, N, K, E, stride, mode)
+    assert_within_tolerance(got, ref, f"tiny moe mode={mode}")
+
+
+@pytest.mark.parametrize("n_tokens,top_k,E,N,K", [(1, 1, 1, 1, 32), (1, 2, 3, 1, 128), (2, 1, 2, 3, 256)])
+def test_swiglu_tiny_shapes(n_tokens, top_k, E, N, K):
+    gate, up, w, stride, ids = _swiglu_case(70 + K, n_tokens, top_k, E, N, K)
+    ref = oracle.q4_0_matmul_id_swiglu(gate, up, w, ids, N, K, E, stride)
+    got = _run_swiglu(gate, up, w, ids, top_k, N, K, E, stride)
+    assert_within_tolerance(got, ref, "tiny swiglu")
