@@ -140,9 +140,11 @@ def test_q4_gemv_static_weights_first_link_matches_oracle():
 # (512, 4096, 256) and (300, 4096, 256) have few 256-token tiles and run 128-token tiles;
 # (512, 1024, 2048) and (300, 512, 4096) split K over a cluster (S = 4 with 128-token tiles,
 # S = 8 with a ragged token tile) and sum the partial tiles in distributed shared memory.
+# (3072, 1792, 512) and (3000, 1700, 256) run 384-token tiles (a ragged last token tile and
+# ragged weight rows in the second).
 @pytest.mark.parametrize("M,N,K", [(16, 256, 512), (256, 128, 64), (300, 200, 96), (17, 130, 1024),
                                    (600, 384, 2048), (513, 256, 160), (512, 4096, 256), (300, 4096, 256),
-                                   (512, 1024, 2048), (300, 512, 4096)])
+                                   (512, 1024, 2048), (300, 512, 4096), (3072, 1792, 512), (3000, 1700, 256)])
 def test_q4_gemm_parity(M, N, K):
     # config-0 data (no outlier columns) at tile-spanning sizes with ragged M, N and K tails;
     # the outlier-column activations of the prefill configuration are checked at its own

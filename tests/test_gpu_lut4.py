@@ -140,3 +140,26 @@ def test_lut4_tiny_shapes(M, N, K, block):
     y = poisoned_bf16(M, N)
     q.lut4_matmul(dev(x), dev(packed), dev(scales), book, y, N, K, block, 1)
     assert_within_tolerance(bf16_out(y), ref, f"lut4 tiny M={M} N={N} K={K} block={block}")
+
+
+def _bf16_round(a):
+    return synth.bf16_bits_to_f32(synth.to_bf16_bits(np.asarray(a, np.float32))).astype(np.float64)
+
+
+# (3000, 1792, 512) runs 384-token tiles; (600, 640, 1024) 256-token ones.
+@pytest.mark.parametrize("M,N,K", [(3000, 1792, 512), (600, 640, 1024)])
+def test_lut4_gemm_matches_bf16_operand_model(M, N, K):
+    """The tensor-core path multiplies bf16(W) (W = fl32(book * scale), the oracle's exact
+    decode) by bf16 x with fp32 accumulation and rounds y to bf16 once.  With many tokens per
+    weight row, a row whose weights round unluckily shows errors against the fp64 value of
+    about 1 % of rms(y) in a few elements (every token of the row shares those roundings);
+    against the bf16-operand model the only differences left are fp32 summation and the
+    output rounding."""
+    x, packed, scales, book = _case(500 + M, M, N, K, 64)
+    y = poisoned_bf16(M, N)
+    q.lut4_matmul(dev(x), dev(packed), dev(scales), book, y, N, K, 64, 1)
+    w = oracle.lut4_dequant(packed, scales, book, N, K, 64)
+    model = synth.bf16_bits_to_f32(x).astype(np.float64) @ _bf16_round(w).T
+    got = bf16_out(y)
+    rms = float(np.sqrt(np.mean(model * model)))
+    assert np.all(np.abs(got - model) <= np.abs(model) * 2.0 ** -8 + 1e-4 * rms)

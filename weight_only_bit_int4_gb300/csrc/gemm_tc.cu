@@ -321,19 +321,34 @@ constexpr uint32_t kRawBytes = kTileW * 32;          // 4 KB of codes per K bloc
 constexpr uint32_t kScBytes = kTileW * 32;           // 4 KB of scales (or biases) per 8 K blocks
 constexpr int kScKb = 8;                             // K blocks per scale tile
 
-// TT: tokens per tile (MMA N), 256 or 128.  128-token tiles double the tile count for
-// small M, at the price of dequantising each weight tile for half as many tokens.
+// TT: tokens per tile, 384, 256 or 128.  128-token tiles double the tile count for small M,
+// at the price of dequantising each weight tile for half as many tokens.  384-token tiles
+// dequantise each weight tile for 1.5 times as many tokens as 256-token ones, which moves
+// the bound from the dequantising producers to the tensor core for large M: two MMAs per
+// k step (N = 256 at accumulator column 0, N = 128 at column 256), one 384-column
+// accumulator (TMEM holds 512 columns, so no second buffer: the epilogue of a tile is not
+// overlapped with the next tile's MMAs), three stages (the x stage is 48 KB), x loaded as
+// three 128-row boxes per stage.
+template <int TT>
+struct TileCfg {
+  static constexpr int kStages = TT == 384 ? 3 : 4;
+  static constexpr int kAccBufs = TT == 384 ? 1 : 2;             // TMEM accumulator buffers
+  static constexpr uint32_t kTmemCols = TT == 384 ? 512u : 2u * TT;
+  static constexpr int kXBox = TT == 384 ? 128 : TT;            // rows per x TMA box
+};
+
 template <int TT>
 struct SmemLayoutT {
+  static constexpr int kS = TileCfg<TT>::kStages;
   static constexpr uint32_t kB = TT * kBK * 2;                   // x stage bytes
   static constexpr uint32_t a = 0;
-  static constexpr uint32_t b = a + kStages * kABytes;
-  static constexpr uint32_t raw = b + kStages * kB;
-  static constexpr uint32_t sc = raw + kStages * kRawBytes;      // [2] scales
+  static constexpr uint32_t b = a + kS * kABytes;
+  static constexpr uint32_t raw = b + kS * kB;
+  static constexpr uint32_t sc = raw + kS * kRawBytes;           // [2] scales
   static constexpr uint32_t bi = sc + 2 * kScBytes;              // [2] biases
   // full_a, full_b, full_w, empty, acc_full[2], acc_empty[2], sc_full[2], sc_empty[2]
   static constexpr uint32_t bars = bi + 2 * kScBytes;
-  static constexpr uint32_t misc = bars + (4 * kStages + 8) * 8;
+  static constexpr uint32_t misc = bars + (4 * kS + 8) * 8;
   static constexpr uint32_t book = misc + 16;
   static constexpr uint32_t total = book + 16 * 4;
 };
@@ -352,8 +367,12 @@ template <bool LUT, int TT, bool SPLIT>
 __global__ void __launch_bounds__(kThreadsT, 1)
     qgemm_tma_kernel(const __grid_constant__ TmaMaps maps, const __grid_constant__ TcGemmParams p) {
   using L = SmemLayoutT<TT>;
+  using C = TileCfg<TT>;
+  constexpr int kStages = C::kStages;
+  constexpr int kAB = C::kAccBufs;
   constexpr uint32_t kBBytesT = L::kB;
-  constexpr uint32_t kTmemColsT = 2 * TT;
+  constexpr uint32_t kTmemColsT = C::kTmemCols;
+  static_assert(!(SPLIT && TT == 384), "384-token tiles run unsplit");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -451,7 +470,10 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         tc::mbar_arrive_expect_tx(bar_full_w + 8 * s, kRawBytes);
         tc::tma_load_2d(sR + s * kRawBytes, &maps.w, (kb_base + kb) * 32, n0, bar_full_w + 8 * s);
         tc::mbar_arrive_expect_tx(bar_full_b + 8 * s, kBBytesT);
-        tc::tma_load_2d(sB + s * kBBytesT, &maps.x, (kb_base + kb) * kBK, m0, bar_full_b + 8 * s);
+#pragma unroll
+        for (int xb = 0; xb < TT / C::kXBox; ++xb)
+          tc::tma_load_2d(sB + s * kBBytesT + xb * C::kXBox * 128, &maps.x, (kb_base + kb) * kBK, m0 + xb * C::kXBox,
+                          bar_full_b + 8 * s);
         ++issued;
       }
       if (*abort_flag) {
@@ -470,11 +492,13 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(kTileW, TT);
+      constexpr int kN0 = TT > 256 ? 256 : TT;                 // first MMA's N; a second covers the rest
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kTileW, kN0);
+      constexpr uint32_t idesc2 = tc::idesc_bf16_f32(kTileW, TT > 256 ? TT - 256 : 16);
       bool ok = true;
       for (int i = 0; i < my_tiles && ok; ++i) {
-        const int ab = i & 1;
-        ok = tc::mbar_wait(bar_acc_empty + 8 * ab, ((i >> 1) & 1) ^ 1, abort_flag);
+        const int ab = i % kAB;
+        ok = tc::mbar_wait(bar_acc_empty + 8 * ab, ((i / kAB) & 1) ^ 1, abort_flag);
         if (!ok) break;
         tc::tc_fence_after();
         const uint32_t dtm = tmem + (uint32_t)(ab * TT);
@@ -489,8 +513,13 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           const uint64_t ad = tc::smem_desc_sw128(sA + s * kABytes);
           const uint64_t bd = tc::smem_desc_sw128(sB + s * kBBytesT);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
+          for (int k = 0; k < kBK / 16; ++k) {
             tc::mma_bf16(dtm, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+            if constexpr (TT > 256) {   // tokens 256..TT-1: B rows 256.. (32 KB on), accumulator column 256
+              const uint64_t bd2 = tc::smem_desc_sw128(sB + s * kBBytesT + 256 * 128);
+              tc::mma_bf16(dtm + 256u, ad + 2 * k, bd2 + 2 * k, idesc2, (kb | k) != 0);
+            }
+          }
           tc::mma_commit(bar_empty + 8 * s);
         }
         if (ok) tc::mma_commit(bar_acc_full + 8 * ab);
@@ -549,8 +578,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     const int quarter = warp & 3;
     float *part = reinterpret_cast<float *>(smem + L::a);   // split mode: [TT tokens][128 rows]
     for (int i = 0; i < my_tiles; ++i) {
-      const int ab = i & 1;
-      if (!tc::mbar_wait(bar_acc_full + 8 * ab, (i >> 1) & 1, abort_flag)) break;
+      const int ab = i % kAB;
+      if (!tc::mbar_wait(bar_acc_full + 8 * ab, (i / kAB) & 1, abort_flag)) break;
       tc::tc_fence_after();
       const int t = tile_of(i);
       const int m0 = (t % m_tiles) * TT;
@@ -680,7 +709,7 @@ unsigned persistent_grid(const TcGemmParams &p, int tt = kTileT) {
   return (unsigned)(tiles < sms ? tiles : sms);
 }
 
-// Tile plan: tokens per tile (TT) and K split (S).  A tile's time is set by its K blocks,
+// Tile plan: tokens per tile (TT: 384, 256 or 128) and K split (S).  A tile's time is set by its K blocks,
 // the dequantising producers being the bound: a 128-token tile costs about 7/8 of a
 // 256-token one per K block (measured on GB300).  S = 1 runs persistent CTAs over all
 // tiles; S > 1 runs one (tile, K slice) per CTA, S CTAs per cluster, plus the reduction of
@@ -689,17 +718,21 @@ unsigned persistent_grid(const TcGemmParams &p, int tt = kTileT) {
 struct TilePlan {
   int tt, S;
 };
+constexpr double kCost384 = 1.33;
 TilePlan pick_tile_plan(const TcGemmParams &p) {
   const int sms = sm_count();
   const int KB = p.K / kBK;
   TilePlan best{256, 1};
   double best1 = 1e30, bestS = 1e30;
   TilePlan planS{256, 1};
-  for (int tt : {256, 128}) {
-    const double f = tt == 256 ? 1.0 : 0.875;
+  for (int tt : {384, 256, 128}) {
+    // Time per tile relative to a 256-token tile, measured on GB300: 128-token tiles 7/8;
+    // 384-token tiles 1.28-1.36 (1.5x the tokens: the tensor core, not the dequantising
+    // producers, now bounds a K block, and the single accumulator exposes the epilogue).
+    const double f = tt == 256 ? 1.0 : tt == 128 ? 0.875 : kCost384;
     const long long T = (long long)((p.N + kTileW - 1) / kTileW) * ((p.M + tt - 1) / tt);
     for (int S : {1, 2, 4, 8}) {
-      if (S > 1 && KB % (8 * S) != 0) continue;
+      if (S > 1 && (tt == 384 || KB % (8 * S) != 0)) continue;
       const long long ctas = T * S;
       const long long rounds = (ctas + sms - 1) / sms;
       const double cost = (double)rounds * ((double)KB / S * f + (S > 1 ? 10.0 : 0.0));
@@ -712,16 +745,22 @@ TilePlan pick_tile_plan(const TcGemmParams &p) {
 
 template <bool LUT, int TT>
 cudaError_t set_tma_smem(int S) {
-  if (S <= 1)
+  if constexpr (TT == 384) {   // 384-token tiles run unsplit
+    (void)S;
     return cudaFuncSetAttribute(qgemm_tma_kernel<LUT, TT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)smem_bytes_t<TT>());
-  return cudaFuncSetAttribute(qgemm_tma_kernel<LUT, TT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem_bytes_t<TT>());
+  } else {
+    if (S <= 1)
+      return cudaFuncSetAttribute(qgemm_tma_kernel<LUT, TT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)smem_bytes_t<TT>());
+    return cudaFuncSetAttribute(qgemm_tma_kernel<LUT, TT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_bytes_t<TT>());
+  }
 }
 
 template <bool LUT, int TT>
 cudaError_t launch_tma_typed(const TmaMaps &maps, const TcGemmParams &q, int S, cudaStream_t s) {
-  if (S <= 1) {
+  if (TT == 384 || S <= 1) {
     auto kern = qgemm_tma_kernel<LUT, TT, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes_t<TT>());
     if (e != cudaSuccess) return e;
@@ -730,6 +769,9 @@ cudaError_t launch_tma_typed(const TmaMaps &maps, const TcGemmParams &q, int S, 
     kern<<<persistent_grid(q1, TT), kThreadsT, smem_bytes_t<TT>(), s>>>(maps, q1);
     return cudaGetLastError();
   }
+  if constexpr (TT == 384) {
+    return cudaErrorInvalidValue;   // not reached: 384-token tiles run unsplit
+  } else {
   auto kern = qgemm_tma_kernel<LUT, TT, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes_t<TT>());
   if (e != cudaSuccess) return e;
@@ -749,6 +791,7 @@ cudaError_t launch_tma_typed(const TmaMaps &maps, const TcGemmParams &q, int S, 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, maps, qs);
+  }
 }
 
 template <bool LUT>
@@ -760,10 +803,11 @@ cudaError_t launch_tc(const TcGemmParams &p, const void *x, cudaStream_t s) {
   if (tma_path) {
     const TilePlan tp = pick_tile_plan(p);
     const int tt = tp.tt;
-    cudaError_t ea = tt == 128 ? set_tma_smem<LUT, 128>(tp.S) : set_tma_smem<LUT, 256>(tp.S);
+    cudaError_t ea = tt == 128 ? set_tma_smem<LUT, 128>(tp.S)
+                   : tt == 384 ? set_tma_smem<LUT, 384>(tp.S) : set_tma_smem<LUT, 256>(tp.S);
     if (ea != cudaSuccess) return ea;
     TmaMaps maps;
-    cudaError_t e = make_x_map(&maps.x, x, p.M, p.K, tt);
+    cudaError_t e = make_x_map(&maps.x, x, p.M, p.K, tt == 384 ? 128 : tt);
     if (e == cudaSuccess)
       e = make_plain_map(&maps.w, p.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.K / 2, p.N, 32, kTileW);
     if (LUT) {
@@ -774,14 +818,16 @@ cudaError_t launch_tc(const TcGemmParams &p, const void *x, cudaStream_t s) {
                            q.lut_sc_box, kTileW);
       maps.b = maps.s;
       if (e != cudaSuccess) return e;
-      return tt == 128 ? launch_tma_typed<true, 128>(maps, q, tp.S, s) : launch_tma_typed<true, 256>(maps, q, tp.S, s);
+      return tt == 128 ? launch_tma_typed<true, 128>(maps, q, tp.S, s)
+           : tt == 384 ? launch_tma_typed<true, 384>(maps, q, tp.S, s) : launch_tma_typed<true, 256>(maps, q, tp.S, s);
     }
     if (e == cudaSuccess)
       e = make_plain_map(&maps.s, p.scales, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.K / 32, p.N, 16, kTileW);
     if (e == cudaSuccess)
       e = make_plain_map(&maps.b, p.biases, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.K / 32, p.N, 16, kTileW);
     if (e != cudaSuccess) return e;
-    return tt == 128 ? launch_tma_typed<false, 128>(maps, p, tp.S, s) : launch_tma_typed<false, 256>(maps, p, tp.S, s);
+    return tt == 128 ? launch_tma_typed<false, 128>(maps, p, tp.S, s)
+         : tt == 384 ? launch_tma_typed<false, 384>(maps, p, tp.S, s) : launch_tma_typed<false, 256>(maps, p, tp.S, s);
   }
   auto kern = qgemm_tc_kernel<LUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
