@@ -610,6 +610,7 @@ CASES = {
     "gemv_m1": "q4_gemv M=1 K=4096 N=14336",
     "gemv_m16": "q4_gemv M=16 K=14336 N=4096",
     "gemm_m2048": "q4_gemm M=2048 K=4096 N=14336",
+    "gemm_m8192": "q4_gemm M=8192 K=14336 N=4096 (384-token tiles)",
     "lut4_m1": "lut4_matmul M=1 K=N=4096",
     "lut4_m512": "lut4_matmul M=512 K=N=4096",
     "moe_n1": "q4_0_matmul_id n_tokens=1 (mat-vec)",
@@ -634,7 +635,7 @@ def run_case(name: str, launches: int = 3):
 
     if name.startswith("gemv") or name.startswith("gemm"):
         M, K, N = {"gemv_m1": (1, 4096, 14336), "gemv_m16": (16, 14336, 4096),
-                   "gemm_m2048": (2048, 4096, 14336)}[name]
+                   "gemm_m2048": (2048, 4096, 14336), "gemm_m8192": (8192, 14336, 4096)}[name]
         w, s, b = synth.int4_weights(1000, N, K)
         x = to_dev(synth.activations_bf16(1100, M, K, outlier_frac=0.01 if M > 16 else 0.0))
         W = (to_dev(w), to_dev(s), to_dev(b))

@@ -402,6 +402,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   const int KB = p.K / kBK / S;
   const int kb_base = SPLIT ? (int)cluster_ctarank() * KB : 0;
   const int SCB = (KB + kScKb - 1) / kScKb;      // scale tiles per weight tile (or split)
+  // Tile t is (token tile t / n_tiles, weight-row tile t % n_tiles): the CTAs running at one
+  // time share a few x tiles and walk the weight tiles, which all stay in L2, so x (which
+  // can be larger than L2 at large M and K) is read from DRAM about once.
   const int m_tiles = (p.M + TT - 1) / TT;
   const int n_tiles = (p.N + kTileW - 1) / kTileW;
   const int T = m_tiles * n_tiles;
@@ -448,8 +451,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       for (int j = 0; j < steps && ok; ++j) {
         const int i = j / KB, kb = j - i * KB;
         const int t = tile_of(i);
-        const int m0 = (t % m_tiles) * TT;
-        const int n0 = (t / m_tiles) * kTileW;
+        const int m0 = (t / n_tiles) * TT;
+        const int n0 = (t % n_tiles) * kTileW;
         if (kb % kScKb == 0) {
           const int q = i * SCB + kb / kScKb;              // scale tile counter
           const int slot = q & 1;
@@ -582,8 +585,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       if (!tc::mbar_wait(bar_acc_full + 8 * ab, (i / kAB) & 1, abort_flag)) break;
       tc::tc_fence_after();
       const int t = tile_of(i);
-      const int m0 = (t % m_tiles) * TT;
-      const int n = (t / m_tiles) * kTileW + quarter * 32 + lane;
+      const int m0 = (t / n_tiles) * TT;
+      const int n = (t % n_tiles) * kTileW + quarter * 32 + lane;
       for (int c0 = 0; c0 < TT; c0 += 32) {
         if (m0 + c0 >= p.M) break;
         uint32_t v[32];
@@ -617,7 +620,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     cluster_sync_all();
     const uint32_t rank = cluster_ctarank();
     const int t = tile_of(0);
-    const int m0 = (t % m_tiles) * TT, n0 = (t / m_tiles) * kTileW;
+    const int m0 = (t / n_tiles) * TT, n0 = (t % n_tiles) * kTileW;
     const int tok_per = TT / S;
     const uint32_t part_s = smem_u32(smem + L::a);
     for (int it = threadIdx.x; it < tok_per * (kTileW / 4); it += kThreadsT) {
