@@ -128,8 +128,9 @@ __device__ __forceinline__ uint4 decode_chunk(uint32_t word, int c, const RawKb 
 }
 
 // Persistent: one CTA per SM walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...; tile t is
-// (weight-row tile t / m_tiles, token tile t % m_tiles), so neighbouring CTAs share W tiles
-// in L2.  Every role counts pipeline steps j = (tile index within the CTA) * KB + kb.
+// (token tile t / n_tiles, weight-row tile t % n_tiles), so the CTAs running at one time
+// share a few x tiles in L2 while the weight tiles (all of which fit) stay there too.  Every
+// role counts pipeline steps j = (tile index within the CTA) * KB + kb.
 template <bool LUT>
 __global__ void __launch_bounds__(kThreads, 1)
     qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ TcGemmParams p) {
@@ -188,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int j = 0; j < steps; ++j) {
         const int i = j / KB, kb = j - i * KB;
-        const int m0 = (tile_of(i) % m_tiles) * kTileT;
+        const int m0 = (tile_of(i) / n_tiles) * kTileT;
         const int s = j % kStages;
         const uint32_t ph = (j / kStages) & 1;
         if (!tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag)) break;
@@ -235,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 6) {
     // ---------------- dequant producers (one weight row per thread) ----------------
     const int tp = threadIdx.x - 64;          // 0..127
-    auto row_of = [&](int j) { return (tile_of(j / KB) / m_tiles) * kTileW + tp; };
+    auto row_of = [&](int j) { return (tile_of(j / KB) % n_tiles) * kTileW + tp; };
     // Four statically rotated buffers: a block's loads are issued three steps before it is
     // decoded, and no register copy ever waits on a load still in flight.
     RawKb b0, b1, b2, b3;
@@ -278,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!tc::mbar_wait(bar_acc_full + 8 * ab, (i >> 1) & 1, abort_flag)) break;
       tc::tc_fence_after();
       const int t = tile_of(i);
-      const int m0 = (t % m_tiles) * kTileT;
-      const int n = (t / m_tiles) * kTileW + quarter * 32 + lane;
+      const int m0 = (t / n_tiles) * kTileT;
+      const int n = (t % n_tiles) * kTileW + quarter * 32 + lane;
       for (int c0 = 0; c0 < kTileT; c0 += 32) {
         if (m0 + c0 >= p.M) break;
         uint32_t v[32];
