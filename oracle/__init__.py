@@ -31,6 +31,9 @@ PINS = {
     "q4_dequant": "pinned: hand-built words, single-nibble case, quantizer round trip, fp64 exactness",
     "q4_matmul": "pinned: hand-built 2x64x8 closed form, all-zero-nibble closed form, single-nibble case",
     "lut4_dequant / lut4_matmul": "pinned: the lut4.rs CPU test's worked example (both transposes, exact)",
+    "lut4_matmul_rounded": "pinned: identity when every decoded value is already representable, f16 "
+                           "underflow to exact zero and overflow to infinity, one-hot x equals the numpy "
+                           "cast of the decoded matrix",
     "q4_0_matmul_id": "pinned: hand-built block, q=8 zero case, one-hot x, top_k=1 dense reduction, id permutation",
     "q4_0_route": "pinned: hand-written lists and brute-force invariants",
     "q4_0_matmul_id_swiglu": "pinned: sigmoid(+-ln 3) closed form, zero gate/up, odd part = plain routed "
@@ -79,6 +82,9 @@ def _declare(L: ctypes.CDLL) -> None:
         "oracle_lut4_dequant": ([_P, _P, _P, _I, _I, _I, _P], None),
         "oracle_lut4_matmul": ([_P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_int, _P], None),
         "oracle_lut4_matmul_at": ([_P, _P, _P, _P, _I, _I, _I, ctypes.c_int, _P, _P, _I, _P], None),
+        "oracle_lut4_matmul_rounded": ([_P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_int, ctypes.c_int, _P], None),
+        "oracle_lut4_matmul_rounded_at": ([_P, _P, _P, _P, _I, _I, _I, ctypes.c_int, ctypes.c_int, _P, _P, _I,
+                                           _P], None),
         "oracle_q4_0_dequant_row": ([_P, _I, _P], None),
         "oracle_q4_0_matmul_id": ([_P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_uint64, _P], None),
         "oracle_q4_0_matmul_id_rows": ([_P, _P, _P, _I, _I, _I, _I, ctypes.c_uint64, _P, _I, _P], None),
@@ -200,6 +206,30 @@ def lut4_matmul_at(x, packed, scales, book, N: int, K: int, block: int, transpos
     out = np.empty(mi.shape, np.float64)
     lib().oracle_lut4_matmul_at(_p(x), _p(p), _p(s), _p(bk), N, K, block, int(transpose),
                                 _p(mi), _p(ni), mi.size, _p(out))
+    return out
+
+
+_ROUNDING = {None: 0, "f16": 1, "bf16": 2}
+
+
+def lut4_matmul_rounded(x, packed, scales, book, M: int, N: int, K: int, block: int, transpose: int,
+                        rounding) -> np.ndarray:
+    """lut4_matmul with the decoded weight rounded to ``rounding`` ("f16" or "bf16", nearest
+    even) and widened back before the product (lut4.rs, `rounded_weight`)."""
+    x, p, s, bk = _c(x, np.uint16), _c(packed, np.uint8), _c(scales, np.float32), _c(book, np.float32)
+    y = np.empty((M, N), np.float64)
+    lib().oracle_lut4_matmul_rounded(_p(x), _p(p), _p(s), _p(bk), M, N, K, block, int(transpose),
+                                     _ROUNDING[rounding], _p(y))
+    return y
+
+
+def lut4_matmul_rounded_at(x, packed, scales, book, N: int, K: int, block: int, transpose: int, rounding,
+                           mi, ni) -> np.ndarray:
+    x, p, s, bk = _c(x, np.uint16), _c(packed, np.uint8), _c(scales, np.float32), _c(book, np.float32)
+    mi, ni = _c(mi, np.int64), _c(ni, np.int64)
+    out = np.empty(mi.shape, np.float64)
+    lib().oracle_lut4_matmul_rounded_at(_p(x), _p(p), _p(s), _p(bk), N, K, block, int(transpose),
+                                        _ROUNDING[rounding], _p(mi), _p(ni), mi.size, _p(out))
     return out
 
 

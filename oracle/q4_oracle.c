@@ -309,6 +309,55 @@ void oracle_lut4_matmul_at(const uint16_t *x, const uint8_t *packed, const float
     }
 }
 
+/* The rounded-weight variant [P2, `rounded_weight` and the Cast matcher in
+ * `lookup_matmul`]: when the graph casts the decoded weight to half or bfloat16
+ * (and, for the adjoint, back to float), the matmul uses the decoded value rounded
+ * to that type and widened again.  rounding: 0 = none (the plain matmul above),
+ * 1 = IEEE binary16, 2 = bfloat16; both round to nearest, ties to even, through the
+ * conversions at the top of this file. */
+static double lut4_rounded_at(const uint8_t *packed, const float *scales, const float *book,
+                              int64_t f, int64_t block, int rounding)
+{
+    float v = lut4_value_at(packed, scales, book, f, block);
+    if (rounding == 1)
+        v = oracle_f16_to_f32(oracle_f32_to_f16(v));
+    else if (rounding == 2)
+        v = oracle_bf16_to_f32(oracle_f32_to_bf16(v));
+    return (double)v;
+}
+
+/* y[m][n] = sum_k x[m][k] * round(W(k, n)), fp64, k ascending. */
+void oracle_lut4_matmul_rounded(const uint16_t *x, const uint8_t *packed, const float *scales,
+                                const float *book, int64_t M, int64_t N, int64_t K,
+                                int64_t block, int transpose, int rounding, double *y)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += (double)oracle_bf16_to_f32(x[m * K + k]) *
+                       lut4_rounded_at(packed, scales, book, lut4_flat(n, k, N, K, transpose),
+                                       block, rounding);
+            y[m * N + n] = acc;
+        }
+}
+
+/* The same at sampled outputs (mi[i], ni[i]). */
+void oracle_lut4_matmul_rounded_at(const uint16_t *x, const uint8_t *packed, const float *scales,
+                                   const float *book, int64_t N, int64_t K, int64_t block,
+                                   int transpose, int rounding, const int64_t *mi,
+                                   const int64_t *ni, int64_t count, double *out)
+{
+    for (int64_t i = 0; i < count; ++i) {
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k)
+            acc += (double)oracle_bf16_to_f32(x[mi[i] * K + k]) *
+                   lut4_rounded_at(packed, scales, book, lut4_flat(ni[i], k, N, K, transpose),
+                                   block, rounding);
+        out[i] = acc;
+    }
+}
+
 /* ------------------------------------------------------------------------- */
 /* GGML Q4_0 expert-routed matmul  [P3 module doc]                           */
 /*   row r = token*top_k + slot; expert e = ids[r]; token row t = r / top_k; */

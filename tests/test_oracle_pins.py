@@ -224,6 +224,89 @@ def test_lut4_transposes_agree_on_transposed_storage():
     np.testing.assert_array_equal(y0, y1)
 
 
+# The rounded-weight variant (lut4.rs, `rounded_weight`): Cast(decode, half|bf16) and back.
+
+def _pack_codes(c):
+    f = c.reshape(-1)
+    return ((f[0::2] << 4) | f[1::2]).astype(np.uint8)
+
+
+def _bf16_round_bits_trick(v):
+    # nearest-even bf16 by the integer carry method (a different route from the oracle's
+    # scale-and-rint); finite inputs only
+    u = np.asarray(v, np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint32) << 16
+    return r.astype(np.uint32).view(np.float32)
+
+
+@pytest.mark.parametrize("transpose", [0, 1])
+def test_lut4_rounded_one_hot_x_is_the_cast_decoded_matrix(transpose):
+    # x = identity (M = K): y[k][n] is exactly round(W[n][k]); f16 by numpy's cast, bf16 by
+    # the carry method.  A swapped rounding type, a transposed W or a dropped cast fails.
+    N, K, block = 6, 8, 4
+    rng = np.random.default_rng(31)
+    book = synth.lut4_book(9)
+    rows, cols = (N, K) if transpose else (K, N)
+    codes = rng.integers(0, 16, (rows, cols))
+    scales = rng.uniform(0.3, 3.0, rows * cols // block).astype(np.float32)
+    packed = _pack_codes(codes)
+    Wst = oracle.lut4_dequant(packed, scales, book, rows, cols, block)
+    W = Wst if transpose else Wst.T              # [N, K]
+    x = bf16(np.eye(K))
+    y16 = oracle.lut4_matmul_rounded(x, packed, scales, book, K, N, K, block, transpose, "f16")
+    ybf = oracle.lut4_matmul_rounded(x, packed, scales, book, K, N, K, block, transpose, "bf16")
+    np.testing.assert_array_equal(y16, W.T.astype(np.float16).astype(np.float64))
+    np.testing.assert_array_equal(ybf, _bf16_round_bits_trick(W.T).astype(np.float64))
+    assert not np.array_equal(y16, ybf)
+    y0 = oracle.lut4_matmul_rounded(x, packed, scales, book, K, N, K, block, transpose, None)
+    np.testing.assert_array_equal(y0, W.T.astype(np.float64))
+
+
+def test_lut4_rounded_is_identity_on_representable_weights():
+    # book entries j/8 and power-of-two scales: every decoded value has <= 4 significant bits
+    # and lies well inside both ranges, so both casts are exact and y equals the plain matmul.
+    M, N, K, block = 3, 5, 64, 16
+    rng = np.random.default_rng(32)
+    book = (np.arange(16) - 8).astype(np.float32) / 8
+    packed = _pack_codes(rng.integers(0, 16, (N, K)))
+    scales = np.ldexp(1.0, rng.integers(-6, 6, N * K // block)).astype(np.float32)
+    x = synth.activations_bf16(33, M, K)
+    plain = oracle.lut4_matmul(x, packed, scales, book, M, N, K, block, 1)
+    for r in ("f16", "bf16"):
+        np.testing.assert_array_equal(
+            oracle.lut4_matmul_rounded(x, packed, scales, book, M, N, K, block, 1, r), plain)
+
+
+def test_lut4_rounded_f16_underflow_and_overflow():
+    M, N, K, block = 2, 4, 32, 32
+    rng = np.random.default_rng(34)
+    book = np.linspace(0.0625, 1.0, 16).astype(np.float32)
+    packed = _pack_codes(rng.integers(1, 16, (N, K)))
+    x = bf16(rng.uniform(0.5, 1.0, (M, K)))      # positive: no inf - inf
+    # |W| <= 2^-30 < 2^-25 (half the smallest f16 subnormal): the f16 cast gives +0 exactly,
+    # while bf16 keeps fp32's exponent range and the value survives.
+    tiny = np.full(N * K // block, 2.0 ** -30, np.float32)
+    y16 = oracle.lut4_matmul_rounded(x, packed, tiny, book, M, N, K, block, 1, "f16")
+    assert np.all(y16 == 0.0)
+    ybf = oracle.lut4_matmul_rounded(x, packed, tiny, book, M, N, K, block, 1, "bf16")
+    assert np.all(ybf > 0.0)
+    # |W| >= 0.0625 * 2^21 = 131072 > 65520: every f16 weight is +inf.
+    big = np.full(N * K // block, 2.0 ** 21, np.float32)
+    assert np.all(np.isposinf(oracle.lut4_matmul_rounded(x, packed, big, book, M, N, K, block, 1, "f16")))
+    assert np.all(np.isfinite(oracle.lut4_matmul_rounded(x, packed, big, book, M, N, K, block, 1, "bf16")))
+
+
+def test_lut4_rounded_sampled_matches_full():
+    M, N, K, block = 4, 7, 96, 32
+    packed, scales, book = synth.lut4_weights(35, N, K, block)
+    x = synth.activations_bf16(36, M, K)
+    mi = np.array([0, 3, 2, 1, 3]); ni = np.array([6, 0, 3, 5, 2])
+    for r in (None, "f16", "bf16"):
+        full = oracle.lut4_matmul_rounded(x, packed, scales, book, M, N, K, block, 1, r)
+        np.testing.assert_array_equal(
+            oracle.lut4_matmul_rounded_at(x, packed, scales, book, N, K, block, 1, r, mi, ni), full[mi, ni])
+
+
 # ---------------------------------------------------------------------------------------
 # GGML Q4_0 expert-routed (quantized_matmul_id_ggml.rs)
 # ---------------------------------------------------------------------------------------
