@@ -534,7 +534,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     const int tp = threadIdx.x - 64;
     const int row = tp & (kTileW - 1), half = tp / kTileW;
     const uint8_t *raw_row = smem + L::raw + row * 32 + half * 16;
-    const uint8_t *sc_row = smem + L::sc + row * 32;
+    // The scale tile lands as a dense [rows][box] array: 32 bytes a row for INT4 and LUT4
+    // block 64 (eight scales per eight K blocks), 16 for LUT4 block 128 (four).
+    const uint8_t *sc_row = smem + L::sc + row * (LUT ? 4 * p.lut_sc_box : 32);
     const uint8_t *bi_row = smem + L::bi + row * 32;
     // Step j = i * KB + kb walks (tile i, K block kb); scale tile q = i * SCB + kb / kScKb.
     // Counters advance incrementally (no divisions per stage).
