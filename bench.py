@@ -481,6 +481,12 @@ def bench_lut4(args, q, synth, to_dev, ring_of, time_graph, dev, pk):
             tp = time_graph(lambda _: [q.lut4_matmul(x, *ring[l % len(ring)], book, y, N, K, 64, 1)
                                        for l in range(L)], L, replays=10) / L
             row["us_plain_launch"] = round(tp * 1e6, 3)
+        # the rounded-weight variants (Q4MM_LUT4_ROUND_F16 / _BF16), same launches
+        for r in ("f16", "bf16"):
+            tr = time_graph(lambda _: [q.lut4_matmul(x, *ring[l % len(ring)], book, y, N, K, 64, 1,
+                                                     static_weights=True, rounding=r)
+                                       for l in range(L)], L, replays=10) / L
+            row[f"us_round_{r}"] = round(tr * 1e6, 3)
         rows.append(row)
     return {"shapes": rows}
 
@@ -613,6 +619,7 @@ CASES = {
     "gemm_m8192": "q4_gemm M=8192 K=14336 N=4096 (384-token tiles)",
     "lut4_m1": "lut4_matmul M=1 K=N=4096",
     "lut4_m512": "lut4_matmul M=512 K=N=4096",
+    "lut4_f16_m1": "lut4_matmul M=1 K=N=4096, weights rounded to f16 (CUDA-core row kernel)",
     "moe_n1": "q4_0_matmul_id n_tokens=1 (mat-vec)",
     "moe_n512": "q4_0_matmul_id n_tokens=512 (mat-mat)",
     "swiglu_n1": "q4_0_matmul_id_swiglu n_tokens=1, K=1408 -> N=2048 (fused SwiGLU mat-vec)",
@@ -642,13 +649,14 @@ def run_case(name: str, launches: int = 3):
         y = torch.empty((M, N), dtype=torch.int16, device=dev)
         fn = (lambda: q.q4_gemv(x, *W, y)) if name.startswith("gemv") else (lambda: q.q4_gemm(x, *W, y))
     elif name.startswith("lut4"):
-        M = 1 if name == "lut4_m1" else 512
+        M = 512 if name == "lut4_m512" else 1
         N = K = 4096
         packed, scales, book = synth.lut4_weights(3000, N, K, 64)
         x = to_dev(synth.activations_bf16(3100 + M, M, K))
         P, S = to_dev(packed), to_dev(scales)
         y = torch.empty((M, N), dtype=torch.int16, device=dev)
-        fn = lambda: q.lut4_matmul(x, P, S, book, y, N, K, 64, 1)
+        rounding = "f16" if name == "lut4_f16_m1" else None
+        fn = lambda: q.lut4_matmul(x, P, S, book, y, N, K, 64, 1, rounding=rounding)
     elif name == "swiglu_n1":
         E, top_k, N, K = 64, 8, 2048, 1408
         w, stride = synth.q4_0_experts(4300, E, N, K)

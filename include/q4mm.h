@@ -143,8 +143,19 @@ q4mm_status lut4_matmul(const uint16_t *x, const uint8_t *packed, const float *s
  * Q4MM_GEMV_STATIC_WEIGHTS: the promise and effect described at q4_gemv_ex, for packed and
  *   scales (the codebook is copied into the launch).  It changes only calls served by the
  *   decode kernels (M <= 16 on the fast layout); other calls launch as with flags = 0.
- *   Results are bit-identical to flags = 0.
+ *   Results are bit-identical to the same call without this bit.
+ * Q4MM_LUT4_ROUND_F16, Q4MM_LUT4_ROUND_BF16 (at most one): the rounded-weight variant of
+ *   lut4.rs (`rounded_weight`; the graph casts the decoded weight to half or bfloat16, and for
+ *   the adjoint back to float).  Each decoded value W = fl32(book[code] * scale) is rounded to
+ *   IEEE binary16 (F16) or bfloat16 (BF16), nearest even, and the matmul multiplies x by that
+ *   rounded value: y[m][n] = sum_k x[m][k] * round(W[n][k]), fp32 accumulation, bf16 y.  With
+ *   F16, |W| below 2^-25 becomes 0 and |W| of 65520 or more becomes infinity (so y may be
+ *   infinite or NaN).  F16 runs on CUDA cores (fp32 FMA); BF16 uses the tensor-core paths
+ *   where their operand is exactly the rounded value.  Every layout lut4_matmul accepts is
+ *   accepted.  Both bits set: Q4MM_ERR_INVALID_ARG.
  * Unknown flag bits: Q4MM_ERR_INVALID_ARG. */
+#define Q4MM_LUT4_ROUND_F16 0x2u
+#define Q4MM_LUT4_ROUND_BF16 0x4u
 q4mm_status lut4_matmul_ex(const uint16_t *x, const uint8_t *packed, const float *scales,
                            const float *book, uint16_t *y, int64_t M, int64_t N, int64_t K,
                            int64_t block, int transpose, uint32_t flags, q4mm_stream_t stream);

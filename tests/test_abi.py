@@ -68,7 +68,11 @@ def test_lut4_argument_checks(L):
     assert L.lut4_matmul(FAKE, FAKE, FAKE, book, FAKE, 1, 4, 4, 3, 1, None) == 1      # odd block
     assert L.lut4_matmul(FAKE, FAKE, FAKE, None, FAKE, 1, 4, 4, 4, 1, None) == 1      # no book
     assert L.lut4_matmul(FAKE, FAKE, FAKE, book, FAKE, 1, 4, 4, 4, 2, None) == 1      # bad transpose flag
-    assert L.lut4_matmul_ex(FAKE, FAKE, FAKE, book, FAKE, 1, 4, 4, 4, 1, 0x4, None) == 1  # unknown flag bit
+    assert L.lut4_matmul_ex(FAKE, FAKE, FAKE, book, FAKE, 1, 4, 4, 4, 1, 0x8, None) == 1  # unknown flag bit
+    assert L.lut4_matmul_ex(FAKE, FAKE, FAKE, book, FAKE, 1, 4, 4, 4, 1, 0x6, None) == 1  # both roundings
+    assert L.lut4_matmul_ex(None, None, None, None, None, 0, 4, 4, 4, 1, 0x6, None) == 1  # even at M = 0
+    assert L.lut4_matmul_ex(None, None, None, None, None, 0, 4, 4, 4, 1, 0x3, None) == 0  # M = 0, valid flags
+    assert L.lut4_matmul_ex(FAKE, FAKE, FAKE, book, FAKE, 1, 4, 4, 3, 1, 0x2, None) == 1  # odd block
     assert L.lut4_matmul_ex(None, None, None, None, None, 0, 4, 4, 4, 1, 0x1, None) == 0  # M = 0
 
 

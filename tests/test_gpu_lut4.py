@@ -24,10 +24,12 @@ def _case(seed, M, N, K, block=64, transpose=1):
 
 # M <= 4 with K % 512 == 0 and block 32/64/128 runs the K-split decode kernel with the
 # codebook pair table (ragged N, each block size, small and large K); the rest the others.
+# M > 16 with K % 256 == 0 and block 128 runs the TMA GEMM with four scales per scale-tile row.
 @pytest.mark.parametrize("M,N,K,block", [(1, 256, 512, 64), (16, 200, 96, 32), (5, 130, 1024, 128),
                                          (512, 256, 512, 64), (40, 300, 640, 64), (129, 128, 256, 64),
                                          (3, 130, 1024, 128), (2, 200, 2048, 32), (4, 1000, 512, 64),
-                                         (1, 72, 4096, 128), (2, 4104, 1024, 64), (300, 512, 2048, 64)])
+                                         (1, 72, 4096, 128), (2, 4104, 1024, 64), (300, 512, 2048, 64),
+                                         (33, 72, 4096, 128), (300, 520, 1024, 128)])
 def test_lut4_fast_paths(M, N, K, block):
     x, packed, scales, book = _case(60 + M, M, N, K, block)
     ref = oracle.lut4_matmul(x, packed, scales, book, M, N, K, block, 1)
@@ -163,3 +165,73 @@ def test_lut4_gemm_matches_bf16_operand_model(M, N, K):
     got = bf16_out(y)
     rms = float(np.sqrt(np.mean(model * model)))
     assert np.all(np.abs(got - model) <= np.abs(model) * 2.0 ** -8 + 1e-4 * rms)
+
+
+# ---------------------------------------------------------------------------------------
+# The rounded-weight variant (Q4MM_LUT4_ROUND_F16 / _BF16): every route against the oracle's
+# rounded matmul with a tight bound.  The rounded weight enters exactly (f16: fp32 FMA on
+# CUDA cores; bf16: the tensor cores' bf16 operand, or fp32 FMA), so what is left is fp32
+# summation and the bf16 output rounding.
+# ---------------------------------------------------------------------------------------
+
+def _assert_tight(got, ref, what):
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    bad = np.abs(got - ref) > np.abs(ref) * 2.0 ** -8 + 1e-4 * rms
+    assert not np.any(bad), f"{what}: {int(bad.sum())} of {ref.size} outside the bound"
+
+
+# route per rounding: f16 -> row kernel (fast layout) or general kernel; bf16 -> row kernel
+# (M <= 4, K % 512 == 0), decode kernels (M <= 16), tensor-core GEMM (M > 16, K and block
+# % 64 == 0), row kernel (other fast shapes), general kernel (other layouts)
+@pytest.mark.parametrize("rounding", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K,block,transpose", [
+    (1, 256, 512, 64, 1), (2, 200, 2048, 32, 1), (5, 130, 1024, 128, 1), (16, 200, 96, 32, 1),
+    (40, 300, 640, 64, 1), (129, 128, 256, 64, 1), (40, 300, 96, 32, 1), (33, 72, 4096, 128, 1),
+    (3, 5, 7, 4, 0), (17, 40, 50, 2, 1), (1, 1, 32, 32, 1), (20, 1, 128, 64, 1)])
+def test_lut4_rounded_every_route(rounding, M, N, K, block, transpose):
+    x, packed, scales, book = _case(900 + M + N, M, N, K, block, transpose)
+    ref = oracle.lut4_matmul_rounded(x, packed, scales, book, M, N, K, block, transpose, rounding)
+    y = poisoned_bf16(M, N)
+    q.lut4_matmul(dev(x), dev(packed), dev(scales), book, y, N, K, block, transpose, rounding=rounding)
+    got = bf16_out(y)
+    _assert_tight(got, ref, f"lut4 {rounding} M={M} N={N} K={K} block={block} t={transpose}")
+    assert_within_tolerance(got, ref, "lut4 rounded")
+
+
+@pytest.mark.parametrize("M,N,K,block,transpose", [(1, 64, 512, 64, 1), (40, 64, 128, 64, 1),
+                                                   (3, 5, 7, 4, 0), (2, 300, 2048, 32, 1)])
+def test_lut4_rounded_f16_underflow_and_overflow(M, N, K, block, transpose):
+    """|W| <= 2^-30 rounds to binary16 zero: y is exactly 0, while bfloat16 (fp32's exponent
+    range) and the unrounded call keep it.  |W| >= 2^17 rounds to binary16 infinity: with
+    positive x and codebook, y is +inf."""
+    rows, cols = (N, K) if transpose else (K, N)
+    rng = np.random.default_rng(M * 7 + K)
+    packed = rng.integers(0, 256, (rows * cols + 1) // 2, dtype=np.uint8)
+    book = np.linspace(0.0625, 1.0, 16).astype(np.float32)
+    x = synth.to_bf16_bits(rng.uniform(0.5, 1.0, (M, K)).astype(np.float32))
+    n_scales = -(-rows * cols // block)
+    for scale, rounding, check in ((2.0 ** -30, "f16", lambda g: np.all(g == 0.0)),
+                                   (2.0 ** -30, "bf16", lambda g: np.all(g > 0.0)),
+                                   (2.0 ** -30, None, lambda g: np.all(g > 0.0)),
+                                   (2.0 ** 21, "f16", lambda g: np.all(np.isposinf(g))),
+                                   (2.0 ** 21, "bf16", lambda g: np.all(np.isfinite(g)))):
+        scales = np.full(n_scales, scale, np.float32)
+        y = poisoned_bf16(M, N)
+        q.lut4_matmul(dev(x), dev(packed), dev(scales), book, y, N, K, block, transpose, rounding=rounding)
+        assert check(bf16_out(y)), (scale, rounding)
+
+
+@pytest.mark.parametrize("M,rounding", [(1, "f16"), (1, "bf16"), (512, "f16"), (512, "bf16")])
+def test_lut4_rounded_full_size_sampled(M, rounding):
+    N = K = 4096
+    x, packed, scales, book = _case(3100 + M, M, N, K)
+    y = poisoned_bf16(M, N)
+    q.lut4_matmul(dev(x), dev(packed), dev(scales), book, y, N, K, 64, 1, rounding=rounding,
+                  static_weights=True)
+    got = bf16_out(y)
+    assert np.all(np.isfinite(got))
+    rng = np.random.default_rng(M + 11)
+    mi = rng.integers(0, M, 500)
+    ni = rng.integers(0, N, 500)
+    ref = oracle.lut4_matmul_rounded_at(x, packed, scales, book, N, K, 64, 1, rounding, mi, ni)
+    _assert_tight(got[mi, ni], ref, f"lut4 {rounding} full M={M}")

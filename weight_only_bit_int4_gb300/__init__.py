@@ -57,6 +57,7 @@ def q4_dequant(w, scales, biases, out, stream=None) -> None:
 
 
 GEMV_STATIC_WEIGHTS = 0x1
+LUT4_ROUND_F16, LUT4_ROUND_BF16 = 0x2, 0x4
 
 
 def q4_gemv(x, w, scales, biases, y, stream=None, static_weights: bool = False) -> None:
@@ -88,16 +89,21 @@ def _book_ptr(book):
     return arr, ctypes.cast(arr, ctypes.c_void_p)
 
 
+_LUT4_ROUND = {None: 0, "f16": LUT4_ROUND_F16, "bf16": LUT4_ROUND_BF16}
+
+
 def lut4_matmul(x, packed, scales, book, y, N: int, K: int, block: int, transpose: int,
-                stream=None, static_weights: bool = False) -> None:
+                stream=None, static_weights: bool = False, rounding=None) -> None:
     """y[M, N] = x[M, K] . W^T with W[n][k] = fl32(book[code] * scale) (see q4mm.h).
-    static_weights=True: lut4_matmul_ex with Q4MM_GEMV_STATIC_WEIGHTS (see q4_gemv)."""
+    static_weights=True: lut4_matmul_ex with Q4MM_GEMV_STATIC_WEIGHTS (see q4_gemv).
+    rounding="f16" | "bf16": lut4_matmul_ex with Q4MM_LUT4_ROUND_F16 | _BF16 (the decoded
+    weight is rounded to that type before the product)."""
     M = x.shape[0]
     keep, bp = _book_ptr(book)
-    if static_weights:
+    flags = (GEMV_STATIC_WEIGHTS if static_weights else 0) | _LUT4_ROUND[rounding]
+    if flags:
         _check("lut4_matmul_ex", lib().lut4_matmul_ex(_ptr(x), _ptr(packed), _ptr(scales), bp, _ptr(y), M, N,
-                                                      K, block, int(transpose), GEMV_STATIC_WEIGHTS,
-                                                      _stream(stream)))
+                                                      K, block, int(transpose), flags, _stream(stream)))
     else:
         _check("lut4_matmul", lib().lut4_matmul(_ptr(x), _ptr(packed), _ptr(scales), bp, _ptr(y), M, N,
                                                 K, block, int(transpose), _stream(stream)))

@@ -147,7 +147,9 @@ q4mm_status lut4_matmul(const uint16_t *x, const uint8_t *packed, const float *s
 q4mm_status lut4_matmul_ex(const uint16_t *x, const uint8_t *packed, const float *scales,
                            const float *book, uint16_t *y, int64_t M, int64_t N, int64_t K,
                            int64_t block, int transpose, uint32_t flags, q4mm_stream_t stream) {
-  if ((flags & ~Q4MM_GEMV_STATIC_WEIGHTS) != 0u) return Q4MM_ERR_INVALID_ARG;
+  const uint32_t known = Q4MM_GEMV_STATIC_WEIGHTS | Q4MM_LUT4_ROUND_F16 | Q4MM_LUT4_ROUND_BF16;
+  if ((flags & ~known) != 0u) return Q4MM_ERR_INVALID_ARG;
+  if ((flags & Q4MM_LUT4_ROUND_F16) && (flags & Q4MM_LUT4_ROUND_BF16)) return Q4MM_ERR_INVALID_ARG;
   if (M == 0) return Q4MM_OK;
   if (M < 0 || M > kMaxDim || (transpose != 0 && transpose != 1)) return Q4MM_ERR_INVALID_ARG;
   const int64_t rows = transpose ? N : K, cols = transpose ? K : N;
@@ -159,14 +161,33 @@ q4mm_status lut4_matmul_ex(const uint16_t *x, const uint8_t *packed, const float
   cudaStream_t s = (cudaStream_t)stream;
   const bool fast = transpose == 1 && K % 32 == 0 && block % 32 == 0 && K % block == 0 &&
                     aligned(x, 16) && aligned(packed, 16) && aligned(y, 16);
-  if (fast && M <= 16)
+  const bool overlap = (flags & Q4MM_GEMV_STATIC_WEIGHTS) != 0u;
+  // rounding code shared with the CUDA-core kernels: 1 = binary16, 2 = bfloat16
+  const int rounding = (flags & Q4MM_LUT4_ROUND_F16) ? 1 : (flags & Q4MM_LUT4_ROUND_BF16) ? 2 : 0;
+  if (rounding == 1) {
+    // A binary16 weight is not a bfloat16 value, so the tensor-core paths (bf16 operands)
+    // cannot take it exactly: fp32 FMA on CUDA cores.
+    if (fast)
+      return from_cuda(launch_lut4_rowdot(x, packed, scales, book, y, (int)M, (int)N, (int)K, (int)block, 1, s));
+    return from_cuda(launch_lut4_general(x, packed, scales, book, y, M, N, K, block, transpose, 1, s));
+  }
+  if (fast && M <= 16) {
+    // The decode kernels' bf16 operand is bf16(fl32(book * scale)): the bfloat16 rounding
+    // itself, except in the K-split kernel (taken only for M <= 4 and K % 512 == 0), which
+    // multiplies by bf16(book) and applies the scale after the MMA.
+    if (rounding == 2 && M <= 4 && K % 512 == 0)
+      return from_cuda(launch_lut4_rowdot(x, packed, scales, book, y, (int)M, (int)N, (int)K, (int)block, 2, s));
     return from_cuda(launch_lut4_gemv(x, packed, scales, book, y, (int)M, (int)N, (int)K, (int)block, s,
-                                      (flags & Q4MM_GEMV_STATIC_WEIGHTS) != 0u));
+                                      overlap));
+  }
   if (fast && K % 64 == 0 && block % 64 == 0) {
+    // the GEMM's operand is bf16(fl32(book * scale)) in every plan
     cudaError_t e = launch_lut4_gemm(x, packed, scales, book, y, (int)M, (int)N, (int)K, (int)block, s);
     if (e != cudaErrorNotSupported) return from_cuda(e);
   }
-  return from_cuda(launch_lut4_general(x, packed, scales, book, y, M, N, K, block, transpose, s));
+  if (rounding == 2 && fast)
+    return from_cuda(launch_lut4_rowdot(x, packed, scales, book, y, (int)M, (int)N, (int)K, (int)block, 2, s));
+  return from_cuda(launch_lut4_general(x, packed, scales, book, y, M, N, K, block, transpose, rounding, s));
 }
 
 q4mm_status lut4_dequant(const uint8_t *packed, const float *scales, const float *book,

@@ -8,6 +8,12 @@
 // These kernels serve every layout the pages allow (either transpose, any even block,
 // blocks straddling rows).  The fused fast paths for the [N, K/2] layout live in gemv.cu
 // (M <= 16) and gemm_tc.cu (M > 16).
+//
+// Rounded-weight variant (lut4.rs, `rounded_weight` and the Cast matcher of the lookup
+// matmul pattern): when the graph casts the decoded weight to half or bfloat16 and back,
+// the matmul multiplies by that rounded value.  ROUND = 1 rounds fl32(book * scale) to IEEE
+// binary16 and widens it again, ROUND = 2 does the same through bfloat16 (both nearest
+// even); the product with x and the sum stay fp32, so the rounded weight enters exactly.
 #include "q4mm_internal.cuh"
 
 namespace q4mm {
@@ -25,7 +31,24 @@ __device__ __forceinline__ float lut4_value(const uint8_t *__restrict__ packed,
   return book[code] * __ldg(scales + f / block);
 }
 
+template <int ROUND>   // 0 = as decoded, 1 = through binary16, 2 = through bfloat16
+__device__ __forceinline__ float round_weight(float v) {
+  if constexpr (ROUND == 1) {
+    return __half2float(__float2half_rn(v));
+  } else if constexpr (ROUND == 2) {
+    return __bfloat162float(__float2bfloat16_rn(v));
+  } else {
+    return v;
+  }
+}
+
+__device__ __forceinline__ void store_bf16(uint16_t *dst, float v) {
+  __nv_bfloat16 b = __float2bfloat16_rn(v);
+  *dst = *reinterpret_cast<uint16_t *>(&b);
+}
+
 // One output element per thread; fp32 accumulation, k ascending.
+template <int ROUND>
 __global__ void __launch_bounds__(128) lut4_general_kernel(
     const uint16_t *__restrict__ x, const uint8_t *__restrict__ packed,
     const float *__restrict__ scales, const __grid_constant__ Book16 bk, uint16_t *__restrict__ y,
@@ -40,10 +63,85 @@ __global__ void __launch_bounds__(128) lut4_general_kernel(
     float acc = 0.f;
     for (int64_t k = 0; k < K; ++k) {
       const int64_t f = transpose ? n * K + k : k * N + n;
-      acc = __fmaf_rn(bf16_bits_to_float(__ldg(xr + k)), lut4_value(packed, scales, book, f, block), acc);
+      acc = __fmaf_rn(bf16_bits_to_float(__ldg(xr + k)),
+                      round_weight<ROUND>(lut4_value(packed, scales, book, f, block)), acc);
     }
-    __nv_bfloat16 b = __float2bfloat16_rn(acc);
-    y[m * N + n] = *reinterpret_cast<uint16_t *>(&b);
+    store_bf16(y + m * N + n, acc);
+  }
+}
+
+// The [N, K/2] layout (K % 32 == 0, block % 32 == 0, 16-byte aligned x and packed) on CUDA
+// cores: one warp per weight row n, each lane taking 32-code chunks (16 bytes of codes under
+// one scale) with the next chunk's load issued before the current one is used; the x rows
+// m0 .. m0+15 of blockIdx.y's group are read from L1/L2; fp32 FMA, then a warp sum.
+template <int ROUND>
+__global__ void __launch_bounds__(256) lut4_rowdot_kernel(
+    const uint16_t *__restrict__ x, const uint8_t *__restrict__ packed,
+    const float *__restrict__ scales, const __grid_constant__ Book16 bk, uint16_t *__restrict__ y,
+    int M, int N, int K, int block) {
+  __shared__ float book[16];
+  if (threadIdx.x < 16) book[threadIdx.x] = bk.v[threadIdx.x];
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int chunks = K / 32;
+  for (int m0 = blockIdx.y * 16; m0 < M; m0 += gridDim.y * 16) {
+    const int mc = M - m0 < 16 ? M - m0 : 16;
+    for (int n = blockIdx.x * 8 + (threadIdx.x >> 5); n < N; n += gridDim.x * 8) {
+      const uint4 *row = reinterpret_cast<const uint4 *>(packed + (size_t)n * (K / 2));
+      float acc[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+      uint4 q = make_uint4(0u, 0u, 0u, 0u);
+      float s = 0.f;
+      if (lane < chunks) {
+        q = __ldg(row + lane);
+        s = __ldg(scales + ((size_t)n * K + (size_t)lane * 32) / block);
+      }
+      for (int c = lane; c < chunks; c += 32) {
+        const uint4 qc = q;
+        const float sc = s;
+        if (c + 32 < chunks) {
+          q = __ldg(row + c + 32);
+          s = __ldg(scales + ((size_t)n * K + (size_t)(c + 32) * 32) / block);
+        }
+        float w[32];
+        const uint32_t words[4] = {qc.x, qc.y, qc.z, qc.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const uint32_t byte = (words[j] >> (8 * b)) & 255u;
+            w[8 * j + 2 * b] = round_weight<ROUND>(book[byte >> 4] * sc);
+            w[8 * j + 2 * b + 1] = round_weight<ROUND>(book[byte & 15u] * sc);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (i < mc) {
+            const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)(m0 + i) * K + (size_t)c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint4 xv = __ldg(xr + v);
+              const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                acc[i] = __fmaf_rn(__uint_as_float(xw[e] << 16), w[8 * v + 2 * e], acc[i]);
+                acc[i] = __fmaf_rn(__uint_as_float(xw[e] & 0xFFFF0000u), w[8 * v + 2 * e + 1], acc[i]);
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (i < mc) {
+          float v = acc[i];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+          if (lane == 0) store_bf16(y + (size_t)(m0 + i) * N + n, v);
+        }
+      }
+    }
   }
 }
 
@@ -75,11 +173,35 @@ __global__ void __launch_bounds__(256) lut4_dequant_kernel(const uint8_t *__rest
 
 cudaError_t launch_lut4_general(const uint16_t *x, const uint8_t *packed, const float *scales,
                                 const float *book, uint16_t *y, int64_t M, int64_t N,
-                                int64_t K, int64_t block, int transpose, cudaStream_t s) {
+                                int64_t K, int64_t block, int transpose, int rounding,
+                                cudaStream_t s) {
   Book16 bk;
   for (int i = 0; i < 16; ++i) bk.v[i] = book[i];
   dim3 grid((unsigned)((N + 127) / 128), (unsigned)(M < 65535 ? M : 65535), 1);
-  lut4_general_kernel<<<grid, 128, 0, s>>>(x, packed, scales, bk, y, M, N, K, block, transpose);
+  if (rounding == 1)
+    lut4_general_kernel<1><<<grid, 128, 0, s>>>(x, packed, scales, bk, y, M, N, K, block, transpose);
+  else if (rounding == 2)
+    lut4_general_kernel<2><<<grid, 128, 0, s>>>(x, packed, scales, bk, y, M, N, K, block, transpose);
+  else
+    lut4_general_kernel<0><<<grid, 128, 0, s>>>(x, packed, scales, bk, y, M, N, K, block, transpose);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lut4_rowdot(const uint16_t *x, const uint8_t *packed, const float *scales,
+                               const float *book, uint16_t *y, int M, int N, int K, int block,
+                               int rounding, cudaStream_t s) {
+  Book16 bk;
+  for (int i = 0; i < 16; ++i) bk.v[i] = book[i];
+  const int row_blocks = (N + 7) / 8;
+  const int m_groups = (M + 15) / 16;
+  dim3 grid((unsigned)(row_blocks < 152 * 64 ? row_blocks : 152 * 64),
+            (unsigned)(m_groups < 65535 ? m_groups : 65535), 1);
+  if (rounding == 1)
+    lut4_rowdot_kernel<1><<<grid, 256, 0, s>>>(x, packed, scales, bk, y, M, N, K, block);
+  else if (rounding == 2)
+    lut4_rowdot_kernel<2><<<grid, 256, 0, s>>>(x, packed, scales, bk, y, M, N, K, block);
+  else
+    lut4_rowdot_kernel<0><<<grid, 256, 0, s>>>(x, packed, scales, bk, y, M, N, K, block);
   return cudaGetLastError();
 }
 

@@ -220,9 +220,17 @@ cudaError_t launch_lut4_gemv(const uint16_t *x, const uint8_t *packed, const flo
                              const float *book, uint16_t *y, int M, int N, int K, int block,
                              cudaStream_t s, bool overlap = false);
 
+// rounding: 0 = the decoded fp32 weight, 1 = rounded through binary16, 2 = through bfloat16.
 cudaError_t launch_lut4_general(const uint16_t *x, const uint8_t *packed, const float *scales,
                                 const float *book, uint16_t *y, int64_t M, int64_t N,
-                                int64_t K, int64_t block, int transpose, cudaStream_t s);
+                                int64_t K, int64_t block, int transpose, int rounding,
+                                cudaStream_t s);
+
+// The [N, K/2] layout on CUDA cores (K % 32 == 0, block % 32 == 0, 16-byte aligned x and
+// packed); any M >= 1; same rounding codes.
+cudaError_t launch_lut4_rowdot(const uint16_t *x, const uint8_t *packed, const float *scales,
+                               const float *book, uint16_t *y, int M, int N, int K, int block,
+                               int rounding, cudaStream_t s);
 
 cudaError_t launch_lut4_dequant(const uint8_t *packed, const float *scales, const float *book,
                                 int64_t rows, int64_t cols, int64_t block, void *out,
