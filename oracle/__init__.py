@@ -54,9 +54,11 @@ _lib = None
 
 
 def lib() -> ctypes.CDLL:
+    """The compiled oracle.  Q4MM_ORACLE_LIB names another build of q4_oracle.c to load
+    instead (the mutation tests load copies with a planted mistake this way)."""
     global _lib
     if _lib is None:
-        _lib = ctypes.CDLL(build())
+        _lib = ctypes.CDLL(os.environ.get("Q4MM_ORACLE_LIB") or build())
         _declare(_lib)
     return _lib
 

@@ -372,11 +372,12 @@ def test_q4_0_routing_rows_follow_ids():
     ids2 = ids.reshape(T, top_k)[:, ::-1].reshape(-1).copy()
     out2 = oracle.q4_0_matmul_id(x, w, ids2, T, top_k, N, K, n_exp, stride)
     np.testing.assert_array_equal(out2.reshape(T, top_k, N)[:, ::-1], out.reshape(T, top_k, N))
-    # an out-of-range id gives a zero row
-    ids3 = ids.copy(); ids3[3] = 99
-    out3 = oracle.q4_0_matmul_id(x, w, ids3, T, top_k, N, K, n_exp, stride)
-    assert np.all(out3[3] == 0.0)
-    np.testing.assert_array_equal(np.delete(out3, 3, 0), np.delete(out, 3, 0))
+    # an out-of-range id (far out, or exactly n_experts) gives a zero row
+    for bad_id in (99, n_exp):
+        ids3 = ids.copy(); ids3[3] = bad_id
+        out3 = oracle.q4_0_matmul_id(x, w, ids3, T, top_k, N, K, n_exp, stride)
+        assert np.all(out3[3] == 0.0)
+        np.testing.assert_array_equal(np.delete(out3, 3, 0), np.delete(out, 3, 0))
 
 
 # ---------------------------------------------------------------------------------------
@@ -486,6 +487,14 @@ def test_q4_0_route_hand_written():
     assert list(htpe) == [2, 1, 0, 3]
     assert list(hids) == [1, 4, 3, 0, 2, 5]
     assert bad == 1
+
+
+def test_q4_0_route_id_range_boundary():
+    # n_experts - 1 is the last valid id; n_experts itself and 2^32 - 1 are invalid
+    htpe, hids, bad = oracle.q4_0_route(np.array([4, 3, 0xFFFFFFFF, 3, 4], np.uint32), 4)
+    assert list(htpe) == [0, 0, 0, 2]
+    assert list(hids) == [1, 3]
+    assert bad == 3
 
 
 def test_q4_0_route_invariants_brute_force():
