@@ -132,8 +132,8 @@ q4mm_status q4_gemm(const uint16_t *x, const uint32_t *w, const uint16_t *scales
  *   x bf16 [M, K]  ->  y bf16 [M, N], y[m][n] = sum_k x[m][k] * W[n][k].
  * Requirements: M >= 0, N, K >= 1, block > 0 and even; packed holds ceil(rows*cols/2) bytes;
  * x, y 2-byte aligned, scales 4-byte aligned.  The fast kernels serve transpose = 1 with K % 32 == 0,
- * block % 32 == 0, K % block == 0 and 16-byte aligned x/packed; any other valid layout runs
- * on a general (slower) kernel with the same results.
+ * block % 32 == 0, K % block == 0 and 16-byte aligned x/packed/y (for M <= 16 also 16-byte aligned
+ * scales); any other valid layout runs on a general (slower) kernel with the same results.
  * ====================================================================================*/
 q4mm_status lut4_matmul(const uint16_t *x, const uint8_t *packed, const float *scales,
                         const float *book, uint16_t *y, int64_t M, int64_t N, int64_t K,

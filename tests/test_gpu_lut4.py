@@ -144,6 +144,24 @@ def test_lut4_tiny_shapes(M, N, K, block):
     assert_within_tolerance(bf16_out(y), ref, f"lut4 tiny M={M} N={N} K={K} block={block}")
 
 
+# Scales only 4-byte aligned (the header's minimum) and scale rows whose pitch is not a
+# multiple of 16 bytes (block 128 with K % 512 != 0): the decode calls take the general
+# kernel and the GEMM its non-TMA form, and the results are those of the aligned call.
+# Block 128 keeps every cp.async copy of the scales 4 bytes wide.
+@pytest.mark.parametrize("M,N,K,block,offset", [(1, 256, 1024, 128, 4), (5, 130, 1024, 128, 4),
+                                                (40, 200, 1024, 128, 4), (40, 200, 768, 128, 0),
+                                                (300, 130, 1280, 128, 0)])
+def test_lut4_scale_alignment_and_pitch(M, N, K, block, offset):
+    x, packed, scales, book = _case(950 + M + K, M, N, K, block)
+    ref = oracle.lut4_matmul(x, packed, scales, book, M, N, K, block, 1)
+    pad = np.zeros(offset // 4, np.float32)
+    S = dev(np.concatenate([pad, scales]))[offset // 4:]
+    assert S.data_ptr() % 16 == offset
+    y = poisoned_bf16(M, N)
+    q.lut4_matmul(dev(x), dev(packed), S, book, y, N, K, block, 1)
+    assert_within_tolerance(bf16_out(y), ref, f"lut4 scales offset {offset} M={M} K={K}")
+
+
 def _bf16_round(a):
     return synth.bf16_bits_to_f32(synth.to_bf16_bits(np.asarray(a, np.float32))).astype(np.float64)
 

@@ -172,6 +172,10 @@ q4mm_status lut4_matmul_ex(const uint16_t *x, const uint8_t *packed, const float
     return from_cuda(launch_lut4_general(x, packed, scales, book, y, M, N, K, block, transpose, 1, s));
   }
   if (fast && M <= 16) {
+    // The decode kernels stage scales with 8- and 16-byte cp.async copies, which need the
+    // scale array 16-byte aligned; the header promises only 4.
+    if (!aligned(scales, 16))
+      return from_cuda(launch_lut4_general(x, packed, scales, book, y, M, N, K, block, transpose, rounding, s));
     // The decode kernels' bf16 operand is bf16(fl32(book * scale)): the bfloat16 rounding
     // itself, except in the K-split kernel (taken only for M <= 4 and K % 512 == 0), which
     // multiplies by bf16(book) and applies the scale after the MMA.

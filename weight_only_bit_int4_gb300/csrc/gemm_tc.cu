@@ -802,7 +802,12 @@ cudaError_t launch_tma_typed(const TmaMaps &maps, const TcGemmParams &q, int S, 
 
 template <bool LUT>
 cudaError_t launch_tc(const TcGemmParams &p, const void *x, cudaStream_t s) {
-  const bool tma_path = p.K % 256 == 0 && (!LUT || p.lut_kb_per_block == 1 || p.lut_kb_per_block == 2);
+  // LUT4 scales go through a tensor map too: its base must be 16-byte aligned and its row
+  // pitch (K / block scales of 4 bytes) a multiple of 16 bytes; otherwise the producers load
+  // them directly (the non-TMA kernel).
+  const bool lut_tma = p.lut_blocks_per_row % 4 == 0 && (reinterpret_cast<uintptr_t>(p.scales) & 15u) == 0 &&
+                       (p.lut_kb_per_block == 1 || p.lut_kb_per_block == 2);
+  const bool tma_path = p.K % 256 == 0 && (!LUT || lut_tma);
   // The kernel's attribute set-up comes first: it makes the device's primary context
   // current on this host thread, which the tensor-map encoding (a driver call) needs when
   // this is the thread's first CUDA work.
