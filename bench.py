@@ -425,7 +425,7 @@ def bench_prefill(args, q, synth, to_dev, time_graph, dev, pk):
         torch.cuda.empty_cache()
     tot_f = sum(2.0 * r["M"] * r["K"] * r["N"] for r in rows)
     tot_t = sum(r["us"] for r in rows) / 1e6
-    return {"kernel": "qgemm_tc_kernel (q4_gemm, tcgen05)", "shapes": rows,
+    return {"kernel": "qgemm_tma_kernel (q4_gemm: tcgen05, TMA-fed; every bench shape has K % 256 == 0)", "shapes": rows,
             "aggregate_TFLOP_s": round(tot_f / tot_t / 1e12, 1),
             "aggregate_frac_bf16_burst": round(tot_f / tot_t / 1e12 / pk["bf16_tflops"], 3),
             "x": "bf16 N(0,1), 1% columns x20, seeded torch generator on device"}
