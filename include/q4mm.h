@@ -16,7 +16,8 @@
  *  - Errors: arguments are checked on the host before anything is enqueued; a failed check
  *    returns a status and launches nothing.  M == 0 (or n_tokens == 0) returns Q4MM_OK
  *    with nothing enqueued.  After enqueueing, a launch failure reported by the CUDA runtime
- *    is returned as Q4MM_ERR_CUDA.  No call falls back to another path or to the CPU.
+ *    is returned as Q4MM_ERR_CUDA.  Each call picks one of this library's kernels from the
+ *    shape, layout and alignment; none hands work to the CPU or to another library.
  *  - Device-side faults are never raised on purpose: bounded waits that give up, and
  *    routed ids outside [0, n_experts), are recorded in a device error word readable
  *    with q4mm_device_errors().
