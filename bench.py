@@ -586,8 +586,7 @@ def cpu_baseline(seconds: float = 15.0):
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    budget = 120.0
-    n_rows = _oracle_sample_rows(budget / max(1, args.steps + args.warmup))
+    n_rows = _oracle_sample_rows(args.reference_seconds / max(1, args.steps + args.warmup))
     cache = {}
     for _ in range(args.warmup):
         oracle_pass(n_rows, cache)
@@ -697,6 +696,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--reference-seconds", type=float, default=120.0,
+                    help="--impl reference: oracle seconds for the whole warmup + steps run")
     ap.add_argument("--case", choices=sorted(CASES), help="run one small named workload (profiling)")
     args = ap.parse_args()
     if args.case:
