@@ -340,6 +340,10 @@ def run_ours(args, rank, world, local_rank):
         out["lut4"] = bench_lut4(args, q, synth, to_dev, ring_of, time_graph, dev, pk)
         out["moe"] = bench_moe(args, q, synth, to_dev, ring_of, time_graph, dev, pk)
         out["dispatch"] = bench_dispatch(q, synth, to_dev, dev, calls=10 if eager else 3000)
+        try:
+            out["dequant"] = bench_dequant(q, synth, to_dev, ring_of, rings, time_graph, dev, pk)
+        except Exception as e:   # an auxiliary section never costs the headline line
+            out["dequant"] = {"error": f"{type(e).__name__}: {e}"[:300]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
     return out
@@ -489,6 +493,33 @@ def bench_lut4(args, q, synth, to_dev, ring_of, time_graph, dev, pk):
                                            for l in range(L)], L, replays=10) / L
                 row[f"us_round_{r}"] = round(tr * 1e6, 3)
         rows.append(row)
+    return {"shapes": rows}
+
+
+def bench_dequant(q, synth, to_dev, ring_of, rings, time_graph, dev, pk):
+    """Standalone dequants to a dense bf16 matrix: INT4 (N = 14336, K = 4096) and LUT4
+    (K = N = 4096, block 64).  HBM-bound: codes and scales (and biases) are read once and the
+    dense matrix is written.  16 calls per graph walk the weight replicas; the outputs rotate
+    through buffers whose total exceeds L2, so the writes reach DRAM."""
+    import torch
+    rows = []
+    K, N = 4096, 14336
+    r = rings[(K, N)]
+    outs = [torch.empty((N, K), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    L = 16
+    t = time_graph(lambda _: [q.q4_dequant(*r[l % len(r)], outs[l % 2]) for l in range(L)], L, replays=5) / L
+    by = N * K * 9 // 16 + N * K * 2
+    rows.append({"op": "q4_dequant", "N": N, "K": K, "out": "bf16", "us": round(t * 1e6, 3),
+                 "GB_s": round(by / t / 1e9, 1), "frac_hbm": round(by / t / 1e9 / pk["hbm_gbs"], 3)})
+    Kl = Nl = 4096
+    packed, scales, book = synth.lut4_weights(3000, Nl, Kl, 64)
+    lr = ring_of((to_dev(packed), to_dev(scales)), packed.nbytes + scales.nbytes)
+    louts = [torch.empty((Nl, Kl), dtype=torch.bfloat16, device=dev) for _ in range(6)]
+    t = time_graph(lambda _: [q.lut4_dequant(*lr[l % len(lr)], book, Nl, Kl, 64, louts[l % 6]) for l in range(L)],
+                   L, replays=5) / L
+    by = packed.nbytes + scales.nbytes + 64 + Nl * Kl * 2
+    rows.append({"op": "lut4_dequant", "N": Nl, "K": Kl, "block": 64, "out": "bf16", "us": round(t * 1e6, 3),
+                 "GB_s": round(by / t / 1e9, 1), "frac_hbm": round(by / t / 1e9 / pk["hbm_gbs"], 3)})
     return {"shapes": rows}
 
 
