@@ -77,6 +77,14 @@ MUTATIONS = {
     "swiglu gate and up swapped": (
         "double h = silu((double)gate[r * K + k]) * (double)up[r * K + k];",
         "double h = silu((double)up[r * K + k]) * (double)gate[r * K + k];"),
+    "lut4 sampled form swaps m and n": (
+        "x[mi[i] * K + k]) *\n                   (double)lut4_value_at(packed, scales, book,\n"
+        "                                         lut4_flat(ni[i], k, N, K, transpose), block);",
+        "x[ni[i] * K + k]) *\n                   (double)lut4_value_at(packed, scales, book,\n"
+        "                                         lut4_flat(mi[i], k, N, K, transpose), block);"),
+    "q4_0 routed-row form reads the routed row as the token": (
+        "q4_0_one_row(x, w, ids[rows[i]], rows[i] / top_k, N, K, n_experts, expert_stride,",
+        "q4_0_one_row(x, w, ids[rows[i]], rows[i], N, K, n_experts, expert_stride,"),
     "route lists descending": (
         "for (int64_t r = 0; r < n_rows; ++r)\n            if ((int64_t)ids[r] == e) {",
         "for (int64_t r = n_rows - 1; r >= 0; --r)\n            if ((int64_t)ids[r] == e) {"),

@@ -224,6 +224,24 @@ def test_lut4_transposes_agree_on_transposed_storage():
     np.testing.assert_array_equal(y0, y1)
 
 
+
+@pytest.mark.parametrize("transpose", [0, 1])
+def test_lut4_matmul_at_matches_full(transpose):
+    # The sampled form used by the full-size checks equals the pinned full matmul at every
+    # chosen (m, n), for both storage orders, with a block (32) that does not divide K (48),
+    # so scale blocks straddle rows of the stored matrix.  M < N and the pairs include
+    # m != n, so an (m, n) mix-up in the sampled index shows.
+    M, N, K, block = 4, 5, 48, 32
+    rng = np.random.default_rng(77)
+    packed = rng.integers(0, 256, N * K // 2, dtype=np.uint8)
+    scales = rng.uniform(0.5, 1.5, -(-N * K // block)).astype(np.float32)
+    book = synth.lut4_book(78)
+    x = synth.activations_bf16(79, M, K)
+    full = oracle.lut4_matmul(x, packed, scales, book, M, N, K, block, transpose)
+    mi = np.array([0, 3, 2, 1, 3, 0]); ni = np.array([4, 0, 3, 2, 1, 0])
+    np.testing.assert_array_equal(
+        oracle.lut4_matmul_at(x, packed, scales, book, N, K, block, transpose, mi, ni), full[mi, ni])
+
 # The rounded-weight variant (lut4.rs, `rounded_weight`): Cast(decode, half|bf16) and back.
 
 def _pack_codes(c):
@@ -379,6 +397,22 @@ def test_q4_0_routing_rows_follow_ids():
         assert np.all(out3[3] == 0.0)
         np.testing.assert_array_equal(np.delete(out3, 3, 0), np.delete(out, 3, 0))
 
+
+
+def test_q4_0_matmul_id_rows_matches_full():
+    # The routed-row form used by the full-size checks equals the matching rows of the
+    # pinned full routed matmul.  top_k = 3 and rows that are not multiples of top_k check
+    # the token row r / top_k.  x holds n_tokens * top_k rows, of which the full call reads
+    # only the first n_tokens: a row read at the wrong token stays inside the buffer and
+    # gives a different value.
+    n_exp, N, K, T, top_k = 6, 5, 96, 4, 3
+    w, stride = synth.q4_0_experts(91, n_exp, N, K)
+    x = synth.activations_f32(92, T * top_k, K)
+    ids = synth.routing_ids(93, T, top_k, n_exp)
+    full = oracle.q4_0_matmul_id(x, w, ids, T, top_k, N, K, n_exp, stride)
+    rows = np.array([0, 5, 7, 11, 3, 10, 1])
+    np.testing.assert_array_equal(
+        oracle.q4_0_matmul_id_rows(x, w, ids, top_k, N, K, n_exp, stride, rows), full[rows])
 
 # ---------------------------------------------------------------------------------------
 # Fused SwiGLU + routed Q4_0 mat-vec (quantized_matmul_id_ggml.rs,
