@@ -508,7 +508,7 @@ def bench_dequant(q, synth, to_dev, ring_of, rings, time_graph, dev, pk):
     outs = [torch.empty((N, K), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     L = 16
     t = time_graph(lambda _: [q.q4_dequant(*r[l % len(r)], outs[l % 2]) for l in range(L)], L, replays=5) / L
-    by = N * K * 9 // 16 + N * K * 2
+    by = N * K // 2 + N * (K // 32) * 4 + N * K * 2   # codes, bf16 scales + biases, bf16 out
     rows.append({"op": "q4_dequant", "N": N, "K": K, "out": "bf16", "us": round(t * 1e6, 3),
                  "GB_s": round(by / t / 1e9, 1), "frac_hbm": round(by / t / 1e9 / pk["hbm_gbs"], 3)})
     Kl = Nl = 4096

@@ -286,6 +286,8 @@ void q4mm_record_free(q4mm_record *rec);
  *     q4_0_matmul_id_workspace_size(n_tokens, top_k, N, K, n_experts) exceeds the array.
  *   - The first call on a device (made with that device current) looks up the array's device
  *     address; make that first call before any stream capture that includes this call.
+ *     Later calls on a stream that is not capturing look it up again, so after a device reset
+ *     (cudaDeviceReset) the next such call picks up the new address; make one before capturing.
  *   - All calls on a device share the array.  Calls that overlap on the GPU race on it and
  *     give wrong results: order them (for instance on one stream).
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.

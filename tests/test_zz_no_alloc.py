@@ -27,8 +27,11 @@ def _call_noalloc(x, w, ids, out, top_k, N, K, E, stride):
                                     top_k, N, K, E, stride, torch.cuda.current_stream().cuda_stream)
 
 
-def test_noalloc_matches_workspace_entry_point_on_two_calls():
-    E, top_k, N, K = 16, 8, 256, 512
+@pytest.mark.parametrize("K", [512, 288])
+def test_noalloc_matches_workspace_entry_point_on_two_calls(K):
+    # K = 512 runs the tensor-core mat-mat kernel; K = 288 (K % 256 != 0) the CUDA-core kernel
+    # over the routed order.  Both read their routing lists from the fixed array.
+    E, top_k, N = 16, 8, 256
     for n_tokens, seed in ((64, 501), (40, 502)):
         w, stride = synth.q4_0_experts(seed, E, N, K)
         ids = synth.routing_ids(seed + 1, n_tokens, top_k, E)
@@ -43,6 +46,8 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         ref_h = ref.cpu().numpy().astype(np.float64)
         got = out.cpu().numpy().astype(np.float64)
         assert np.all(np.isfinite(got))
+        # the same kernels on the same inputs: bit for bit, so stale scratch would show
+        np.testing.assert_array_equal(got, ref_h, err_msg=f"noalloc vs workspace entry, n_tokens={n_tokens}")
         assert_within_tolerance(got, ref_h, f"noalloc vs workspace entry, n_tokens={n_tokens}")
         # and both against the oracle on a few rows
         rows = np.arange(0, n_tokens * top_k, 37)

@@ -224,7 +224,9 @@ q4mm_status q4_0_route(const uint32_t *ids, int64_t n_rows, int64_t n_experts, u
 
 size_t q4_0_matmul_id_workspace_size(int64_t n_tokens, int64_t top_k, int64_t N, int64_t K,
                                      int64_t n_experts) {
-  if (n_tokens < 1 || top_k < 1 || N < 1 || K < 32 || n_experts < 1) return 0;
+  if (n_tokens < 1 || !routed_rows_ok(n_tokens, top_k) || N < 1 || K < 32 || N > kMaxDim || K > kMaxDim ||
+      n_experts < 1 || n_experts > 1024)
+    return 0;
   return q4_0_mm_workspace_bytes(n_tokens, top_k, N, K, n_experts);
 }
 
@@ -237,7 +239,7 @@ q4mm_status q4_0_matmul_id(const float *x, const void *w, const uint32_t *ids, f
   if (n_tokens < 0 || top_k < 1 || N < 1 || K < 32 || K % 32 != 0 || n_experts < 1 ||
       n_experts > 1024 || N > kMaxDim || K > kMaxDim)
     return Q4MM_ERR_INVALID_ARG;
-  if (n_tokens * top_k > (int64_t(1) << 24)) return Q4MM_ERR_INVALID_ARG;
+  if (!routed_rows_ok(n_tokens, top_k)) return Q4MM_ERR_INVALID_ARG;
   const uint64_t per_expert = (uint64_t)N * (uint64_t)(K / 32) * 18u;
   if (expert_stride < per_expert) return Q4MM_ERR_INVALID_ARG;
   if (mode < 0 || mode > 2) return Q4MM_ERR_INVALID_ARG;
@@ -268,7 +270,7 @@ q4mm_status q4_0_matmul_id_swiglu(const float *gate, const float *up, const void
   if (n_tokens < 0 || top_k < 1 || N < 1 || K < 32 || K % 32 != 0 || n_experts < 1 ||
       n_experts > 1024 || N > kMaxDim || K > kMaxDim)
     return Q4MM_ERR_INVALID_ARG;
-  if (n_tokens * top_k > (int64_t(1) << 24)) return Q4MM_ERR_INVALID_ARG;
+  if (!routed_rows_ok(n_tokens, top_k)) return Q4MM_ERR_INVALID_ARG;
   const uint64_t per_expert = (uint64_t)N * (uint64_t)(K / 32) * 18u;
   if (expert_stride < per_expert) return Q4MM_ERR_INVALID_ARG;
   if (!aligned(gate, 16) || !aligned(up, 16) || !aligned(out, 16) || !aligned(ids, 4))
@@ -340,7 +342,7 @@ q4mm_status q4_0_matmul_id_mv_record(int64_t n_tokens, int64_t top_k, int64_t N,
   *out = nullptr;
   if (swiglu != 0 && swiglu != 1) return Q4MM_ERR_INVALID_ARG;
   if (n_tokens < 1 || top_k < 1 || N < 1 || K < 32 || K % 32 != 0 || n_experts < 1 || n_experts > 1024 ||
-      N > kMaxDim || K > kMaxDim || n_tokens * top_k > (int64_t(1) << 24))
+      N > kMaxDim || K > kMaxDim || !routed_rows_ok(n_tokens, top_k))
     return Q4MM_ERR_INVALID_ARG;
   if (expert_stride < (uint64_t)N * (uint64_t)(K / 32) * 18u) return Q4MM_ERR_INVALID_ARG;
   q4mm_status st = check_device();

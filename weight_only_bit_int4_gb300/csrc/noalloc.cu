@@ -13,7 +13,10 @@
 // Q4MM_NOALLOC_SCRATCH_BYTES of it until the process exits.  Host code cannot use the
 // array's name as a device address; on the first call on a device (with that device
 // current) the address is fetched with cudaGetSymbolAddress and kept per device.  That first
-// call should therefore happen before any stream capture that includes this call.
+// call should therefore happen before any stream capture that includes this call.  Every
+// later call whose stream is not capturing fetches the address again, so a device reset
+// (which reloads the library's module in a new context) leaves no stale address behind;
+// calls made while their stream is capturing use the kept one.
 //
 // All calls on a device share the one array, which keeps whatever the previous call left.
 // Nothing in it has to start at zero: each call's routing pass rewrites every routing field
@@ -29,7 +32,7 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[Q4MM_NOALLOC_SCRATCH_BYTES];
 
 std::mutex g_scratch_mutex;
-void *g_scratch_ptr[64] = {};   // device address of g_noalloc_scratch, per device ordinal
+void *g_scratch_ptr[64] = {};   // last fetched device address of g_noalloc_scratch, per device ordinal
 
 bool is_aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -43,7 +46,7 @@ extern "C" q4mm_status q4_0_matmul_id_noalloc(const float *x, const void *w, con
   if (!x || !w || !ids || !out) return Q4MM_ERR_INVALID_ARG;
   const int64_t kMax = int64_t(1) << 30;
   if (n_tokens < 0 || top_k < 1 || N < 1 || K < 32 || K % 32 != 0 || n_experts < 1 || n_experts > 1024 ||
-      N > kMax || K > kMax || n_tokens * top_k > (int64_t(1) << 24))
+      N > kMax || K > kMax || !q4mm::routed_rows_ok(n_tokens, top_k))
     return Q4MM_ERR_INVALID_ARG;
   if (expert_stride < (uint64_t)N * (uint64_t)(K / 32) * 18u) return Q4MM_ERR_INVALID_ARG;
   if (!is_aligned(x, 16) || !is_aligned(out, 16) || !is_aligned(ids, 4)) return Q4MM_ERR_UNSUPPORTED;
@@ -60,10 +63,12 @@ extern "C" q4mm_status q4_0_matmul_id_noalloc(const float *x, const void *w, con
     return Q4MM_ERR_CUDA;
   if (major != 10 || minor != 3) return Q4MM_ERR_DEVICE;
 
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing((cudaStream_t)stream, &capture) != cudaSuccess) return Q4MM_ERR_CUDA;
   void *scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
+    if (g_scratch_ptr[dev] == nullptr || capture == cudaStreamCaptureStatusNone) {
       void *p = nullptr;
       if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return Q4MM_ERR_CUDA;
       g_scratch_ptr[dev] = p;

@@ -259,6 +259,13 @@ cudaError_t launch_q4_0_mm(const float *x, const uint8_t *w, const uint32_t *ids
                            int n_tokens, int top_k, int N, int K, int n_experts,
                            uint64_t expert_stride, void *workspace, cudaStream_t s);
 
+// Routed-row count check: n_tokens and top_k are each bounded before their product is
+// formed, so a huge top_k cannot overflow int64 and wrap past the 2^24 limit.
+inline bool routed_rows_ok(int64_t n_tokens, int64_t top_k) {
+  const int64_t kMaxRows = int64_t(1) << 24;
+  return n_tokens >= 0 && top_k >= 1 && n_tokens <= kMaxRows && top_k <= kMaxRows &&
+         n_tokens * top_k <= kMaxRows;
+}
 size_t q4_0_mm_workspace_bytes(int64_t n_tokens, int64_t top_k, int64_t N, int64_t K,
                                int64_t n_experts);
 
