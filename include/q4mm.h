@@ -59,8 +59,9 @@ typedef enum q4mm_dtype { Q4MM_F32 = 0, Q4MM_BF16 = 1, Q4MM_F16 = 2 } q4mm_dtype
 /* Bits of the device error word. */
 #define Q4MM_DEVERR_WAIT_TIMEOUT 0x1u  /* a pipeline wait gave up; that output is invalid */
 #define Q4MM_DEVERR_BAD_EXPERT 0x2u    /* an id >= n_experts was routed (its row is zero) */
-#define Q4MM_DEVERR_F16_RANGE 0x4u     /* mat-mat Q4_0: some |x| > 65504, outside the fp16
-                                          operand range (that output is not valid) */
+#define Q4MM_DEVERR_F16_RANGE 0x4u     /* reserved, never raised: the Q4_0 mat-mat form scales
+                                          each gathered x row by a power of two and serves
+                                          every finite f32 x */
 
 /* Static string for a status code (never NULL). */
 const char *q4mm_status_string(int status);

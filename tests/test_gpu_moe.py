@@ -93,6 +93,30 @@ def test_moe_invalid_id_gives_zero_row(mode, n_tokens, top_k, E, bad_rows):
     assert q.device_errors() & 0x2
 
 
+
+# Rows of x far outside the fp16 range and far below its normal range: the mat-mat form scales
+# each gathered row by a power of two, so every finite f32 row is served.  Each routed row is
+# held to the tolerance with rms over that row alone, so a small row is not excused by the
+# large ones.  K = 512 runs the tensor-core kernel (fp16 operands); K = 288 the CUDA-core one.
+@pytest.mark.parametrize("K", [512, 288])
+@pytest.mark.parametrize("mode", [0, 2])
+def test_moe_mm_any_f32_row_range(mode, K):
+    n_tokens, top_k, E, N = 48, 4, 8, 192
+    x, w, stride, ids = _moe_case(4200 + K, n_tokens, top_k, E, N, K)
+    x = x.copy()
+    gains = np.array([1e6, 1e-6, 1.0, 3e4, 2e-5, 7e7, 1e-30, 5e30], np.float32)
+    x *= gains[np.arange(n_tokens) % gains.size][:, None]
+    x[5, 17] = 1e9                      # one element far above the rest of its row
+    x[9, :] *= np.float32(1e-8)         # a row that sits in f32's low range
+    assert np.all(np.isfinite(x))
+    q.device_errors()
+    got = _run(x, w, ids, top_k, N, K, E, stride, mode)
+    ref = oracle.q4_0_matmul_id(x, w, ids, n_tokens, top_k, N, K, E, stride)
+    assert np.all(np.isfinite(got))
+    for r in range(n_tokens * top_k):
+        assert_within_tolerance(got[r], ref[r], f"routed row {r} (token {r // top_k}), mode={mode}, K={K}")
+    assert q.device_errors() == 0
+
 @pytest.mark.parametrize("n_tokens", [1, 512])
 @pytest.mark.parametrize("mode", [0, 1, 2])
 def test_moe_full_size_sampled(n_tokens, mode):

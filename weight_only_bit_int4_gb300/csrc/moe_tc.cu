@@ -6,19 +6,22 @@
 //
 //  1. routing (moe.cu): per-expert counts, ascending row lists, and a list of token blocks
 //     of <= 128 rows, each inside one expert;
-//  2. gather: xs[p] = fp16(x[hids[p] / top_k]) -- the rows of x in routed order;
+//  2. gather: xs[p] = fp16(2^e_p * x[hids[p] / top_k]) -- the rows of x in routed order, each
+//     scaled by a power of two that brings its largest magnitude into [2^14, 2^15);
 //  3. this kernel, persistent over work items (token block, 128-row weight tile):
 //       A = the expert's Q4_0 weight rows, decoded to fp16 by four producer warps from
 //           144-byte TMA boxes (8 blocks of 18 bytes = 256 k per box);
 //       B = the block's gathered x rows (TMA, 64-row boxes, 128-byte swizzle);
 //       D = 128 weight rows x (rows rounded up to 16) fp32 in tensor memory;
-//     epilogue warps scatter D column j to out[hids[p0 + j]][n0 .. n0+127] (fp32).
+//     epilogue warps scatter 2^-e_p * D column j to out[hids[p0 + j]][n0 .. n0+127] (fp32).
 //     Each expert's weights stream once from HBM per token block.
 //
 // Operands are fp16 (fp32 accumulation): Q4_0's d is already fp16, so (q - 8) * d is formed
 // with one fp16 multiply (a single rounding of the exact product), and x is rounded from fp32
-// to fp16 once in the gather.  Values |x| > 65504 would overflow; the gather flags them in
-// the device error word (Q4MM_DEVERR_F16_RANGE).  The mat-vec form rounds x to bf16 instead.
+// to fp16 once in the gather.  The power-of-two row scaling is exact in both directions, so
+// any finite f32 row is served: its largest element lands near 2^14 (no fp16 overflow, and no
+// fp16 subnormals unless an element is 2^-28 below the row's largest), and the rounding to
+// fp16 is relative to the row's own range.  The mat-vec form rounds x to bf16 instead.
 #include "tc_common.cuh"
 
 #include <cudaTypedefs.h>
@@ -56,6 +59,7 @@ constexpr size_t kSmem = SmemL::total + 1024;
 struct MmParams {
   float *out;
   const int32_t *hids;
+  const float *xun;   // per gathered row: the power of two that undoes the gather's scaling
   const int4 *blk;
   const uint32_t *n_blk;
   int N, K;
@@ -312,10 +316,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * kMoeTokBlock + c0), v);
         tc::tmem_ld_wait();
         const int r_lane = c0 + lane < bi.z ? p.hids[bi.y + c0 + lane] : 0;
+        const float un_lane = c0 + lane < bi.z ? p.xun[bi.y + c0 + lane] : 1.f;
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
           const int r = __shfl_sync(0xFFFFFFFFu, r_lane, jj);
-          if (c0 + jj < bi.z && n < p.N) p.out[(size_t)r * p.N + n] = __uint_as_float(v[jj]);
+          const float un = __shfl_sync(0xFFFFFFFFu, un_lane, jj);
+          if (c0 + jj < bi.z && n < p.N) p.out[(size_t)r * p.N + n] = __uint_as_float(v[jj]) * un;
         }
       }
       tc::tc_fence_before();
@@ -332,20 +338,60 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// xs[p] = fp16(x[hids[p] / top_k]) for p < number of valid routed rows, each 32-element
-// block laid out in the chunk order of q4_0_chunk.  Item = (row, block, chunk m): two float4
-// loads (elements 4m.. and 16+4m..) and one 16-byte store.  A CTA takes four rows at a time,
-// so each thread has four items' loads in flight.
+// xs[p] = fp16(2^e_p * x[hids[p] / top_k]) for p < number of valid routed rows, each 32-element
+// block laid out in the chunk order of q4_0_chunk, and xun[p] = 2^-e_p.  e_p is chosen so
+// that the row's largest magnitude m lands in [2^14, 2^15) (e_p = 15 - frexp exponent of m,
+// clamped to [-126, 127] so that both powers of two are f32 values; m == 0 or a non-finite m
+// keeps e_p = 0).  Multiplying by a power of two is exact, so the only rounding is the one to
+// fp16, relative to the row's own range.  A CTA takes four rows at a time: one pass finds the
+// four maxima (item = (row, block, chunk m): two float4 loads, elements 4m.. and 16+4m..), a
+// second pass reloads the rows (L1-resident) and stores one 16-byte chunk per item.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const float *__restrict__ x, const int32_t *__restrict__ hids,
                                                           const uint32_t *__restrict__ n_valid, int top_k, int K,
-                                                          uint16_t *__restrict__ xs, int n_rows) {
+                                                          uint16_t *__restrict__ xs, float *__restrict__ xun,
+                                                          int n_rows) {
+  __shared__ float red[8][4];
+  __shared__ float fac[4];
   const int nv = min((int)*n_valid, n_rows);
   const int per_row = K / 8;   // items per row: K / 32 blocks x 4 chunks
-  bool out_of_range = false;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   for (int pos0 = blockIdx.x * 4; pos0 < nv; pos0 += gridDim.x * 4) {
     const float *src[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) src[u] = pos0 + u < nv ? x + (size_t)(hids[pos0 + u] / top_k) * K : nullptr;
+    float mx[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int i = threadIdx.x; i < per_row; i += blockDim.x) {
+      const int off = (i >> 2) * 32 + 4 * (i & 3);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (src[u] != nullptr) {
+          const float4 a = __ldg(reinterpret_cast<const float4 *>(src[u] + off));
+          const float4 b = __ldg(reinterpret_cast<const float4 *>(src[u] + off + 16));
+          mx[u] = fmaxf(mx[u], fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                                     fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w)))));
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx[u] = fmaxf(mx[u], __shfl_xor_sync(0xFFFFFFFFu, mx[u], o));
+      if (lane == 0) red[warp][u] = mx[u];
+    }
+    __syncthreads();
+    if (threadIdx.x < 4) {
+      const int u = threadIdx.x;
+      float m = 0.f;
+      for (int wv = 0; wv < (int)(blockDim.x / 32); ++wv) m = fmaxf(m, red[wv][u]);
+      int e = 0;
+      if (m > 0.f && m <= 3.402823466e38f) {
+        int ex = 0;
+        frexpf(m, &ex);          // m in [2^(ex-1), 2^ex)
+        e = min(max(15 - ex, -126), 127);
+      }
+      fac[u] = ldexpf(1.f, e);
+      if (pos0 + u < nv) xun[pos0 + u] = ldexpf(1.f, -e);
+    }
+    __syncthreads();
     for (int i = threadIdx.x; i < per_row; i += blockDim.x) {
       const int off = (i >> 2) * 32 + 4 * (i & 3);
       float4 lo[4], hi[4];
@@ -358,19 +404,17 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const float *__restric
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         if (src[u] != nullptr) {
+          const float f = fac[u];
           const float4 a = lo[u], b = hi[u];
-          const float mx = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
-                                 fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
-          out_of_range |= !(mx <= 65504.f);
-          __half2 h0 = __floats2half2_rn(a.x, a.z), h1 = __floats2half2_rn(a.y, a.w);
-          __half2 h2 = __floats2half2_rn(b.x, b.z), h3 = __floats2half2_rn(b.y, b.w);
+          __half2 h0 = __floats2half2_rn(a.x * f, a.z * f), h1 = __floats2half2_rn(a.y * f, a.w * f);
+          __half2 h2 = __floats2half2_rn(b.x * f, b.z * f), h3 = __floats2half2_rn(b.y * f, b.w * f);
           *reinterpret_cast<uint4 *>(xs + (size_t)(pos0 + u) * K + (size_t)i * 8) =
               make_uint4(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
                          *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
         }
     }
+    __syncthreads();   // red and fac are reused by the next four rows
   }
-  if (out_of_range) raise_device_error(Q4MM_DEVERR_F16_RANGE);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -398,10 +442,11 @@ cudaError_t launch_q4_0_mm_tc(const float *x, const uint8_t *w, float *out, int 
   const int32_t *hids = reinterpret_cast<const int32_t *>(ws + L.hids);
   const uint32_t *offs = reinterpret_cast<const uint32_t *>(ws + L.offs);
   uint16_t *xs = reinterpret_cast<uint16_t *>(ws + L.xs);
+  float *xun = reinterpret_cast<float *>(ws + L.xun);
   int sms = 148, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
 
-  gather_rows_kernel<<<(unsigned)(4 * sms), 256, 0, s>>>(x, hids, offs + n_experts, top_k, K, xs, n_rows);
+  gather_rows_kernel<<<(unsigned)(4 * sms), 256, 0, s>>>(x, hids, offs + n_experts, top_k, K, xs, xun, n_rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -430,6 +475,7 @@ cudaError_t launch_q4_0_mm_tc(const float *x, const uint8_t *w, float *out, int 
   MmParams p{};
   p.out = out;
   p.hids = hids;
+  p.xun = xun;
   p.blk = reinterpret_cast<const int4 *>(ws + L.blk);
   p.n_blk = reinterpret_cast<const uint32_t *>(ws + L.n_blk);
   p.N = N;

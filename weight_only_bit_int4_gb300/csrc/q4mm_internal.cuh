@@ -276,10 +276,12 @@ size_t q4_0_mm_workspace_bytes(int64_t n_tokens, int64_t top_k, int64_t N, int64
 //   invalid u32 [1]        rows whose id is >= E
 //   blk     int4 [B]       token blocks (expert, first position in hids, count <= 128, 0)
 //   n_blk   u32 [1]        number of token blocks
-//   xs      fp16 [R, K]    x rows gathered in hids order (the mm operand)
+//   xs      fp16 [R, K]    x rows gathered in hids order, each scaled by a power of two
+//                          (the mm operand)
+//   xun     f32 [R]        per gathered row, the power of two that undoes its scaling
 constexpr int kMoeTokBlock = 128;
 struct MoeWorkspace {
-  size_t htpe, offs, hids, invalid, blk, n_blk, xs, total;
+  size_t htpe, offs, hids, invalid, blk, n_blk, xs, xun, total;
 };
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 inline MoeWorkspace moe_workspace_layout(int64_t n_rows, int64_t K, int64_t E) {
@@ -293,6 +295,7 @@ inline MoeWorkspace moe_workspace_layout(int64_t n_rows, int64_t K, int64_t E) {
   w.blk = o; o = align256(o + 16 * max_blk);
   w.n_blk = o; o = align256(o + 4);
   w.xs = o; o = align256(o + 2 * (size_t)n_rows * (size_t)K);
+  w.xun = o; o = align256(o + 4 * (size_t)n_rows);
   w.total = o;
   return w;
 }
