@@ -39,7 +39,8 @@ def test_q4_dequant_bit_exact(N, K):
                                    (3, 200, 384), (1, 72, 14336), (4, 1000, 128), (3, 1000, 512),
                                    (1, 9, 256), (2, 4104, 2048), (8, 300, 2048), (12, 1000, 4096),
                                    (6, 72, 14336), (13, 4104, 384), (5, 130, 256), (11, 4104, 768),
-                                   (16, 200, 768), (7, 64, 512), (10, 2000, 14336)])
+                                   (16, 200, 768), (7, 64, 512), (10, 2000, 14336),
+                                   (1, 1000, 2304), (9, 1500, 2304), (16, 40, 7424), (1, 2100, 2304)])
 def test_q4_gemv_parity(M, N, K):
     x, w, s, b = _case(20 + M, M, N, K)
     ref = oracle.q4_matmul(x, w, s, b, M, N, K)

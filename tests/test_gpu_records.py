@@ -32,6 +32,30 @@ def test_gemv_record_matches_direct_call(M, N, K, static_weights):
     rec.close()
 
 
+def test_gemv_record_survives_smaller_plans_of_the_same_kernel():
+    """Several shapes share one decode kernel with different shared-memory sizes.  A record
+    planned for the largest must still launch after smaller shapes of the same kernel were
+    recorded and called (the kernel's shared-memory limit is only ever raised)."""
+    shapes = [(4, 14336, 4096), (4, 4096, 4096), (1, 4096, 4096)]   # (M, N, K), largest first
+    data = {}
+    for M, N, K in shapes:
+        w, s, b = synth.int4_weights(770 + M + N // 1024, N, K)
+        x = synth.activations_bf16(771 + M, M, K)
+        data[(M, N, K)] = (x, (dev(w), dev(s), dev(b)))
+    recs = [q.q4_gemv_record(M, N, K, static_weights=True) for M, N, K in shapes]
+    for M, N, K in shapes[1:]:
+        x, W = data[(M, N, K)]
+        q.q4_gemv(dev(x), *W, poisoned_bf16(M, N))
+    for rec, (M, N, K) in zip(recs, shapes):
+        x, W = data[(M, N, K)]
+        y0, y1 = poisoned_bf16(M, N), poisoned_bf16(M, N)
+        rec.gemv(dev(x), *W, y1)
+        q.q4_gemv(dev(x), *W, y0, static_weights=True)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(host_u16(y0), host_u16(y1))
+        rec.close()
+
+
 def test_gemv_records_chain_in_a_graph():
     """A decode chain of recorded calls (x -> y -> next x), captured into a CUDA graph on its
     first replay, gives the bits of the same chain of direct calls."""

@@ -12,9 +12,30 @@
 
 #include <stdint.h>
 
+#include <map>
+#include <mutex>
 #include <new>
+#include <utility>
 
 using namespace q4mm;
+
+namespace q4mm {
+
+cudaError_t ensure_dynamic_smem(const void *fn, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void *>, int> limit;   // (device, kernel) -> limit set
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  int &cur = limit[{dev, fn}];
+  if (bytes <= cur) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) cur = bytes;
+  return e;
+}
+
+}  // namespace q4mm
 
 namespace {
 

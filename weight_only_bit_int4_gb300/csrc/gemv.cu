@@ -20,6 +20,9 @@
 //     through distributed shared memory in rank order (deterministic, no workspace,
 //     no atomics).
 #include "q4mm_internal.cuh"
+#include "tc_common.cuh"
+
+#include <cudaTypedefs.h>
 
 #include <new>
 
@@ -1329,6 +1332,8 @@ struct LaunchSpec {
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[2]{};
   GemvParams params{};
+  int tma_rows = 0;     // > 0: a TMA-fed kernel whose tensor maps are encoded per launch
+  int tma_stages = 0;
 };
 
 template <typename Kern>
@@ -1398,7 +1403,7 @@ Plan make_plan(int M, int N, int K) {
 template <int MT, int RT, bool LUT>
 cudaError_t launch_typed(const GemvParams &p, const Plan &pl, cudaStream_t s, bool overlap, LaunchSpec *rec) {
   auto kern = gemv_kernel<MT, RT, LUT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), (int)pl.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   const int rows_cta = kWarps * 16 * RT;
@@ -1492,7 +1497,7 @@ cudaError_t launch_async_typed(const GemvParams &p, const Plan &pl, cudaStream_t
   if constexpr (!LUT) {
     if (p.K % 256 == 0) kern = gemv_async_kernel<MT, RT, false, true>;
   }
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), (int)pl.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((p.N + kWarps * 16 * RT - 1) / (kWarps * 16 * RT)), (unsigned)pl.S, 1);
@@ -1522,7 +1527,7 @@ cudaError_t launch_gc_typed(const GemvParams &p, const Plan &pl, cudaStream_t s,
                   (reinterpret_cast<uintptr_t>(p.biases) & 15u) == 0;
   auto kern = sb ? gemv_gc_kernel<MT2, RT, true> : gemv_gc_kernel<MT2, RT, false>;
   const size_t smem = gc_smem_bytes(p.M, RT, pl.max_chunks);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((p.N + kWarps * 16 * RT - 1) / (kWarps * 16 * RT)), (unsigned)pl.S, 1);
@@ -1592,7 +1597,7 @@ KsPlan make_ks_plan(int M, int N, int K) {
 template <int MT2, int KS, int DEPTH>
 cudaError_t launch_ks_typed(const GemvParams &p, const KsPlan &pl, cudaStream_t s, bool overlap, LaunchSpec *rec) {
   auto kern = gemv_ks_kernel<MT2, KS, DEPTH>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), (int)pl.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((p.N + 15) / 16), (unsigned)pl.S, 1);
@@ -1675,7 +1680,7 @@ KsPlan make_lks_plan(int M, int N, int K, int block) {
 template <int MT2, int KS, int DEPTH>
 cudaError_t launch_lks_typed(const GemvParams &p, const KsPlan &pl, cudaStream_t s, bool overlap, LaunchSpec *rec) {
   auto kern = gemv_lks_kernel<MT2, KS, DEPTH>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), (int)pl.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((p.N + 15) / 16), (unsigned)pl.S, 1);
@@ -1713,9 +1718,188 @@ cudaError_t launch_lks(const GemvParams &p, const KsPlan &pl, cudaStream_t s, bo
   return launch_lks_typed<MT2, 8, 8>(p, pl, s, overlap, rec);
 }
 
+#include "gemv_tma.cuh"
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// Tensor maps of one decode call: codes uint8 [N][K/2] in 128-byte boxes with the 128-byte
+// swizzle, scales and biases bf16 [N][K/32] in 8-group boxes; R rows per box, zero fill past N.
+cudaError_t make_tq_maps(GemvTmaArgs &a, int R) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const GemvParams &p = a.p;
+  const cuuint32_t estr[2] = {1, 1};
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)(p.K / 2), (cuuint64_t)p.N};
+    const cuuint64_t strides[1] = {(cuuint64_t)(p.K / 2)};
+    const cuuint32_t box[2] = {128u, (cuuint32_t)R};
+    if (enc(&a.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(p.w), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)(p.K / 32), (cuuint64_t)p.N};
+  const cuuint64_t strides[1] = {(cuuint64_t)(p.K / 32) * 2};
+  const cuuint32_t box[2] = {8u, (cuuint32_t)R};
+  if (enc(&a.smap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(p.scales), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+      enc(&a.bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(p.biases), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
+struct TqPlan {
+  int WC = 0, S = 0, maxnh = 0, stages = 0;
+  size_t smem = 0;
+};
+
+// Plans for gemv_tma_kernel, from a sweep of (warps, K splits, stages) over the decode shapes
+// on GB300.  What the sweep showed: every CTA resident at once, at most two CTAs per SM (the
+// next call's CTAs then find room to start streaming while this call finishes), the work as
+// evenly spread over the SMs as that allows, at least 8 consumer warps per SM, and as many
+// ring stages as the CTA's share of shared memory holds.  Ties go to the fewest K splits
+// (each split adds a cluster reduction), then to 8 consumer warps per CTA for M >= 3 and 4
+// below (measured best in each range).
+TqPlan make_tq_plan(int M, int N, int K) {
+  TqPlan best;
+  int sms = 152, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
+  }
+  const int NH = K / 256, NB = (NH + 1) / 2;
+  const int regs = 112;   // per thread, at least what ptxas -v reports for these kernels
+  const int wc_pref = M >= 3 ? 8 : 4;
+  double best_score = -1e30;
+  for (int WC : {wc_pref, 12 - wc_pref}) {
+    const int R = 16 * WC, threads = (WC + 1) * 32;
+    for (int S : {1, 2, 4, 8}) {
+      if (S > NB) break;
+      int maxnh = 0;
+      for (int sp = 0; sp < S; ++sp) {
+        const int b0 = (sp * NB) / S, b1 = ((sp + 1) * NB) / S;
+        maxnh = std::max(maxnh, std::min(2 * b1, NH) - 2 * b0);
+      }
+      const long long ctas = (long long)((N + R - 1) / R) * S;
+      const int need = (int)((ctas + sms - 1) / sms);   // CTAs on the busiest SM
+      if (need > 2 || need * threads * regs > 65536) continue;
+      const size_t budget = (size_t)(227 * 1024) / need;
+      const size_t fixed = tq_smem_bytes(M, maxnh, R, 0);
+      if (fixed >= budget) continue;
+      const int stages = (int)std::min<size_t>(8, (budget - fixed) / (tq_stage_bytes(R) + 16));
+      if (stages < 3) continue;
+      const double balance = (double)ctas / (double)((long long)need * sms);
+      const double score = balance * std::min(1.0, need * WC / 8.0) - 1e-3 * S;
+      if (score > best_score + 1e-9) {
+        best_score = score;
+        best.WC = WC; best.S = S; best.maxnh = maxnh; best.stages = stages;
+        best.smem = tq_smem_bytes(M, maxnh, R, stages);
+      }
+    }
+  }
+  return best;
+}
+
+template <int NT, int WC>
+cudaError_t launch_tq_typed(GemvParams &p, const TqPlan &pl, cudaStream_t s, bool overlap, LaunchSpec *rec) {
+  auto kern = gemv_tma_kernel<NT, WC>;
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), (int)pl.smem);
+  if (e != cudaSuccess) return e;
+  p.max_chunks_per_cta = pl.maxnh;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((p.N + 16 * WC - 1) / (16 * WC)), (unsigned)pl.S, 1);
+  cfg.blockDim = dim3((WC + 1) * 32, 1, 1);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pl.S > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 1;
+    attr[n].val.clusterDim.y = (unsigned)pl.S;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (overlap) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = (unsigned)n;
+  if (rec != nullptr) {
+    rec->fn = reinterpret_cast<const void *>(kern);
+    rec->cfg = cfg;
+    for (int i = 0; i < n; ++i) rec->attr[i] = attr[i];
+    rec->cfg.attrs = nullptr;   // re-pointed at rec->attr by each replay
+    rec->params = p;
+    rec->tma_rows = 16 * WC;
+    rec->tma_stages = pl.stages;
+    return cudaSuccess;
+  }
+  GemvTmaArgs args{};
+  args.p = p;
+  args.stages = pl.stages;
+  e = make_tq_maps(args, 16 * WC);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, kern, args);
+}
+
+template <int NT>
+cudaError_t launch_tq_w(GemvParams &p, const TqPlan &pl, cudaStream_t s, bool overlap, LaunchSpec *rec) {
+  if (pl.WC == 4) return launch_tq_typed<NT, 4>(p, pl, s, overlap, rec);
+  return launch_tq_typed<NT, 8>(p, pl, s, overlap, rec);
+}
+
+#ifdef Q4MM_TUNING
+// Tuning builds only: environment overrides of the decode plan, for plan sweeps.
+int tuning_env(const char *name, int dflt) {
+  const char *v = getenv(name);
+  return v ? atoi(v) : dflt;
+}
+#endif
+
 template <bool LUT>
 cudaError_t launch_any(GemvParams &p, cudaStream_t s, bool overlap, LaunchSpec *rec = nullptr) {
   p.chunks = (p.K / 32 + 3) / 4;
+  // INT4 with K % 256 == 0: the TMA-fed kernel for 3 <= M <= 16; at M <= 2 the K-split
+  // group-column kernel below measured faster on the decode shapes.
+  bool use_tq = !LUT && p.M >= 3 && p.M <= 16 && p.K % 256 == 0;
+#ifdef Q4MM_TUNING
+  use_tq = use_tq && tuning_env("Q4MM_TQ", 1) != 0;
+#endif
+  if (use_tq) {
+    TqPlan tp = make_tq_plan(p.M, p.N, p.K);
+#ifdef Q4MM_TUNING
+    if (getenv("Q4MM_TQ_W") || getenv("Q4MM_TQ_S") || getenv("Q4MM_TQ_ST")) {
+      tp.WC = tuning_env("Q4MM_TQ_W", tp.WC);
+      tp.S = tuning_env("Q4MM_TQ_S", tp.S);
+      const int NH = p.K / 256, NB = (NH + 1) / 2;
+      tp.maxnh = 0;
+      for (int sp = 0; sp < tp.S; ++sp) {
+        const int b0 = (sp * NB) / tp.S, b1 = ((sp + 1) * NB) / tp.S;
+        tp.maxnh = std::max(tp.maxnh, std::min(2 * b1, NH) - 2 * b0);
+      }
+      tp.stages = tuning_env("Q4MM_TQ_ST", tp.stages);
+      tp.smem = tq_smem_bytes(p.M, tp.maxnh, 16 * tp.WC, tp.stages);
+    }
+#endif
+    if (tp.WC > 0) return p.M <= 8 ? launch_tq_w<1>(p, tp, s, overlap, rec) : launch_tq_w<2>(p, tp, s, overlap, rec);
+  }
   if (LUT && p.M <= 4 && p.K % 512 == 0 &&
       (p.lut_block_shift_div == 1 || p.lut_block_shift_div == 2 || p.lut_block_shift_div == 4) &&
       (reinterpret_cast<uintptr_t>(p.scales) & 15u) == 0) {
@@ -1800,6 +1984,15 @@ cudaError_t replay_q4_gemv(const void *record, const uint16_t *x, const uint32_t
   cudaLaunchConfig_t cfg = rec->cfg;
   cfg.attrs = const_cast<cudaLaunchAttribute *>(rec->attr);
   cfg.stream = s;
+  if (rec->tma_rows > 0) {   // the tensor maps hold the pointers: encode them for this launch
+    GemvTmaArgs ta{};
+    ta.p = p;
+    ta.stages = rec->tma_stages;
+    const cudaError_t e = make_tq_maps(ta, rec->tma_rows);
+    if (e != cudaSuccess) return e;
+    void *args[] = {&ta};
+    return cudaLaunchKernelExC(&cfg, rec->fn, args);
+  }
   void *args[] = {&p};
   return cudaLaunchKernelExC(&cfg, rec->fn, args);
 }

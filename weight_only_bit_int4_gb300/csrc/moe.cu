@@ -443,7 +443,7 @@ cudaError_t launch_route_internal(const uint32_t *ids, int n_rows, int E, uint32
   }
   const int nw = route_warps(E);
   const size_t sm = route_smem(E, nw);
-  cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(route_kernel), (int)sm);
   if (e != cudaSuccess) return e;
   route_kernel<<<1, nw * 32, sm, s>>>(ids, n_rows, E, nw, htpe, offs, hids, n_invalid, blk, n_blk, zero_out,
                                       zero_cols);
@@ -681,7 +681,7 @@ template <bool SWIGLU, int PIECE>
 cudaError_t plan_mv_mma_typed(const MvParams &p, int ks, int maxc, size_t smem, MvSpec *sp) {
   auto kern = ks == 4 ? q4_0_mv_mma_kernel<4, SWIGLU, PIECE>
             : ks == 2 ? q4_0_mv_mma_kernel<2, SWIGLU, PIECE> : q4_0_mv_mma_kernel<1, SWIGLU, PIECE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   sp->fn = reinterpret_cast<const void *>(kern);
   sp->grid = dim3((unsigned)((p.N + 15) / 16), (unsigned)(p.n_rows < 65535 ? p.n_rows : 65535), 1);

@@ -259,6 +259,11 @@ cudaError_t launch_q4_0_mm(const float *x, const uint8_t *w, const uint32_t *ids
                            int n_tokens, int top_k, int N, int K, int n_experts,
                            uint64_t expert_stride, void *workspace, cudaStream_t s);
 
+// Raise kernel `fn`'s dynamic shared-memory limit on the current device to at least `bytes`,
+// never lowering it.  The same kernel serves shapes of different sizes, and a dispatch record
+// planned for a large shape must still launch after a smaller shape was planned or called.
+cudaError_t ensure_dynamic_smem(const void *fn, int bytes);
+
 // Routed-row count check: n_tokens and top_k are each bounded before their product is
 // formed, so a huge top_k cannot overflow int64 and wrap past the 2^24 limit.
 inline bool routed_rows_ok(int64_t n_tokens, int64_t top_k) {
