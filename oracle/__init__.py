@@ -90,6 +90,9 @@ def _declare(L: ctypes.CDLL) -> None:
         "oracle_q4_0_dequant_row": ([_P, _I, _P], None),
         "oracle_q4_0_matmul_id": ([_P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_uint64, _P], None),
         "oracle_q4_0_matmul_id_rows": ([_P, _P, _P, _I, _I, _I, _I, ctypes.c_uint64, _P, _I, _P], None),
+        "oracle_q8_0_dequant_row": ([_P, _I, _P], None),
+        "oracle_q8_0_matmul_id": ([_P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_uint64, _P], None),
+        "oracle_q8_0_matmul_id_rows": ([_P, _P, _P, _I, _I, _I, _I, ctypes.c_uint64, _P, _I, _P], None),
         "oracle_q4_0_route": ([_P, _I, _I, _P, _P, _P], None),
         "oracle_q4_0_matmul_id_swiglu": ([_P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_uint64, _P], None),
         "oracle_q4_0_matmul_id_swiglu_rows": ([_P, _P, _P, _P, _I, _I, _I, ctypes.c_uint64, _P, _I, _P],
@@ -260,6 +263,33 @@ def q4_0_matmul_id_rows(x, w, ids, top_k: int, N: int, K: int, n_experts: int,
     rows = _c(rows, np.int64)
     out = np.empty((rows.size, N), np.float64)
     lib().oracle_q4_0_matmul_id_rows(_p(x), _p(w), _p(ids), top_k, N, K, n_experts,
+                                     expert_stride, _p(rows), rows.size, _p(out))
+    return out
+
+
+def q8_0_dequant_row(row_bytes, K: int) -> np.ndarray:
+    r = _c(row_bytes, np.uint8)
+    out = np.empty(K, np.float32)
+    lib().oracle_q8_0_dequant_row(_p(r), K, _p(out))
+    return out
+
+
+def q8_0_matmul_id(x, w, ids, n_tokens: int, top_k: int, N: int, K: int, n_experts: int,
+                   expert_stride: int) -> np.ndarray:
+    """fp64 [n_tokens*top_k, N]: out[r] = x[r / top_k] . dequant(W[ids[r]])^T, Q8_0 blocks."""
+    x, w, ids = _c(x, np.float32), _c(w, np.uint8), _c(ids, np.uint32)
+    out = np.empty((n_tokens * top_k, N), np.float64)
+    lib().oracle_q8_0_matmul_id(_p(x), _p(w), _p(ids), n_tokens, top_k, N, K, n_experts,
+                                expert_stride, _p(out))
+    return out
+
+
+def q8_0_matmul_id_rows(x, w, ids, top_k: int, N: int, K: int, n_experts: int,
+                        expert_stride: int, rows) -> np.ndarray:
+    x, w, ids = _c(x, np.float32), _c(w, np.uint8), _c(ids, np.uint32)
+    rows = _c(rows, np.int64)
+    out = np.empty((rows.size, N), np.float64)
+    lib().oracle_q8_0_matmul_id_rows(_p(x), _p(w), _p(ids), top_k, N, K, n_experts,
                                      expert_stride, _p(rows), rows.size, _p(out))
     return out
 

@@ -28,7 +28,9 @@
  *        routed mat-vec.
  *   The Q4_0 block layout itself (fp16 d + 16 bytes of nibbles, low nibbles are
  *   elements 0..15, high nibbles 16..31, value (q-8)*d) is not printed on [P3]; it is
- *   the GGML Q4_0 format as the problem statement gives it.
+ *   the GGML Q4_0 format as the problem statement gives it.  [P3] also names Q8_0 among
+ *   its routed kernels without printing its block; the GGML Q8_0 block is used: fp16 d,
+ *   then 32 signed bytes, value q*d.
  */
 #include <math.h>
 #include <stdint.h>
@@ -414,6 +416,64 @@ void oracle_q4_0_matmul_id_rows(const float *x, const uint8_t *w, const uint32_t
 {
     for (int64_t i = 0; i < count; ++i)
         q4_0_one_row(x, w, ids[rows[i]], rows[i] / top_k, N, K, n_experts, expert_stride,
+                     out + i * N);
+}
+
+/* ------------------------------------------------------------------------- */
+/* GGML Q8_0 expert-routed matmul  [P3 module doc; the type is one of the     */
+/* routed kernels the page names]                                            */
+/*   Same routing as Q4_0.  Block (32 values, 34 bytes): fp16 d (little      */
+/*   endian), then 32 signed bytes qs; element j is qs[j] (two's complement) */
+/*   and its value is qs[j] * d.                                             */
+/* ------------------------------------------------------------------------- */
+
+static float q8_0_value(const uint8_t *row, int64_t k)
+{
+    const uint8_t *blk = row + (k / 32) * 34;
+    float d = oracle_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));
+    int q = (int)blk[2 + k % 32];
+    if (q >= 128)
+        q -= 256;                    /* the byte is a signed integer */
+    return (float)q * d;             /* exact: 8-bit integer times 11-bit d */
+}
+
+void oracle_q8_0_dequant_row(const uint8_t *row, int64_t K, float *out)
+{
+    for (int64_t k = 0; k < K; ++k)
+        out[k] = q8_0_value(row, k);
+}
+
+static void q8_0_one_row(const float *x, const uint8_t *w, uint32_t e, int64_t t,
+                         int64_t N, int64_t K, int64_t n_experts, uint64_t expert_stride,
+                         double *out_row)
+{
+    for (int64_t n = 0; n < N; ++n) {
+        double acc = 0.0;
+        if ((int64_t)e < n_experts) {
+            const uint8_t *row = w + (uint64_t)e * expert_stride + (uint64_t)(n * (K / 32) * 34);
+            for (int64_t k = 0; k < K; ++k)
+                acc += (double)x[t * K + k] * (double)q8_0_value(row, k);
+        }
+        out_row[n] = acc;
+    }
+}
+
+void oracle_q8_0_matmul_id(const float *x, const uint8_t *w, const uint32_t *ids,
+                           int64_t n_tokens, int64_t top_k, int64_t N, int64_t K,
+                           int64_t n_experts, uint64_t expert_stride, double *out)
+{
+    for (int64_t r = 0; r < n_tokens * top_k; ++r)
+        q8_0_one_row(x, w, ids[r], r / top_k, N, K, n_experts, expert_stride, out + r * N);
+}
+
+/* Only the routed rows listed in rows[] (out is [count, N]). */
+void oracle_q8_0_matmul_id_rows(const float *x, const uint8_t *w, const uint32_t *ids,
+                                int64_t top_k, int64_t N, int64_t K, int64_t n_experts,
+                                uint64_t expert_stride, const int64_t *rows, int64_t count,
+                                double *out)
+{
+    for (int64_t i = 0; i < count; ++i)
+        q8_0_one_row(x, w, ids[rows[i]], rows[i] / top_k, N, K, n_experts, expert_stride,
                      out + i * N);
 }
 

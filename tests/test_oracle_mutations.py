@@ -85,6 +85,15 @@ MUTATIONS = {
     "q4_0 routed-row form reads the routed row as the token": (
         "q4_0_one_row(x, w, ids[rows[i]], rows[i] / top_k, N, K, n_experts, expert_stride,",
         "q4_0_one_row(x, w, ids[rows[i]], rows[i], N, K, n_experts, expert_stride,"),
+    "q8_0 bytes read as unsigned": (
+        "    if (q >= 128)\n        q -= 256;                    /* the byte is a signed integer */\n",
+        ""),
+    "q8_0 block stride 32 bytes": (
+        "const uint8_t *blk = row + (k / 32) * 34;",
+        "const uint8_t *blk = row + (k / 32) * 32;"),
+    "q8_0 routed-row form reads the routed row as the token": (
+        "q8_0_one_row(x, w, ids[rows[i]], rows[i] / top_k, N, K, n_experts, expert_stride,",
+        "q8_0_one_row(x, w, ids[rows[i]], rows[i], N, K, n_experts, expert_stride,"),
     "route lists descending": (
         "for (int64_t r = 0; r < n_rows; ++r)\n            if ((int64_t)ids[r] == e) {",
         "for (int64_t r = n_rows - 1; r >= 0; --r)\n            if ((int64_t)ids[r] == e) {"),

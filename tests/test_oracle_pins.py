@@ -415,6 +415,58 @@ def test_q4_0_matmul_id_rows_matches_full():
         oracle.q4_0_matmul_id_rows(x, w, ids, top_k, N, K, n_exp, stride, rows), full[rows])
 
 # ---------------------------------------------------------------------------------------
+# GGML Q8_0 expert-routed (the same routing; 34-byte blocks: fp16 d, 32 signed bytes)
+# ---------------------------------------------------------------------------------------
+
+def _q8_hand_block():
+    # d = 0.5 (fp16 0x3800, little endian); qs[j] = 8j - 128 (two's complement bytes),
+    # except qs[31] = 127: the signed range's ends are both present
+    qs = [(8 * j - 128) & 0xFF for j in range(31)] + [127]
+    return np.array([0x00, 0x38] + qs, np.uint8)
+
+
+def test_q8_0_block_hand_built():
+    got = oracle.q8_0_dequant_row(_q8_hand_block(), 32)
+    want = [(8 * j - 128) * 0.5 for j in range(31)] + [127 * 0.5]
+    np.testing.assert_array_equal(got, np.array(want, np.float32))
+
+
+def test_q8_0_zero_bytes_give_zero_and_one_hot_reads_a_column():
+    n_exp, N, K = 2, 3, 64
+    w = np.zeros(n_exp * N * (K // 32) * 34, np.uint8)
+    blocks = w.reshape(n_exp, N, K // 32, 34)
+    blocks[..., 1] = 0x3C                      # d = 1.0, qs = 0 everywhere
+    x = synth.activations_f32(95, 2, K)
+    ids = np.array([1, 0, 0, 1], np.uint32)
+    assert np.all(oracle.q8_0_matmul_id(x, w, ids, 2, 2, N, K, n_exp, N * (K // 32) * 34) == 0.0)
+    blocks[1, 2, 1] = _q8_hand_block()         # expert 1, row 2, second block (k = 32..63)
+    k0 = 32 + 5                                # element 5: (40 - 128) * 0.5 = -44
+    x1 = np.zeros((1, K), np.float32); x1[0, k0] = 1.0
+    out = oracle.q8_0_matmul_id(x1, w, np.array([1], np.uint32), 1, 1, N, K, n_exp, N * (K // 32) * 34)
+    np.testing.assert_array_equal(out[0], [0.0, 0.0, -44.0])
+
+
+def test_q8_0_top1_ids_zero_is_dense_matmul_and_rows_follow_ids():
+    n_exp, N, K, T, top_k = 3, 6, 96, 5, 2
+    w, stride = synth.q8_0_experts(97, n_exp, N, K, expert_stride=N * (K // 32) * 34 + 32)
+    x = synth.activations_f32(98, T, K)
+    out = oracle.q8_0_matmul_id(x, w, np.zeros(T, np.uint32), T, 1, N, K, n_exp, stride)
+    Wd = np.stack([oracle.q8_0_dequant_row(w[n * (K // 32) * 34:(n + 1) * (K // 32) * 34], K)
+                   for n in range(N)]).astype(np.float64)
+    np.testing.assert_allclose(out, x.astype(np.float64) @ Wd.T, rtol=1e-12, atol=1e-12)
+    ids = np.array([2, 1, 0, 2, 1, 1, 0, 0, 2, 99], np.uint32)      # the last id is out of range
+    full = oracle.q8_0_matmul_id(x, w, ids, T, top_k, N, K, n_exp, stride)
+    for r in range(T * top_k - 1):
+        one = oracle.q8_0_matmul_id(x[r // top_k:r // top_k + 1], w, ids[r:r + 1], 1, 1, N, K, n_exp, stride)
+        np.testing.assert_array_equal(full[r], one[0])
+    assert np.all(full[-1] == 0.0)
+    xr = synth.activations_f32(99, T * top_k, K)   # extra rows: a wrong token row reads real data
+    rows = np.array([0, 3, 5, 8, 9, 1])
+    np.testing.assert_array_equal(oracle.q8_0_matmul_id_rows(xr, w, ids, top_k, N, K, n_exp, stride, rows),
+                                  oracle.q8_0_matmul_id(xr, w, ids, T, top_k, N, K, n_exp, stride)[rows])
+
+
+# ---------------------------------------------------------------------------------------
 # Fused SwiGLU + routed Q4_0 mat-vec (quantized_matmul_id_ggml.rs,
 # quantized_matmul_id_swiglu_q4_0): out[r] = (silu(gate[r]) * up[r]) . dequant(W[ids[r]])^T
 # ---------------------------------------------------------------------------------------

@@ -146,6 +146,29 @@ def q4_0_experts(seed: int, n_experts: int, N: int, K: int, expert_stride: int |
     return w, stride
 
 
+Q8_0_BLOCK_BYTES = 34
+
+
+def q8_0_experts(seed: int, n_experts: int, N: int, K: int, expert_stride: int | None = None):
+    """(w uint8 [n_experts * expert_stride], expert_stride): each 34-byte block holds an
+    fp16 d ~ U[0.005, 0.02] (little endian) followed by 32 uniform random bytes (signed
+    integers -128..127)."""
+    assert K % 32 == 0
+    per_expert = N * (K // 32) * Q8_0_BLOCK_BYTES
+    stride = per_expert if expert_stride is None else expert_stride
+    assert stride >= per_expert
+    nblk = n_experts * N * (K // 32)
+    blocks = np.empty((nblk, Q8_0_BLOCK_BYTES), np.uint8)
+    d = (0.005 + 0.015 * uniform(seed, 13, nblk)).astype(np.float16).view(np.uint8).reshape(nblk, 2)
+    blocks[:, 0:2] = d
+    blocks[:, 2:] = (u64(seed, 14, nblk * 32) >> np.uint64(56)).astype(np.uint8).reshape(nblk, 32)
+    w = np.zeros(n_experts * stride, np.uint8)
+    per = blocks.reshape(n_experts, per_expert)
+    for e in range(n_experts):
+        w[e * stride:e * stride + per_expert] = per[e]
+    return w, stride
+
+
 def routing_ids(seed: int, n_tokens: int, top_k: int, n_experts: int) -> np.ndarray:
     """ids uint32 [n_tokens * top_k]: top_k distinct experts per token, uniform."""
     assert top_k <= n_experts
