@@ -230,6 +230,26 @@ q4mm_status q4_0_matmul_id_swiglu(const float *gate, const float *up, const void
                                   uint64_t expert_stride, q4mm_stream_t stream);
 
 /* ======================================================================================
+ * GGML Q8_0 expert-routed matmul  (quantized_matmul_id_ggml.rs names Q8_0 among its routed
+ * kernels and its decode records; the page does not print the block, so this is the GGML
+ * Q8_0 block:)  34 bytes per 32 values: fp16 d (little endian), then 32 signed bytes qs;
+ * value of element j = qs[j] * d.  Row n of expert e is K/32 consecutive blocks at
+ * w + e*expert_stride + n*(K/32)*34.  x, ids, out, routing and modes as q4_0_matmul_id:
+ *   out[r][n] = sum_k x[r / top_k][k] * W[ids[r]][n][k]   (f32, fp32 accumulation);
+ *   an id >= n_experts gives a zero row and sets Q4MM_DEVERR_BAD_EXPERT.
+ * Mode 0 (automatic: mat-mat when n_tokens > Q4MM_MM_ID_THRESHOLD), 1 (mat-vec: each routed
+ * row in order) or 2 (mat-mat: route, then visit the routed rows expert by expert).  The
+ * mat-mat form needs q8_0_matmul_id_workspace_size(...) bytes of 256-byte aligned workspace
+ * (the routing lists).  Requirements: K % 32 == 0, expert_stride >= N*(K/32)*34, x and out
+ * 16-byte aligned, ids 4-byte aligned. */
+size_t q8_0_matmul_id_workspace_size(int64_t n_tokens, int64_t top_k, int64_t N, int64_t K,
+                                     int64_t n_experts);
+q4mm_status q8_0_matmul_id(const float *x, const void *w, const uint32_t *ids, float *out,
+                           int64_t n_tokens, int64_t top_k, int64_t N, int64_t K,
+                           int64_t n_experts, uint64_t expert_stride, int mode,
+                           void *workspace, size_t workspace_bytes, q4mm_stream_t stream);
+
+/* ======================================================================================
  * Dispatch records: plan a decode call once, replay it with new pointers.
  *
  * The counterpart of the pages' pre-baked decode dispatches (quantized_matmul_id_ggml.rs,

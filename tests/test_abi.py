@@ -94,6 +94,26 @@ def test_moe_argument_checks(L):
     assert L.q4_0_matmul_id_swiglu(None, None, None, None, None, 0, 8, 64, 64, 16, 0, None) == 0
     # routing: too many experts
     assert L.q4_0_route(FAKE, 8, 2000, FAKE, FAKE, None, None) == 1
+    # a top_k so large that n_tokens * top_k would overflow int64 is refused, not wrapped
+    assert L.q4_0_matmul_id(FAKE, FAKE, FAKE, FAKE, 1 << 40, 1 << 40, 64, 64, 16, 1 << 20, 1, None, 0, None) == 1
+    assert L.q4_0_matmul_id_workspace_size(1 << 40, 1 << 40, 64, 64, 16) == 0
+
+
+def test_q8_0_argument_checks(L):
+    stride = 64 * 2 * 34
+    # expert_stride smaller than one expert (34-byte blocks) -> INVALID_ARG
+    assert L.q8_0_matmul_id(FAKE, FAKE, FAKE, FAKE, 2, 8, 64, 64, 16, stride - 1, 1, None, 0, None) == 1
+    # K not a multiple of 32, bad mode
+    assert L.q8_0_matmul_id(FAKE, FAKE, FAKE, FAKE, 2, 8, 64, 48, 16, 1 << 20, 1, None, 0, None) == 1
+    assert L.q8_0_matmul_id(FAKE, FAKE, FAKE, FAKE, 2, 8, 64, 64, 16, stride, 3, None, 0, None) == 1
+    # mat-mat without (enough) workspace -> WORKSPACE; misaligned x -> UNSUPPORTED
+    assert L.q8_0_matmul_id(FAKE, FAKE, FAKE, FAKE, 64, 8, 64, 64, 16, stride, 2, None, 0, None) == 3
+    need = L.q8_0_matmul_id_workspace_size(64, 8, 64, 64, 16)
+    assert 0 < need < L.q4_0_matmul_id_workspace_size(64, 8, 64, 64, 16)   # no gathered rows
+    assert L.q8_0_matmul_id(FAKE, FAKE, FAKE, FAKE, 64, 8, 64, 64, 16, stride, 2, FAKE, need - 1, None) == 3
+    assert L.q8_0_matmul_id(FAKE + 4, FAKE, FAKE, FAKE, 2, 8, 64, 64, 16, stride, 1, None, 0, None) == 2
+    # n_tokens == 0 is a no-op
+    assert L.q8_0_matmul_id(None, None, None, None, 0, 8, 64, 64, 16, 0, 0, None, 0, None) == 0
 
 
 def test_record_argument_checks(L):

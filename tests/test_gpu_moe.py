@@ -230,3 +230,62 @@ def test_swiglu_tiny_shapes(n_tokens, top_k, E, N, K):
     ref = oracle.q4_0_matmul_id_swiglu(gate, up, w, ids, N, K, E, stride)
     got = _run_swiglu(gate, up, w, ids, top_k, N, K, E, stride)
     assert_within_tolerance(got, ref, "tiny swiglu")
+
+
+# ---------------------------------------------------------------------------------------
+# GGML Q8_0 routed matmul: both forms against the oracle
+# ---------------------------------------------------------------------------------------
+
+def _q8_case(seed, n_tokens, top_k, E, N, K, pad=0):
+    per = N * (K // 32) * 34
+    w, stride = synth.q8_0_experts(seed, E, N, K, expert_stride=per + pad)
+    ids = synth.routing_ids(seed + 1, n_tokens, top_k, E)
+    x = synth.activations_f32(seed + 2, n_tokens, K)
+    return x, w, stride, ids
+
+
+def _run_q8(x, w, ids, top_k, N, K, E, stride, mode):
+    n_rows = x.shape[0] * top_k
+    out = torch.full((n_rows, N), float("nan"), dtype=torch.float32, device=DEV)
+    ws = None
+    if mode != 1:
+        ws = torch.empty(q.q8_0_matmul_id_workspace_size(x.shape[0], top_k, N, K, E), dtype=torch.uint8, device=DEV)
+    q.q8_0_matmul_id(dev(x), dev(w), dev(ids), out, top_k, N, K, E, stride, mode=mode, workspace=ws)
+    return out.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("n_tokens,top_k,E,N,K,pad", [(1, 8, 64, 96, 256, 0), (5, 2, 6, 64, 2048, 2),
+                                                      (40, 8, 16, 130, 512, 16), (33, 1, 3, 256, 96, 0),
+                                                      (3, 4, 9, 70, 4096, 0), (2, 2, 3, 20, 32, 0)])
+def test_q8_0_parity(mode, n_tokens, top_k, E, N, K, pad):
+    x, w, stride, ids = _q8_case(200 + n_tokens, n_tokens, top_k, E, N, K, pad)
+    ref = oracle.q8_0_matmul_id(x, w, ids, n_tokens, top_k, N, K, E, stride)
+    got = _run_q8(x, w, ids, top_k, N, K, E, stride, mode)
+    assert_within_tolerance(got, ref, f"q8_0_matmul_id mode={mode}")
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_q8_0_invalid_id_gives_zero_row(mode):
+    n_tokens, top_k, E, N, K = 300, 4, 8, 64, 128
+    x, w, stride, ids = _q8_case(17, n_tokens, top_k, E, N, K)
+    ids = ids.copy()
+    bad_rows = [5, 100, 101, 700, 1199]
+    ids[bad_rows] = 99
+    q.device_errors()
+    got = _run_q8(x, w, ids, top_k, N, K, E, stride, mode)
+    assert np.all(got[bad_rows] == 0.0)
+    assert_within_tolerance(got, oracle.q8_0_matmul_id(x, w, ids, n_tokens, top_k, N, K, E, stride), "q8_0 invalid id")
+    assert q.device_errors() & 0x2
+
+
+@pytest.mark.parametrize("n_tokens,mode", [(1, 1), (512, 2)])
+def test_q8_0_full_size_sampled(n_tokens, mode):
+    E, top_k, N, K = 64, 8, 1408, 2048
+    x, w, stride, ids = _q8_case(4600 + n_tokens, n_tokens, top_k, E, N, K)
+    got = _run_q8(x, w, ids, top_k, N, K, E, stride, mode)
+    assert np.all(np.isfinite(got))
+    rows = np.unique(np.concatenate([np.arange(min(8, n_tokens * top_k)),
+                                     np.random.default_rng(n_tokens + 7).integers(0, n_tokens * top_k, 24)]))
+    ref = oracle.q8_0_matmul_id_rows(x, w, ids, top_k, N, K, E, stride, rows)
+    assert_within_tolerance(got[rows], ref, f"q8_0 full n_tokens={n_tokens} mode={mode}")

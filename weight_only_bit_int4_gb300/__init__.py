@@ -136,6 +136,20 @@ def q4_0_matmul_id(x, w, ids, out, top_k: int, N: int, K: int, n_experts: int,
         mode, _ptr(workspace), ws_bytes, _stream(stream)))
 
 
+def q8_0_matmul_id_workspace_size(n_tokens: int, top_k: int, N: int, K: int, n_experts: int) -> int:
+    return int(lib().q8_0_matmul_id_workspace_size(n_tokens, top_k, N, K, n_experts))
+
+
+def q8_0_matmul_id(x, w, ids, out, top_k: int, N: int, K: int, n_experts: int,
+                   expert_stride: int, mode: int = 0, workspace=None, stream=None) -> None:
+    """out[n_tokens*top_k, N] f32: row r = x[r // top_k] . dequant_q8_0(W[ids[r]])^T."""
+    n_tokens = x.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("q8_0_matmul_id", lib().q8_0_matmul_id(
+        _ptr(x), _ptr(w), _ptr(ids), _ptr(out), n_tokens, top_k, N, K, n_experts, expert_stride,
+        mode, _ptr(workspace), ws_bytes, _stream(stream)))
+
+
 def q4_0_matmul_id_swiglu(gate, up, w, ids, out, top_k: int, N: int, K: int, n_experts: int,
                           expert_stride: int, stream=None) -> None:
     """out[r, N] f32 = (silu(gate[r]) * up[r]) . dequant_q4_0(W[ids[r]])^T for every routed row

@@ -282,6 +282,41 @@ q4mm_status q4_0_matmul_id(const float *x, const void *w, const uint32_t *ids, f
                                   (int)n_experts, expert_stride, s));
 }
 
+size_t q8_0_matmul_id_workspace_size(int64_t n_tokens, int64_t top_k, int64_t N, int64_t K,
+                                     int64_t n_experts) {
+  if (n_tokens < 1 || !routed_rows_ok(n_tokens, top_k) || N < 1 || K < 32 || N > kMaxDim || K > kMaxDim ||
+      n_experts < 1 || n_experts > 1024)
+    return 0;
+  return q8_0_mm_workspace_bytes(n_tokens, top_k, n_experts);
+}
+
+q4mm_status q8_0_matmul_id(const float *x, const void *w, const uint32_t *ids, float *out,
+                           int64_t n_tokens, int64_t top_k, int64_t N, int64_t K,
+                           int64_t n_experts, uint64_t expert_stride, int mode,
+                           void *workspace, size_t workspace_bytes, q4mm_stream_t stream) {
+  if (n_tokens == 0) return Q4MM_OK;
+  if (!x || !w || !ids || !out) return Q4MM_ERR_INVALID_ARG;
+  if (n_tokens < 0 || top_k < 1 || N < 1 || K < 32 || K % 32 != 0 || n_experts < 1 ||
+      n_experts > 1024 || N > kMaxDim || K > kMaxDim)
+    return Q4MM_ERR_INVALID_ARG;
+  if (!routed_rows_ok(n_tokens, top_k)) return Q4MM_ERR_INVALID_ARG;
+  const uint64_t per_expert = (uint64_t)N * (uint64_t)(K / 32) * 34u;
+  if (expert_stride < per_expert) return Q4MM_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 2) return Q4MM_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(ids, 4)) return Q4MM_ERR_UNSUPPORTED;
+  const bool mm = mode == 2 || (mode == 0 && n_tokens > Q4MM_MM_ID_THRESHOLD);
+  if (mm) {
+    const size_t need = q8_0_mm_workspace_bytes(n_tokens, top_k, n_experts);
+    if (!workspace || workspace_bytes < need) return Q4MM_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return Q4MM_ERR_UNSUPPORTED;
+  }
+  q4mm_status st = check_device();
+  if (st != Q4MM_OK) return st;
+  return from_cuda(launch_q8_0_matmul_id(x, static_cast<const uint8_t *>(w), ids, out, (int)n_tokens, (int)top_k,
+                                         (int)N, (int)K, (int)n_experts, expert_stride, mm, workspace,
+                                         (cudaStream_t)stream));
+}
+
 q4mm_status q4_0_matmul_id_swiglu(const float *gate, const float *up, const void *w,
                                   const uint32_t *ids, float *out, int64_t n_tokens, int64_t top_k,
                                   int64_t N, int64_t K, int64_t n_experts, uint64_t expert_stride,

@@ -1880,6 +1880,7 @@ cudaError_t launch_any(GemvParams &p, cudaStream_t s, bool overlap, LaunchSpec *
   // group-column kernel below measured faster on the decode shapes.
   bool use_tq = !LUT && p.M >= 3 && p.M <= 16 && p.K % 256 == 0;
 #ifdef Q4MM_TUNING
+  if (!LUT && p.M <= 16 && p.K % 256 == 0 && getenv("Q4MM_TQ_W")) use_tq = true;
   use_tq = use_tq && tuning_env("Q4MM_TQ", 1) != 0;
 #endif
   if (use_tq) {

@@ -182,11 +182,15 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const uint32_t *__
 // Mat-vec: CTA = (routed row, 32 weight rows).  4 warps x 8 weight rows.  Lane l takes
 // blocks l, l+32, ... of a K segment; its x values for those blocks stay in registers
 // across the warp's 8 weight rows.  Weight rows are first copied to shared memory with
-// coalesced loads (18-byte blocks are not 4-byte aligned in global memory).
+// coalesced loads (18- and 34-byte blocks are not 4-byte aligned in global memory).
+// BT selects the block type: Q4_0 (18 bytes: fp16 d, 16 bytes of nibbles, value (q - 8) d)
+// or Q8_0 (34 bytes: fp16 d, 32 signed bytes, value q d).
 // ---------------------------------------------------------------------------------------
 constexpr int kMvWarps = 4;
 constexpr int kMvRowsPerWarp = 8;
-constexpr int kMvSegBlocks = 64;   // K segment: 64 blocks = 2048 values = 1152 bytes
+constexpr int kMvSegBlocks = 64;   // K segment: 64 blocks = 2048 values
+constexpr int kQ4_0 = 0, kQ8_0 = 1;
+__host__ __device__ constexpr int block_bytes(int bt) { return bt == kQ8_0 ? 34 : 18; }
 
 struct MvParams {
   const float *x;           // x [n_tokens, K]; the SwiGLU form: gate [n_rows, K]
@@ -218,9 +222,10 @@ __device__ __forceinline__ float4 mv_input4(const float *xr, const float *ur, in
   }
 }
 
-template <bool SWIGLU>
-__global__ void __launch_bounds__(kMvWarps * 32) q4_0_mv_kernel(const __grid_constant__ MvParams p) {
-  __shared__ __align__(16) uint8_t wrow[kMvWarps][kMvSegBlocks * 18];
+template <bool SWIGLU, int BT>
+__global__ void __launch_bounds__(kMvWarps * 32) routed_mv_kernel(const __grid_constant__ MvParams p) {
+  constexpr int kBB = block_bytes(BT);
+  __shared__ __align__(16) uint8_t wrow[kMvWarps][kMvSegBlocks * kBB];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int n_visit = p.n_order ? (int)*p.n_order : p.n_rows;
   for (int i = blockIdx.y; i < n_visit; i += gridDim.y) {
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(kMvWarps * 32) q4_0_mv_kernel(const __grid_con
   const uint8_t *wexp = p.w + (size_t)e * p.expert_stride;
   const float *xr = p.x + (SWIGLU ? (size_t)r : (size_t)tok) * p.K;
   const float *ur = SWIGLU ? p.up + (size_t)r * p.K : nullptr;
-  const size_t row_bytes = (size_t)nblk * 18;
+  const size_t row_bytes = (size_t)nblk * kBB;
   float acc[kMvRowsPerWarp];
 #pragma unroll
   for (int j = 0; j < kMvRowsPerWarp; ++j) acc[j] = 0.f;
@@ -260,11 +265,11 @@ __global__ void __launch_bounds__(kMvWarps * 32) q4_0_mv_kernel(const __grid_con
         for (int v = 0; v < 32; ++v) xv[h][v] = 0.f;
       }
     }
-    const int seg_bytes = seg_blocks * 18;
+    const int seg_bytes = seg_blocks * kBB;
     for (int j = 0; j < kMvRowsPerWarp; ++j) {
       const int n = n_base + j;
       if (n >= p.N) break;
-      const uint8_t *src = wexp + (size_t)n * row_bytes + (size_t)sb * 18;
+      const uint8_t *src = wexp + (size_t)n * row_bytes + (size_t)sb * kBB;
       __syncwarp();
       if ((reinterpret_cast<uintptr_t>(src) & 15) == 0 && (seg_bytes & 15) == 0) {
         for (int o = lane * 16; o < seg_bytes; o += 32 * 16)
@@ -278,18 +283,27 @@ __global__ void __launch_bounds__(kMvWarps * 32) q4_0_mv_kernel(const __grid_con
       for (int h = 0; h < 2; ++h) {
         const int bl = lane + 32 * h;
         if (bl < seg_blocks) {
-          const uint16_t *blk = reinterpret_cast<const uint16_t *>(&wrow[warp][bl * 18]);
+          const uint16_t *blk = reinterpret_cast<const uint16_t *>(&wrow[warp][bl * kBB]);
           const float d = f16_bits_to_float(blk[0]);
           float s = 0.f;
+          if constexpr (BT == kQ8_0) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t two = blk[1 + q];   // qs bytes 2q, 2q+1
+            for (int q = 0; q < 16; ++q) {
+              const uint32_t two = blk[1 + q];   // qs bytes 2q, 2q+1: elements 2q, 2q+1
+              s = __fmaf_rn(xv[h][2 * q], static_cast<float>(static_cast<int8_t>(two & 0xFFu)), s);
+              s = __fmaf_rn(xv[h][2 * q + 1], static_cast<float>(static_cast<int8_t>(two >> 8)), s);
+            }
+          } else {
 #pragma unroll
-            for (int bb = 0; bb < 2; ++bb) {
-              const uint32_t byte = (two >> (8 * bb)) & 0xFFu;
-              const int jj = 2 * q + bb;
-              s = __fmaf_rn(xv[h][jj], static_cast<float>((int)(byte & 15u) - 8), s);
-              s = __fmaf_rn(xv[h][16 + jj], static_cast<float>((int)(byte >> 4) - 8), s);
+            for (int q = 0; q < 8; ++q) {
+              const uint32_t two = blk[1 + q];   // qs bytes 2q, 2q+1
+#pragma unroll
+              for (int bb = 0; bb < 2; ++bb) {
+                const uint32_t byte = (two >> (8 * bb)) & 0xFFu;
+                const int jj = 2 * q + bb;
+                s = __fmaf_rn(xv[h][jj], static_cast<float>((int)(byte & 15u) - 8), s);
+                s = __fmaf_rn(xv[h][16 + jj], static_cast<float>((int)(byte >> 4) - 8), s);
+              }
             }
           }
           part = __fmaf_rn(d, s, part);
@@ -711,7 +725,7 @@ cudaError_t plan_mv_any(const MvParams &p, MvSpec *sp) {
                  : plan_mv_mma_typed<SWIGLU, 8>(p, ks, maxc, smem, sp);
   }
   const int rows_cta = kMvWarps * kMvRowsPerWarp;
-  sp->fn = reinterpret_cast<const void *>(q4_0_mv_kernel<SWIGLU>);
+  sp->fn = reinterpret_cast<const void *>(routed_mv_kernel<SWIGLU, kQ4_0>);
   sp->grid = dim3((unsigned)((p.N + rows_cta - 1) / rows_cta), (unsigned)(p.n_rows < 65535 ? p.n_rows : 65535), 1);
   sp->block = dim3(kMvWarps * 32);
   sp->smem = 0;
@@ -779,8 +793,43 @@ cudaError_t launch_q4_0_mm(const float *x, const uint8_t *w, const uint32_t *ids
   p.expert_stride = expert_stride;
   const int rows_cta = kMvWarps * kMvRowsPerWarp;
   dim3 grid((unsigned)((N + rows_cta - 1) / rows_cta), (unsigned)(n_rows < 65535 ? n_rows : 65535), 1);
-  q4_0_mv_kernel<false><<<grid, kMvWarps * 32, 0, s>>>(p);
+  routed_mv_kernel<false, kQ4_0><<<grid, kMvWarps * 32, 0, s>>>(p);
   return cudaGetLastError();
+}
+
+// GGML Q8_0 routed matmul (the type is among the routed kernels of quantized_matmul_id_ggml.rs):
+// mat-vec visits routed rows in order; mat-mat routes first (per-expert lists in the
+// workspace) and visits the rows expert by expert, so that the CTAs running at one time
+// share an expert's weights through L2.  Both run the fp32 FMA kernel.
+cudaError_t launch_q8_0_matmul_id(const float *x, const uint8_t *w, const uint32_t *ids, float *out,
+                                  int n_tokens, int top_k, int N, int K, int n_experts, uint64_t expert_stride,
+                                  bool mm, void *workspace, cudaStream_t s) {
+  const int n_rows = n_tokens * top_k;
+  MvParams p{};
+  p.x = x; p.up = nullptr; p.w = w; p.ids = ids; p.order = nullptr; p.n_order = nullptr; p.out = out;
+  p.n_rows = n_rows; p.top_k = top_k; p.N = N; p.K = K; p.E = n_experts;
+  p.expert_stride = expert_stride;
+  if (mm) {
+    const MoeWorkspace L = moe_workspace_layout(n_rows, 0, n_experts);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint32_t *offs = reinterpret_cast<uint32_t *>(ws + L.offs);
+    int32_t *hids = reinterpret_cast<int32_t *>(ws + L.hids);
+    cudaError_t e = launch_route_internal(ids, n_rows, n_experts, reinterpret_cast<uint32_t *>(ws + L.htpe), offs,
+                                          hids, reinterpret_cast<uint32_t *>(ws + L.invalid), s,
+                                          reinterpret_cast<int4 *>(ws + L.blk),
+                                          reinterpret_cast<uint32_t *>(ws + L.n_blk), out, N);
+    if (e != cudaSuccess) return e;
+    p.order = hids;
+    p.n_order = offs + n_experts;
+  }
+  const int rows_cta = kMvWarps * kMvRowsPerWarp;
+  dim3 grid((unsigned)((N + rows_cta - 1) / rows_cta), (unsigned)(n_rows < 65535 ? n_rows : 65535), 1);
+  routed_mv_kernel<false, kQ8_0><<<grid, kMvWarps * 32, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+size_t q8_0_mm_workspace_bytes(int64_t n_tokens, int64_t top_k, int64_t n_experts) {
+  return moe_workspace_layout(n_tokens * top_k, 0, n_experts).total;
 }
 
 // Dispatch records for the routed mat-vec (quantized_matmul_id_ggml.rs pre-bakes its decode

@@ -264,6 +264,11 @@ cudaError_t launch_q4_0_mm(const float *x, const uint8_t *w, const uint32_t *ids
 // planned for a large shape must still launch after a smaller shape was planned or called.
 cudaError_t ensure_dynamic_smem(const void *fn, int bytes);
 
+cudaError_t launch_q8_0_matmul_id(const float *x, const uint8_t *w, const uint32_t *ids, float *out,
+                                  int n_tokens, int top_k, int N, int K, int n_experts, uint64_t expert_stride,
+                                  bool mm, void *workspace, cudaStream_t s);
+size_t q8_0_mm_workspace_bytes(int64_t n_tokens, int64_t top_k, int64_t n_experts);
+
 // Routed-row count check: n_tokens and top_k are each bounded before their product is
 // formed, so a huge top_k cannot overflow int64 and wrap past the 2^24 limit.
 inline bool routed_rows_ok(int64_t n_tokens, int64_t top_k) {
