@@ -323,14 +323,39 @@ def run_ours(args, rank, world, local_rank):
         "decode_shapes": shape_rows,
     }
     t_h, by_h = headline
-    out["roofline"] = {"bound": "hbm", "kernel": "gemv_ks_kernel (q4_gemv_ex, static weights)",
-                       "shape": {"M": HEADLINE[0], "K": HEADLINE[1], "N": HEADLINE[2]},
-                       "achieved": round(by_h / t_h / 1e9, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                       "frac": round(by_h / t_h / 1e9 / pk["hbm_gbs"], 3),
-                       "frac_vs_8TBs": round(by_h / t_h / 8e12, 3),
-                       "peak_source": pk["source"] + " (hbm_gbs, burst copy)",
-                       "traffic": profiled_traffic("gemv_ks_kernel_q4_gemv_M1_K4096_N14336.md"),
-                       "algorithmic_bytes_per_launch": by_h}
+    # The decode kernel of each shape: the K-split group-column kernel at M <= 2, the TMA-fed
+    # warp-specialised kernel at 3 <= M <= 16 (every bench shape has K % 256 == 0).
+    def kernel_of(M):
+        return "gemv_ks_kernel" if M <= 2 else "gemv_tma_kernel"
+    by_kernel = {}
+    for r in shape_rows:
+        k = kernel_of(r["M"])
+        r["kernel"] = k
+        tb = by_kernel.setdefault(k, [0.0, 0, 0])
+        tb[0] += r["us"] * 1e-6
+        tb[1] += int4_bytes(r["M"], r["K"], r["N"])
+        tb[2] += 1
+    dom = max(by_kernel, key=lambda k: by_kernel[k][0])
+    t_d, by_d, n_d = by_kernel[dom]
+    share = t_d / sum(v[0] for v in by_kernel.values())
+    out["roofline"] = {
+        "bound": "hbm", "kernel": f"{dom} (q4_gemv_ex, static weights): the step's dominant kernel, "
+                                  f"{n_d} of 9 launches, {share:.0%} of the summed per-shape time",
+        "achieved": round(by_d / t_d / 1e9, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+        "frac": round(by_d / t_d / 1e9 / pk["hbm_gbs"], 3),
+        "frac_vs_8TBs": round(by_d / t_d / 8e12, 3),
+        "peak_source": pk["source"] + " (hbm_gbs, burst copy)",
+        "traffic": profiled_traffic(f"{dom}_q4_gemv_M16_K14336_N4096.md"),
+        "traffic_note": "ncu DRAM bytes (read + write) of one launch of the M=16, K=14336, N=4096 shape, "
+                        "whose algorithmic bytes are 37224448",
+        "algorithmic_bytes_per_launch": round(by_d / n_d),
+        "step_frac": round(value / pk["hbm_gbs"], 3),
+        "headline_shape": {"M": HEADLINE[0], "K": HEADLINE[1], "N": HEADLINE[2], "kernel": kernel_of(HEADLINE[0]),
+                           "achieved": round(by_h / t_h / 1e9, 1), "frac": round(by_h / t_h / 1e9 / pk["hbm_gbs"], 3),
+                           "traffic": profiled_traffic("gemv_ks_kernel_q4_gemv_M1_K4096_N14336.md"),
+                           "algorithmic_bytes_per_launch": by_h},
+        # per decode shape: [M, K, N, us, GB/s, fraction of the measured HBM peak]
+        "shapes": [[r["M"], r["K"], r["N"], r["us"], r["GB_s"], r["frac_hbm"]] for r in shape_rows]}
 
     # ---------------- e2e through the public API with host buffers ----------------
     out["e2e"] = e2e_decode(args, q, synth, rings, dev)
@@ -345,8 +370,27 @@ def run_ours(args, rank, world, local_rank):
         except Exception as e:   # an auxiliary section never costs the headline line
             out["dequant"] = {"error": f"{type(e).__name__}: {e}"[:300]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+        gpu_ms = {"0": small_case_ms(q, synth, to_dev, time_graph, dev), "1": elapsed / args.steps * 1e3}
+        if not args.quick:
+            gpu_ms["2"] = sum(r["us"] for r in out["prefill"]["shapes"]) / 1e3
+            gpu_ms["3"] = sum(r["us"] for r in out["lut4"]["shapes"]) / 1e3
+            gpu_ms["4"] = sum(r["us"] for r in out["moe"]["shapes"]) / 1e3
+        out["cpu_baseline"] = cpu_baseline(gpu_ms, with_configs=not args.quick)
+    # last, so that a tail of the printed line keeps it: per decode shape [M, K, N, us, frac]
+    out["decode_summary"] = [[r["M"], r["K"], r["N"], r["us"], r["frac_hbm"]] for r in shape_rows]
     return out
+
+
+def small_case_ms(q, synth, to_dev, time_graph, dev):
+    """GPU ms per call of the small INT4 case (M=16, K=512, N=256) through q4_gemv."""
+    import torch
+    M, K, N = 16, 512, 256
+    w, s, b = synth.int4_weights(1000, N, K)
+    W = (to_dev(w), to_dev(s), to_dev(b))
+    x = to_dev(synth.activations_bf16(1001, M, K))
+    y = torch.empty((M, N), dtype=torch.int16, device=dev)
+    L = 50
+    return time_graph(lambda _: [q.q4_gemv(x, *W, y) for _ in range(L)], L, replays=5) / L * 1e3
 
 
 def e2e_decode(args, q, synth, rings, dev):
@@ -569,23 +613,29 @@ def bench_moe(args, q, synth, to_dev, ring_of, time_graph, dev, pk):
 # ------------------------------------------------------------------------------------------
 # CPU oracle timing (the cpu_baseline leg and the reference arm)
 # ------------------------------------------------------------------------------------------
-def _oracle_sample_rows(seconds: float):
-    """Rows of every decode shape to run so that one pass takes about `seconds`."""
-    import oracle
-    from weight_only_bit_int4_gb300 import synth
-    K, N = 4096, 64
-    w, s, b = synth.int4_weights(1000, N, K)
-    x = synth.activations_bf16(1100, 16, K)
+def _host_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def _split_run(fn, n: int, threads: int) -> float:
+    """fn(i0, i1) over [0, n) in `threads` contiguous slices on a thread pool (the oracle's C
+    calls release the GIL, so the slices run in parallel).  Returns wall seconds."""
+    from concurrent.futures import ThreadPoolExecutor
+    threads = max(1, min(threads, n))
+    step = -(-n // threads)
     t0 = time.perf_counter()
-    oracle.q4_matmul(x, w, s, b, 16, N, K)
-    per_mac = (time.perf_counter() - t0) / (16 * N * K)
-    macs_per_row = sum(M * K for (M, K, N) in decode_shapes())
-    return max(8, int(seconds / (per_mac * macs_per_row)))
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(lambda i: fn(i * step, min(n, (i + 1) * step)), range(threads)))
+    return time.perf_counter() - t0
 
 
-def oracle_pass(n_rows: int, cache: dict):
-    """One pass of the decode workload on the oracle, restricted to the first n_rows weight
-    rows of every shape.  Returns (seconds, algorithmic bytes of the sampled work)."""
+def decode_oracle_pass(n_rows: int, cache: dict, threads: int):
+    """The decode workload (all 9 shapes, all M tokens, full K) on the oracle, restricted to
+    the first n_rows weight rows of every shape (n_rows >= N: the full shapes), split over
+    weight rows on `threads` threads.  Returns (seconds, algorithmic bytes of that work)."""
     import oracle
     from weight_only_bit_int4_gb300 import synth
     t = 0.0
@@ -595,48 +645,143 @@ def oracle_pass(n_rows: int, cache: dict):
         if key not in cache:
             i = DECODE_KN.index((K, N))
             w, s, b = synth.int4_weights(1000 + i, N, K)
-            rows = min(n_rows, N)
-            cache[key] = (synth.activations_bf16(1100 + j, M, K), w[:rows].copy(), s[:rows].copy(),
-                          b[:rows].copy(), rows)
-        x, w, s, b, rows = cache[key]
-        t0 = time.perf_counter()
-        oracle.q4_matmul(x, w, s, b, M, rows, K)
-        t += time.perf_counter() - t0
+            cache[key] = (synth.activations_bf16(1100 + j, M, K), w, s, b)
+        x, w, s, b = cache[key]
+        rows = min(n_rows, N)
+        t += _split_run(lambda r0, r1: oracle.q4_matmul(x, w[r0:r1], s[r0:r1], b[r0:r1], M, r1 - r0, K),
+                        rows, threads)
         by += int4_bytes(M, K, rows)
     return t, by
 
 
-def cpu_baseline(seconds: float = 15.0):
-    n_rows = _oracle_sample_rows(seconds)
-    t, by = oracle_pass(n_rows, {})
-    return {"value": round(by / t / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"decode workload, first {n_rows} weight rows of each of the 9 shapes "
-                      f"(all M tokens, full K), one pass, {t:.1f} s"}
+def oracle_configs(threads: int, gpu_ms: dict):
+    """The oracle on every configuration of the workload list, on `threads` host threads:
+    0, 1, 3 and 4 in full, 2 (prefill, up to 1.5 T multiply-adds) on 8 sampled token rows
+    per weight shape, scaled to the full token count.  Each is also timed on one thread over a
+    1/threads share of its work and scaled up (the one-core figure).  Returns per config the
+    oracle time per call (all threads and one core), the GPU time per call of the same work
+    (from this bench run) and their ratio."""
+    import oracle
+    from weight_only_bit_int4_gb300 import synth
+    out = {}
+
+    def entry(cfg, what, t_all, t_one, scale=1.0):
+        e = {"what": what, "oracle_ms": round(t_all * scale * 1e3, 2),
+             "oracle_ms_1core": round(t_one * scale * 1e3, 2)}
+        g = gpu_ms.get(cfg)
+        if g:
+            e["gpu_ms"] = round(g, 5)
+            e["gpu_speedup_vs_oracle"] = round(t_all * scale * 1e3 / g, 1)
+        out[cfg] = e
+
+    # 0: INT4 M=16 K=512 N=256
+    M, K, N = 16, 512, 256
+    w, s, b = synth.int4_weights(1000, N, K)
+    x = synth.activations_bf16(1001, M, K)
+    f = lambda r0, r1: oracle.q4_matmul(x, w[r0:r1], s[r0:r1], b[r0:r1], M, r1 - r0, K)
+    entry("0", "INT4 M=16 K=512 N=256", _split_run(f, N, threads), _split_run(f, -(-N // threads), 1) * threads)
+    # 1: decode, nine shapes
+    cache = {}
+    t_all, _ = decode_oracle_pass(1 << 30, cache, threads)
+    t_one = 0.0
+    for (M, K, N) in decode_shapes():
+        x, w, s, b = cache[(M, K, N)]
+        share = -(-N // threads)
+        t_one += _split_run(lambda r0, r1: oracle.q4_matmul(x, w[r0:r1], s[r0:r1], b[r0:r1], M, r1 - r0, K),
+                            share, 1) * (N / share)
+    entry("1", "INT4 decode, 9 shapes (one step)", t_all, t_one)
+    # 2: prefill, 9 shapes, 8 token rows sampled per weight shape, scaled to the full M
+    t_all = t_one = 0.0
+    for i, (K, N) in enumerate(PREFILL_KN):
+        w, s, b = synth.int4_weights(2000 + i, N, K)
+        x = synth.activations_bf16(2100 + i, 8, K, outlier_frac=0.01)
+        f = lambda r0, r1: oracle.q4_matmul(x, w[r0:r1], s[r0:r1], b[r0:r1], 8, r1 - r0, K)
+        share = -(-N // threads)
+        ta, to = _split_run(f, N, threads), _split_run(f, share, 1) * (N / share)
+        tot_m = sum(PREFILL_M)
+        t_all += ta * tot_m / 8
+        t_one += to * tot_m / 8
+    entry("2", "INT4 prefill, 9 shapes (sampled: 8 token rows per weight shape)", t_all, t_one)
+    # 3: LUT4 M in {1, 512}, K = N = 4096, block 64
+    Kl = Nl = 4096
+    packed, sc, book = synth.lut4_weights(3000, Nl, Kl, 64)
+    t_all = t_one = 0.0
+    for Ml in (1, 512):
+        xl = synth.activations_bf16(3100 + Ml, Ml, Kl)
+        if Ml == 1:   # split over weight rows (the packed rows of [N, K/2] are contiguous)
+            f = lambda r0, r1: oracle.lut4_matmul(xl, packed[r0 * Kl // 2:r1 * Kl // 2],
+                                                  sc[r0 * Kl // 64:r1 * Kl // 64], book, 1, r1 - r0, Kl, 64, 1)
+            n = Nl
+        else:         # split over tokens
+            f = lambda r0, r1: oracle.lut4_matmul(xl[r0:r1], packed, sc, book, r1 - r0, Nl, Kl, 64, 1)
+            n = Ml
+        share = -(-n // threads)
+        t_all += _split_run(f, n, threads)
+        t_one += _split_run(f, share, 1) * (n / share)
+    entry("3", "LUT4 M in {1, 512}, K = N = 4096", t_all, t_one)
+    # 4: Q4_0 MoE, 64 experts, top 8, K = 2048, N = 1408, n_tokens in {1, 512}
+    E, top_k, Nm, Km = 64, 8, 1408, 2048
+    wq, stride = synth.q4_0_experts(4000, E, Nm, Km)
+    t_all = t_one = 0.0
+    for nt in (1, 512):
+        ids = synth.routing_ids(4100 + nt, nt, top_k, E)
+        xm = synth.activations_f32(4200 + nt, nt, Km)
+        if nt == 1:   # split over routed rows
+            f = lambda r0, r1: oracle.q4_0_matmul_id_rows(xm, wq, ids, top_k, Nm, Km, E, stride,
+                                                          np.arange(r0, r1))
+            n = top_k
+        else:         # split over tokens
+            f = lambda r0, r1: oracle.q4_0_matmul_id(xm[r0:r1], wq, ids[r0 * top_k:r1 * top_k], r1 - r0, top_k,
+                                                     Nm, Km, E, stride)
+            n = nt
+        share = -(-n // threads)
+        t_all += _split_run(f, n, threads)
+        t_one += _split_run(f, share, 1) * (n / share)
+    entry("4", "Q4_0 MoE, 64 experts top 8, n_tokens in {1, 512}", t_all, t_one)
+    return out
+
+
+def cpu_baseline(gpu_ms: dict, with_configs: bool = True):
+    """The oracle on the GPU machine's host cores: `value` is the full decode workload (one step
+    of the nine shapes) in the metric's unit on every host thread; `configs` gives every
+    configuration's oracle time per call and the GPU's speed-up over it."""
+    threads = _host_threads()
+    t, by = decode_oracle_pass(1 << 30, {}, threads)
+    res = {"value": round(by / t / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+           "sample": f"decode workload, all 9 shapes in full (one step), split over weight rows on "
+                     f"{threads} threads, {t:.1f} s"}
+    if with_configs:
+        res["configs"] = oracle_configs(threads, gpu_ms)
+    return res
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    n_rows = _oracle_sample_rows(args.reference_seconds / max(1, args.steps + args.warmup))
+    threads = _host_threads()
+    # rows per shape so that the whole run spends about --reference-seconds
     cache = {}
+    t1, by1 = decode_oracle_pass(64, cache, threads)
+    per_row = t1 / 64
+    n_rows = max(16, int(args.reference_seconds / max(1, args.steps + args.warmup) / per_row))
     for _ in range(args.warmup):
-        oracle_pass(n_rows, cache)
+        decode_oracle_pass(n_rows, cache, threads)
     t_tot, by_tot = 0.0, 0
     for _ in range(args.steps):
-        t, by = oracle_pass(n_rows, cache)
+        t, by = decode_oracle_pass(n_rows, cache, threads)
         t_tot += t
         by_tot += by
     value = by_tot / t_tot / 1e9
-    sample = (f"decode workload, first {n_rows} weight rows of each of the 9 shapes per step "
-              f"(all M tokens, full K)")
+    sample = (f"decode workload, first {min(n_rows, 14336)} weight rows of each of the 9 shapes per step "
+              f"(all M tokens, full K), {threads} threads")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(t_tot / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "INT4 g32 affine decode GEMV, M in {1,4,16} x (K,N) in "
                                    "{(4096,14336),(14336,4096),(4096,4096)} (bounded row sample)",
-                       "parallelism": "cpu oracle, 1 thread"},
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                       "parallelism": f"cpu oracle, {threads} threads"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
@@ -726,7 +871,6 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=120.0,
                     help="--impl reference: oracle seconds for the whole warmup + steps run")
     ap.add_argument("--case", choices=sorted(CASES), help="run one small named workload (profiling)")

@@ -73,6 +73,15 @@ int q4mm_version(void);
  * resets it.  Synchronises the device (diagnostics only, not for hot loops). */
 q4mm_status q4mm_device_errors(uint32_t *out_flags, int clear);
 
+/* Self-test of the bounded waits (diagnostics; the source pages have no counterpart).  Runs
+ * one small kernel whose wait on a pipeline barrier that nothing completes gives up after
+ * limit_ns nanoseconds (1 .. 10^9), exactly as every pipeline wait of the library gives up
+ * after its 2 s limit: it sets Q4MM_DEVERR_WAIT_TIMEOUT, the other waiting warp leaves on the
+ * CTA's abort flag, and a bulk copy the kernel started lands before the kernel exits.  src16:
+ * device pointer to 16 readable, 16-byte aligned bytes (the copy's source).  Nothing faults
+ * or traps; the next calls run normally.  Read the bit with q4mm_device_errors. */
+q4mm_status q4mm_selftest_wait_timeout(const void *src16, uint32_t limit_ns, q4mm_stream_t stream);
+
 /* ======================================================================================
  * INT4 group-32 affine MatMulNBits  (quant_fastkernel.rs)
  *   w       uint32 [N, K/8]: element k of row n is bits 4*(k%8)..4*(k%8)+3 of word

@@ -57,8 +57,11 @@ MUTATIONS = {
         "v = oracle_f16_to_f32(oracle_f32_to_f16(v));",
         "v = v;"),
     "q4_0 d read big endian": (
-        "oracle_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));",
-        "oracle_f16_to_f32((uint16_t)(blk[1] | (blk[0] << 8)));"),
+        "oracle_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));\n    int64_t j = k % 32;",
+        "oracle_f16_to_f32((uint16_t)(blk[1] | (blk[0] << 8)));\n    int64_t j = k % 32;"),
+    "q8_0 d read big endian": (
+        "oracle_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));\n    int q = (int)blk[2 + k % 32];",
+        "oracle_f16_to_f32((uint16_t)(blk[1] | (blk[0] << 8)));\n    int q = (int)blk[2 + k % 32];"),
     "silu is the bare sigmoid": (
         "return z / (1.0 + exp(-z));",
         "return 1.0 / (1.0 + exp(-z));"),

@@ -16,6 +16,7 @@ SIGNATURES = {
     "q4mm_status_string": ([_S], ctypes.c_char_p),
     "q4mm_version": ([], _S),
     "q4mm_device_errors": ([_P, _S], _S),
+    "q4mm_selftest_wait_timeout": ([_P, ctypes.c_uint32, _P], _S),
     "q4_dequant": ([_P, _P, _P, _I, _I, _P, _S, _P], _S),
     "q4_gemv": ([_P, _P, _P, _P, _P, _I, _I, _I, _P], _S),
     "q4_gemv_ex": ([_P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_uint32, _P], _S),

@@ -87,8 +87,18 @@ q4mm_status q4mm_device_errors(uint32_t *out_flags, int clear) {
   if (read_errors_moe(&v, clear) != cudaSuccess) return Q4MM_ERR_CUDA;
   if (read_errors_gemm(&v, clear) != cudaSuccess) return Q4MM_ERR_CUDA;
   if (read_errors_moe_tc(&v, clear) != cudaSuccess) return Q4MM_ERR_CUDA;
+  if (read_errors_gemv(&v, clear) != cudaSuccess) return Q4MM_ERR_CUDA;
+  if (read_errors_selftest(&v, clear) != cudaSuccess) return Q4MM_ERR_CUDA;
   *out_flags = v;
   return Q4MM_OK;
+}
+
+q4mm_status q4mm_selftest_wait_timeout(const void *src16, uint32_t limit_ns, q4mm_stream_t stream) {
+  if (!src16 || limit_ns == 0 || limit_ns > 1000000000u) return Q4MM_ERR_INVALID_ARG;
+  if (!aligned(src16, 16)) return Q4MM_ERR_UNSUPPORTED;
+  q4mm_status st = check_device();
+  if (st != Q4MM_OK) return st;
+  return from_cuda(launch_wait_timeout_selftest(src16, limit_ns, (cudaStream_t)stream));
 }
 
 // ------------------------------------------------------------------------------------------

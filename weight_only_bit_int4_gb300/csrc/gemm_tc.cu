@@ -9,23 +9,35 @@
 // simdgroup 8x8 MMA, a half-precision transposed W tile) is prior art only; this is the
 // GB300 design:
 //
-//  * Weights are the MMA's M side: a tile is 128 weight rows x 256 tokens, its fp32
-//    accumulator (128 lanes x 256 columns) lives in tensor memory.  Two accumulators (all
-//    512 columns) let the epilogue of one tile overlap the main loop of the next.
-//  * Persistent CTAs, one per SM (the 4-stage ring takes ~197 KB of shared memory).
-//  * Warp 0, one lane: TMA loads x tiles [256 tokens x 64 k] (bf16, 128-byte swizzle).
-//  * Warps 2-5 (128 threads, one weight row each): load the raw codes of a 64-wide K block
-//    (two 16-byte loads per row, prefetched three blocks ahead, across tile boundaries),
-//    dequantise in registers (INT4: magic-number bf16 conversion + one bf16x2 FMA per
-//    pair, so each value is code*s+b rounded once; LUT4: codebook lookup in shared
-//    memory, one fp32 product, rounded to bf16), and write the bf16 row into the
-//    128-byte-swizzled K-major tile the MMA reads.
-//  * Warp 1, one lane: issues tcgen05.mma (M=128, N=256, K=16) x4 per K block and commits
-//    each stage back to the producers, and each finished accumulator to the epilogue.
-//  * Warps 6-9: tcgen05.ld 32 columns at a time, round to bf16, store y, release the
+// Two kernels:
+//
+//  qgemm_tma_kernel<LUT, TT, SPLIT> (K % 256 == 0; every prefill shape of the workload):
+//  * Weights are the MMA's M side: a tile is 128 weight rows x TT tokens, TT in {384, 256,
+//    128}, its fp32 accumulator in tensor memory.  TT = 256 / 128 keep two accumulators
+//    (2 TT columns), so the epilogue of one tile overlaps the main loop of the next;
+//    TT = 384 takes one 384-column accumulator (two MMAs per k step, N = 256 + 128), so a
+//    dequantised weight tile serves 1.5 times as many tokens.
+//  * SPLIT = false: persistent CTAs, one per SM, walk the tiles with the weight tile
+//    varying fastest, so the CTAs running at one time share a few x tiles in L2.
+//    SPLIT = true (small M): one (tile, K slice) per CTA, the K slices of a tile form a
+//    cluster and sum their fp32 partials in rank order through distributed shared memory.
+//  * Warp 0, one lane: TMA loads of the x tiles (bf16, 128-byte swizzle), of the code tiles
+//    [128 rows x 32 B] per 64-wide K block and of the scale / bias tiles per 8 K blocks.
+//  * Warps 2-9 (256 threads, two per weight row, 32 k each): dequantise from shared memory
+//    (INT4: magic-number bf16 conversion + one bf16x2 FMA per pair, so each value is
+//    code*s+b rounded once; LUT4: codebook lookup, one fp32 product, rounded to bf16) into
+//    the 128-byte-swizzled K-major bf16 tile the MMA reads.
+//  * Warp 1, one lane: issues tcgen05.mma (M = 128, K = 16) x4 per K block (x8 for
+//    TT = 384) and commits each stage back to the producers and each finished accumulator
+//    to the epilogue.
+//  * Warps 10-13: tcgen05.ld 32 columns at a time, round to bf16, store y, release the
 //    accumulator.
-//  * Every mbarrier wait is bounded (a timeout sets the device error word and unwinds the
-//    CTA; tensor memory is always released).
+//
+//  qgemm_tc_kernel (any K % 32 == 0): the same roles with 256-token tiles, 4 producer warps
+//  that load the codes with plain 16-byte loads instead of TMA, and one CTA per SM.
+//
+//  Every mbarrier wait is bounded (a timeout sets the device error word and unwinds the
+//  CTA; tensor memory is always released).
 #include "tc_common.cuh"
 
 #include <cudaTypedefs.h>

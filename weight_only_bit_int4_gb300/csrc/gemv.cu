@@ -29,6 +29,9 @@
 #include <algorithm>
 
 namespace q4mm {
+
+Q4MM_DEFINE_ERROR_READER(read_errors_gemv)
+
 namespace {
 
 constexpr int kWarps = 4;

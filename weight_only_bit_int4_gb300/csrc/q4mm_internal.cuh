@@ -35,6 +35,9 @@ static __device__ unsigned int g_device_error = 0;
 cudaError_t read_errors_moe(unsigned int *out, int clear);
 cudaError_t read_errors_gemm(unsigned int *out, int clear);
 cudaError_t read_errors_moe_tc(unsigned int *out, int clear);
+cudaError_t read_errors_gemv(unsigned int *out, int clear);
+cudaError_t read_errors_selftest(unsigned int *out, int clear);
+cudaError_t launch_wait_timeout_selftest(const void *src16, unsigned long long limit_ns, cudaStream_t s);
 
 __device__ __forceinline__ void raise_device_error(unsigned int bit) {
   atomicOr(&g_device_error, bit);

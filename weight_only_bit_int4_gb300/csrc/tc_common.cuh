@@ -55,18 +55,20 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t addr, uint32_t pari
 }
 
 // Waits for the phase of parity `parity` to complete.  Gives up (returns false) after
-// kWaitLimitNs, or as soon as another role has given up (*abort != 0); the first thread to
-// time out records Q4MM_DEVERR_WAIT_TIMEOUT and sets *abort so the whole CTA unwinds.
-// The clock and the abort flag are looked at only every 16 polls.
+// limit_ns (kWaitLimitNs unless a self-test asks for less), or as soon as another role has
+// given up (*abort != 0); the first thread to time out records Q4MM_DEVERR_WAIT_TIMEOUT and
+// sets *abort so the whole CTA unwinds.  The clock and the abort flag are looked at only
+// every 16 polls.
 __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, volatile int *abort,
-                                          uint32_t hint_ns = 2000) {
+                                          uint32_t hint_ns = 2000,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(addr, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_sleep(addr, parity, hint_ns)) return true;
     if ((it & 15u) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort = 1;
         raise_device_error(Q4MM_DEVERR_WAIT_TIMEOUT);
         return false;
