@@ -607,7 +607,27 @@ def bench_moe(args, q, synth, to_dev, ring_of, time_graph, dev, pk):
                                                       Nd, Kd, E, stride_d) for l in range(L)], L, replays=5) / L
     swiglu = {"n_tokens": n_tokens, "N": Nd, "K": Kd, "us": round(t * 1e6, 2), "GB_s": round(by / t / 1e9, 1),
               "frac_hbm": round(by / t / 1e9 / pk["hbm_gbs"], 3)}
-    return {"experts": E, "top_k": top_k, "N": N, "K": K, "shapes": rows, "swiglu_down_mv": swiglu}
+    # GGML Q8_0 routed matmul on the same MoE shape (34-byte blocks): mat-vec at one token,
+    # mat-mat (route, then the routed rows expert by expert) at 512 tokens.
+    w8, stride8 = synth.q8_0_experts(4700, E, N, K)
+    ring8 = ring_of((to_dev(w8),), w8.nbytes)
+    q8 = []
+    for n_tokens, mode in ((1, 1), (512, 2)):
+        ids = synth.routing_ids(4100 + n_tokens, n_tokens, top_k, E)
+        x = to_dev(synth.activations_f32(4200 + n_tokens, n_tokens, K))
+        idd = to_dev(ids.view(np.int32))
+        out = torch.empty((n_tokens * top_k, N), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(1, q.q8_0_matmul_id_workspace_size(n_tokens, top_k, N, K, E)), dtype=torch.uint8,
+                         device=dev)
+        by = len(np.unique(ids)) * N * (K // 32) * 34 + x.numel() * 4 + out.numel() * 4 + ids.nbytes
+        L = 2 * len(ring8) if n_tokens == 1 else 2
+        t = time_graph(lambda _: [q.q8_0_matmul_id(x, ring8[l % len(ring8)][0], idd, out, top_k, N, K, E,
+                                                   stride8, mode=mode, workspace=ws)
+                                  for l in range(L)], L, replays=5 if n_tokens == 1 else 2) / L
+        q8.append({"n_tokens": n_tokens, "mode": {1: "mv", 2: "mm"}[mode], "us": round(t * 1e6, 2),
+                   "GB_s": round(by / t / 1e9, 1), "frac_hbm": round(by / t / 1e9 / pk["hbm_gbs"], 3)})
+    return {"experts": E, "top_k": top_k, "N": N, "K": K, "shapes": rows, "swiglu_down_mv": swiglu,
+            "q8_0": q8}
 
 
 # ------------------------------------------------------------------------------------------

@@ -1766,66 +1766,86 @@ cudaError_t make_tq_maps(GemvTmaArgs &a, int R) {
 }
 
 struct TqPlan {
-  int WC = 0, S = 0, maxnh = 0, stages = 0;
+  int WC = 0, KS = 1, S = 0, maxnh = 0, stages = 0;
   size_t smem = 0;
 };
 
-// Plans for gemv_tma_kernel, from a sweep of (warps, K splits, stages) over the decode shapes
-// on GB300.  What the sweep showed: every CTA resident at once, at most two CTAs per SM (the
-// next call's CTAs then find room to start streaming while this call finishes), the work as
-// evenly spread over the SMs as that allows, at least 8 consumer warps per SM, and as many
-// ring stages as the CTA's share of shared memory holds.  Ties go to the fewest K splits
-// (each split adds a cluster reduction), then to 8 consumer warps per CTA for M >= 3 and 4
-// below (measured best in each range).
+// Plans for gemv_tma_kernel, from sweeps of (consumer warps, consumer groups, K splits,
+// stages) over the decode shapes on GB300.  What they showed: every CTA resident at once and
+// at most two CTAs per SM (the next call's CTAs then find room to start streaming while this
+// call finishes); the decode arithmetic, not the stream, bounds the kernel, so more consumer
+// warps per SM help: 12 consumer warps in two groups over 96-row tiles (6 x 2) win wherever
+// their one-CTA-per-SM grid covers nearly every SM (N = 14336: 150 CTAs); otherwise 8
+// consumer warps in one group with the K split that spreads the CTAs best.  Each CTA takes
+// as many ring stages as its share of shared memory holds.
+TqPlan tq_plan_for(int M, int N, int K, int WC, int KS, int S, int sms, int max_need) {
+  TqPlan pl;
+  const int NH = K / 256, NB = (NH + 1) / 2;
+  if (S > NB) return pl;
+  const int R = 16 * WC, threads = (WC * KS + 1) * 32, regs = 112;   // regs: >= what ptxas -v reports
+  int maxnh = 0;
+  for (int sp = 0; sp < S; ++sp) {
+    const int b0 = (sp * NB) / S, b1 = ((sp + 1) * NB) / S;
+    maxnh = std::max(maxnh, std::min(2 * b1, NH) - 2 * b0);
+  }
+  const long long ctas = (long long)((N + R - 1) / R) * S;
+  const int need = (int)((ctas + sms - 1) / sms);   // CTAs on the busiest SM
+  if (need > max_need || need * threads * regs > 65536) return pl;
+  // Ring stages.  One consumer group: as many as the CTA's share of shared memory holds
+  // (up to 8; measured best).  Two groups (512-k stages): only what fits in half of the SM,
+  // at least 2; measured best, since the rest lets the next call's CTAs start early.
+  const size_t budget = (size_t)(227 * 1024) / need;
+  const size_t fixed = tq_smem_bytes(M, maxnh, R, KS, 0);
+  if (fixed >= budget) return pl;
+  const size_t per = tq_stage_bytes(R, KS) + 16;
+  int stages = (int)std::min<size_t>(8, (budget - fixed) / per);
+  if (KS > 1) {
+    const size_t half_sm = (size_t)(113 * 1024) / need;
+    const int s_half = fixed < half_sm ? (int)((half_sm - fixed) / per) : 0;
+    stages = std::min(stages, std::max(s_half, 2));
+  }
+  if (stages < 2 || stages * KS < 3) return pl;
+  pl.WC = WC; pl.KS = KS; pl.S = S; pl.maxnh = maxnh; pl.stages = stages;
+  pl.smem = tq_smem_bytes(M, maxnh, R, KS, stages);
+  return pl;
+}
+
 TqPlan make_tq_plan(int M, int N, int K) {
-  TqPlan best;
   int sms = 152, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) {
     int v = 0;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
   }
-  const int NH = K / 256, NB = (NH + 1) / 2;
-  const int regs = 112;   // per thread, at least what ptxas -v reports for these kernels
-  const int wc_pref = M >= 3 ? 8 : 4;
+  // 12 consumer warps (6 rows groups x 2 consumer groups), one CTA per SM, no K split.
+  const TqPlan wide = tq_plan_for(M, N, K, 6, 2, 1, sms, 1);
+  if (wide.WC > 0 && (double)((N + 95) / 96) / sms >= 0.95) return wide;
+  TqPlan best;
   double best_score = -1e30;
-  for (int WC : {wc_pref, 12 - wc_pref}) {
-    const int R = 16 * WC, threads = (WC + 1) * 32;
+  for (int WC : {8, 4})
     for (int S : {1, 2, 4, 8}) {
-      if (S > NB) break;
-      int maxnh = 0;
-      for (int sp = 0; sp < S; ++sp) {
-        const int b0 = (sp * NB) / S, b1 = ((sp + 1) * NB) / S;
-        maxnh = std::max(maxnh, std::min(2 * b1, NH) - 2 * b0);
-      }
-      const long long ctas = (long long)((N + R - 1) / R) * S;
-      const int need = (int)((ctas + sms - 1) / sms);   // CTAs on the busiest SM
-      if (need > 2 || need * threads * regs > 65536) continue;
-      const size_t budget = (size_t)(227 * 1024) / need;
-      const size_t fixed = tq_smem_bytes(M, maxnh, R, 0);
-      if (fixed >= budget) continue;
-      const int stages = (int)std::min<size_t>(8, (budget - fixed) / (tq_stage_bytes(R) + 16));
-      if (stages < 3) continue;
+      const TqPlan pl = tq_plan_for(M, N, K, WC, 1, S, sms, 2);
+      if (pl.WC == 0) continue;
+      const long long ctas = (long long)((N + 16 * WC - 1) / (16 * WC)) * S;
+      const int need = (int)((ctas + sms - 1) / sms);
       const double balance = (double)ctas / (double)((long long)need * sms);
       const double score = balance * std::min(1.0, need * WC / 8.0) - 1e-3 * S;
       if (score > best_score + 1e-9) {
         best_score = score;
-        best.WC = WC; best.S = S; best.maxnh = maxnh; best.stages = stages;
-        best.smem = tq_smem_bytes(M, maxnh, R, stages);
+        best = pl;
       }
     }
-  }
   return best;
 }
 
-template <int NT, int WC>
+template <int NT, int WC, int KS>
 cudaError_t launch_tq_typed(GemvParams &p, const TqPlan &pl, cudaStream_t s, bool overlap, LaunchSpec *rec) {
-  auto kern = gemv_tma_kernel<NT, WC>;
+  auto kern = gemv_tma_kernel<NT, WC, KS>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), (int)pl.smem);
   if (e != cudaSuccess) return e;
   p.max_chunks_per_cta = pl.maxnh;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((p.N + 16 * WC - 1) / (16 * WC)), (unsigned)pl.S, 1);
-  cfg.blockDim = dim3((WC + 1) * 32, 1, 1);
+  cfg.blockDim = dim3((WC * KS + 1) * 32, 1, 1);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -1864,8 +1884,13 @@ cudaError_t launch_tq_typed(GemvParams &p, const TqPlan &pl, cudaStream_t s, boo
 
 template <int NT>
 cudaError_t launch_tq_w(GemvParams &p, const TqPlan &pl, cudaStream_t s, bool overlap, LaunchSpec *rec) {
-  if (pl.WC == 4) return launch_tq_typed<NT, 4>(p, pl, s, overlap, rec);
-  return launch_tq_typed<NT, 8>(p, pl, s, overlap, rec);
+  if (pl.KS == 2) {
+    if (pl.WC == 4) return launch_tq_typed<NT, 4, 2>(p, pl, s, overlap, rec);
+    if (pl.WC == 6) return launch_tq_typed<NT, 6, 2>(p, pl, s, overlap, rec);
+    return launch_tq_typed<NT, 8, 2>(p, pl, s, overlap, rec);
+  }
+  if (pl.WC == 4) return launch_tq_typed<NT, 4, 1>(p, pl, s, overlap, rec);
+  return launch_tq_typed<NT, 8, 1>(p, pl, s, overlap, rec);
 }
 
 #ifdef Q4MM_TUNING
@@ -1891,6 +1916,7 @@ cudaError_t launch_any(GemvParams &p, cudaStream_t s, bool overlap, LaunchSpec *
 #ifdef Q4MM_TUNING
     if (getenv("Q4MM_TQ_W") || getenv("Q4MM_TQ_S") || getenv("Q4MM_TQ_ST")) {
       tp.WC = tuning_env("Q4MM_TQ_W", tp.WC);
+      tp.KS = tuning_env("Q4MM_TQ_KS", tp.KS);
       tp.S = tuning_env("Q4MM_TQ_S", tp.S);
       const int NH = p.K / 256, NB = (NH + 1) / 2;
       tp.maxnh = 0;
@@ -1899,7 +1925,7 @@ cudaError_t launch_any(GemvParams &p, cudaStream_t s, bool overlap, LaunchSpec *
         tp.maxnh = std::max(tp.maxnh, std::min(2 * b1, NH) - 2 * b0);
       }
       tp.stages = tuning_env("Q4MM_TQ_ST", tp.stages);
-      tp.smem = tq_smem_bytes(p.M, tp.maxnh, 16 * tp.WC, tp.stages);
+      tp.smem = tq_smem_bytes(p.M, tp.maxnh, 16 * tp.WC, tp.KS, tp.stages);
     }
 #endif
     if (tp.WC > 0) return p.M <= 8 ? launch_tq_w<1>(p, tp, s, overlap, rec) : launch_tq_w<2>(p, tp, s, overlap, rec);

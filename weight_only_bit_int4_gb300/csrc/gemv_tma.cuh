@@ -58,20 +58,23 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 //         [piece p = 0..3][lane t = 0..3][16 B] = B fragments of k-steps 2p, 2p + 1
 //   xsum  [M][nbmax][t][16 B]: (hi(2t, 2t+1), hi(2t+8, 2t+9), lo(2t, 2t+1), lo(2t+8, 2t+9))
 //         bf16 pairs of the group sums of each 16-group block
-//   red   [M][R] fp32 partial tile for the reduction
+//   red   [KS][M][R] fp32 partial tiles of the consumer groups, summed in group order
 //   full[stages], empty[stages] mbarriers, abort flag
-__host__ __device__ inline uint32_t tq_stage_bytes(int R) { return (uint32_t)R * 160u; }
+// A stage holds KS half-blocks (KS consumer groups split it); each half-block sub-stage is
+// [codes R x 128 B | scales R x 16 B | biases R x 16 B], a multiple of 1024 bytes.
+__host__ __device__ inline uint32_t tq_stage_bytes(int R, int KS) { return (uint32_t)R * 160u * (uint32_t)KS; }
 __host__ __device__ inline int tq_ts(int nh) { return nh * 512 + 64; }
-__host__ __device__ inline size_t tq_smem_bytes(int M, int nh, int R, int stages) {
+__host__ __device__ inline size_t tq_smem_bytes(int M, int nh, int R, int KS, int stages) {
   const int nb = (nh + 1) / 2;
-  return 1024 + (size_t)stages * tq_stage_bytes(R) + (size_t)M * tq_ts(nh) + (size_t)M * nb * 64 +
-         (size_t)M * R * 4 + (size_t)stages * 16 + 16;
+  return 1024 + (size_t)stages * tq_stage_bytes(R, KS) + (size_t)M * tq_ts(nh) + (size_t)M * nb * 64 +
+         (size_t)KS * M * R * 4 + (size_t)stages * 16 + 16;
 }
 
-template <int NT, int WC>
-__global__ void __launch_bounds__((WC + 1) * 32) gemv_tma_kernel(const __grid_constant__ GemvTmaArgs a) {
+template <int NT, int WC, int KS>
+__global__ void __launch_bounds__((WC * KS + 1) * 32) gemv_tma_kernel(const __grid_constant__ GemvTmaArgs a) {
   constexpr int R = 16 * WC;
-  constexpr uint32_t kStage = R * 160u, kCodes = R * 128u;
+  constexpr int NC = WC * KS;                       // consumer warps; warp NC is the producer
+  constexpr uint32_t kSub = R * 160u, kCodes = R * 128u, kStage = kSub * KS;
   const GemvParams &p = a.p;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -93,15 +96,16 @@ __global__ void __launch_bounds__((WC + 1) * 32) gemv_tma_kernel(const __grid_co
   uint8_t *xs = ring + (size_t)ST * kStage;
   uint8_t *xsum = xs + (size_t)p.M * TS;
   float *red = reinterpret_cast<float *>(xsum + (size_t)p.M * nbmax * 64);
-  const uint32_t full0 = smem_u32(red + p.M * R);
+  const uint32_t full0 = smem_u32(red + KS * p.M * R);
   const uint32_t empty0 = full0 + 8u * (uint32_t)ST;
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(red + p.M * R + 4 * ST);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(red + KS * p.M * R + 4 * ST);
   const int row0 = (int)blockIdx.x * R;
+  const int nst = (nh + KS - 1) / KS;        // stages of this slice (the last may hold one half-block)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < ST; ++s) {
       tc::mbar_init(full0 + 8 * s, 1);
-      tc::mbar_init(empty0 + 8 * s, WC);
+      tc::mbar_init(empty0 + 8 * s, NC);
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -109,22 +113,26 @@ __global__ void __launch_bounds__((WC + 1) * 32) gemv_tma_kernel(const __grid_co
   __syncthreads();
   griddep_launch_dependents();   // the next kernel may start streaming its (static) weights
 
-  if (warp == WC) {
-    // ---------------- producer: TMA of codes, scales and biases, one stage per half-block ----------------
+  if (warp == NC) {
+    // ---------------- producer: TMA of codes, scales and biases, KS half-blocks per stage ----------------
     if (lane == 0) {
       tc::tma_prefetch_desc(&a.wmap);
       tc::tma_prefetch_desc(&a.smap);
       tc::tma_prefetch_desc(&a.bmap);
       int issued = 0;
-      for (int lh = 0, s = 0, ph = 0; lh < nh; ++lh) {
-        if (lh >= ST && !tc::mbar_wait(empty0 + 8 * s, (uint32_t)(ph ^ 1), abort_flag)) break;
+      for (int i = 0, s = 0, ph = 0; i < nst; ++i) {
+        if (i >= ST && !tc::mbar_wait(empty0 + 8 * s, (uint32_t)(ph ^ 1), abort_flag)) break;
         const uint32_t dst = smem_u32(ring) + (uint32_t)s * kStage;
         const uint32_t bar = full0 + 8 * s;
-        tc::mbar_arrive_expect_tx(bar, kStage);
-        const int hb = h0 + lh;
-        tc::tma_load_2d(dst, &a.wmap, hb * 128, row0, bar);
-        tc::tma_load_2d(dst + kCodes, &a.smap, hb * 8, row0, bar);
-        tc::tma_load_2d(dst + kCodes + R * 16, &a.bmap, hb * 8, row0, bar);
+        const int nsub = min(KS, nh - i * KS);
+        tc::mbar_arrive_expect_tx(bar, kSub * (uint32_t)nsub);
+        for (int j = 0; j < nsub; ++j) {
+          const int hb = h0 + i * KS + j;
+          const uint32_t d = dst + (uint32_t)j * kSub;
+          tc::tma_load_2d(d, &a.wmap, hb * 128, row0, bar);
+          tc::tma_load_2d(d + kCodes, &a.smap, hb * 8, row0, bar);
+          tc::tma_load_2d(d + kCodes + R * 16, &a.bmap, hb * 8, row0, bar);
+        }
         ++issued;
         if (++s == ST) {
           s = 0;
@@ -132,9 +140,9 @@ __global__ void __launch_bounds__((WC + 1) * 32) gemv_tma_kernel(const __grid_co
         }
       }
       if (*abort_flag) {   // let the loads in flight land before the CTA exits
-        for (int lh = (issued > ST ? issued - ST : 0); lh < issued; ++lh) {
+        for (int i = (issued > ST ? issued - ST : 0); i < issued; ++i) {
           volatile int dummy = 0;
-          tc::mbar_wait(full0 + 8 * (lh % ST), (uint32_t)((lh / ST) & 1), &dummy);
+          tc::mbar_wait(full0 + 8 * (i % ST), (uint32_t)((i / ST) & 1), &dummy);
         }
       }
     }
@@ -149,11 +157,11 @@ __global__ void __launch_bounds__((WC + 1) * 32) gemv_tma_kernel(const __grid_co
       const int ngrp = 16 * nb;   // groups of the slice's blocks (a last half-block may be missing)
       const int items = p.M * ngrp;
       constexpr int kU = 4;
-      for (int it0 = threadIdx.x; it0 < items; it0 += kU * WC * 32) {
+      for (int it0 = threadIdx.x; it0 < items; it0 += kU * NC * 32) {
         uint4 v[kU][4];
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-          const int it = it0 + u * WC * 32;
+          const int it = it0 + u * NC * 32;
           const int tok = it / ngrp, gi = 16 * b0 + it % ngrp;
           if (it < items && gi < 8 * h1) {
             const uint4 *src = reinterpret_cast<const uint4 *>(p.x + (size_t)tok * p.K + (size_t)gi * 32);
@@ -166,7 +174,7 @@ __global__ void __launch_bounds__((WC + 1) * 32) gemv_tma_kernel(const __grid_co
         }
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-          const int it = it0 + u * WC * 32;
+          const int it = it0 + u * NC * 32;
           if (it >= items) break;
           const int tok = it / ngrp, gl = it % ngrp;
           const int gi = 16 * b0 + gl;             // group index in the row
@@ -200,7 +208,7 @@ __global__ void __launch_bounds__((WC + 1) * 32) gemv_tma_kernel(const __grid_co
         }
       }
     }
-    consumer_sync(WC * 32);
+    consumer_sync(NC * 32);
 
     // B-fragment rows: token 8 nt + g (tokens past M read token M - 1; their columns are
     // never stored, and a product column depends only on its own B column).
@@ -218,7 +226,8 @@ __global__ void __launch_bounds__((WC + 1) * 32) gemv_tma_kernel(const __grid_co
     constexpr uint32_t kMask = 0x000F000Fu, kMagic = 0x43004300u, kNeg128 = 0xC300C300u;
     // This warp's rows inside a stage: codes of row r, 16-byte chunk c at r * 128 + ((c ^ (r & 7)) * 16)
     // (the TMA's 128-byte swizzle); lane (g, t) reads chunks 2t, 2t + 1 of rows g and g + 8.
-    const int rA = warp * 16 + g;
+    const int kh = warp / WC;                 // this warp's half-block of every stage
+    const int rA = (warp % WC) * 16 + g;
     uint32_t coff[2][2];
 #pragma unroll
     for (int h = 0; h < 2; ++h)
@@ -275,61 +284,99 @@ __global__ void __launch_bounds__((WC + 1) * 32) gemv_tma_kernel(const __grid_co
       }
     };
 
-    // Two half-blocks (one 512-k block) per iteration; a stage is released as soon as its
-    // values are in registers.
     int s = 0, ph = 0;
     bool ok = true;
-    for (int lh = 0; lh < nh && ok; lh += 2) {
-      uint32_t bA[2], bB[2] = {0u, 0u};
+    // Reads this warp's codes, scale pairs and bias pairs of a half-block sub-stage and
+    // releases the stage (its values are then in registers).
+    auto take = [&](const uint8_t *st, uint4 (&qv)[2][2], uint32_t (&sv)[2], uint32_t (&bq)[2]) {
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int l = lh + j;
-        if (l < nh) {
-          if (!tc::mbar_wait(full0 + 8 * s, (uint32_t)ph, abort_flag, 200)) {
-            ok = false;
-            break;
-          }
-          const uint8_t *st = ring + (size_t)s * kStage;
-          uint4 qv[2][2];
-          uint32_t sv[2];
-          uint32_t (&bq)[2] = j == 0 ? bA : bB;
+      for (int h = 0; h < 2; ++h) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+        for (int jj = 0; jj < 2; ++jj) qv[h][jj] = *reinterpret_cast<const uint4 *>(st + coff[h][jj]);
+        sv[h] = *reinterpret_cast<const uint32_t *>(st + soff0 + h * 128);
+        bq[h] = *reinterpret_cast<const uint32_t *>(st + soff0 + R * 16 + h * 128);
+      }
+    };
+    auto release = [&]() {
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(empty0 + 8 * s);
+      if (++s == ST) {
+        s = 0;
+        ph ^= 1;
+      }
+    };
+    if constexpr (KS == 1) {
+      // Two half-blocks (one 512-k block) per iteration, one stage each.
+      for (int lh = 0; lh < nh && ok; lh += 2) {
+        uint32_t bA[2], bB[2] = {0u, 0u};
 #pragma unroll
-            for (int jj = 0; jj < 2; ++jj) qv[h][jj] = *reinterpret_cast<const uint4 *>(st + coff[h][jj]);
-            sv[h] = *reinterpret_cast<const uint32_t *>(st + soff0 + h * 128);
-            bq[h] = *reinterpret_cast<const uint32_t *>(st + soff0 + R * 16 + h * 128);
-          }
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(empty0 + 8 * s);   // the stage's values are in registers
-          half_product(l, qv, sv);
-          if (++s == ST) {
-            s = 0;
-            ph ^= 1;
+        for (int j = 0; j < 2; ++j) {
+          const int l = lh + j;
+          if (l < nh) {
+            if (!tc::mbar_wait(full0 + 8 * s, (uint32_t)ph, abort_flag, 200)) {
+              ok = false;
+              break;
+            }
+            uint4 qv[2][2];
+            uint32_t sv[2];
+            take(ring + (size_t)s * kStage, qv, sv, j == 0 ? bA : bB);
+            release();
+            half_product(l, qv, sv);
           }
         }
+        if (!ok) break;
+        if (lh + 1 < nh) bias_product(bA[0], bA[1], bB[0], bB[1], lh >> 1);
+        else bias_product(bA[0], bA[1], bA[0], bA[1], lh >> 1);   // the slice ends after a first half:
+                                                                   // that block's other X are zero
       }
-      if (!ok) break;
-      if (lh + 1 < nh) bias_product(bA[0], bA[1], bB[0], bB[1], lh >> 1);
-      else bias_product(bA[0], bA[1], bA[0], bA[1], lh >> 1);   // the slice ends after a first half:
-                                                                 // that block's other X are zero
+    } else {
+      // One 512-k block per stage; consumer group kh takes its half-block kh, and its bias
+      // product carries zeros in place of the other half's biases.
+      for (int i = 0; i < nst; ++i) {
+        if (!tc::mbar_wait(full0 + 8 * s, (uint32_t)ph, abort_flag, 200)) {
+          ok = false;
+          break;
+        }
+        const int l = 2 * i + kh;
+        if (l < nh) {
+          uint4 qv[2][2];
+          uint32_t sv[2], bq[2];
+          take(ring + (size_t)s * kStage + (size_t)kh * kSub, qv, sv, bq);
+          release();
+          half_product(l, qv, sv);
+          if (kh == 0) bias_product(bq[0], bq[1], 0u, 0u, i);
+          else bias_product(0u, 0u, bq[0], bq[1], i);
+        } else {
+          release();
+        }
+      }
     }
 
-    // Partial tile -> red[tok][row].
+    // Partial tile of this consumer group -> red[kh][tok][row].
+    float *rk = red + kh * p.M * R;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int tk = 8 * nt + 2 * t;
       if (tk < p.M) {
-        red[tk * R + rA] = acc[nt][0];
-        red[tk * R + rA + 8] = acc[nt][2];
+        rk[tk * R + rA] = acc[nt][0];
+        rk[tk * R + rA + 8] = acc[nt][2];
       }
       if (tk + 1 < p.M) {
-        red[(tk + 1) * R + rA] = acc[nt][1];
-        red[(tk + 1) * R + rA + 8] = acc[nt][3];
+        rk[(tk + 1) * R + rA] = acc[nt][1];
+        rk[(tk + 1) * R + rA + 8] = acc[nt][3];
       }
     }
   }
 
+  if constexpr (KS > 1) {   // the consumer groups' partials, summed in group order
+    __syncthreads();
+    for (int i = threadIdx.x; i < p.M * R; i += (NC + 1) * 32) {
+      float v = red[i];
+#pragma unroll
+      for (int k = 1; k < KS; ++k) v += red[k * p.M * R + i];
+      red[i] = v;
+    }
+  }
   // red -> y (one split) or the cluster's rank-order sum; every thread of the CTA takes part.
   if (S > 1) {
     cluster_sum_store<R>(p, red);
@@ -337,7 +384,7 @@ __global__ void __launch_bounds__((WC + 1) * 32) gemv_tma_kernel(const __grid_co
   }
   __syncthreads();
   const int quads = R / 4;
-  for (int i = threadIdx.x; i < p.M * quads; i += (WC + 1) * 32) {
+  for (int i = threadIdx.x; i < p.M * quads; i += (NC + 1) * 32) {
     const int tok = i / quads, qd = i % quads;
     const float4 v = *reinterpret_cast<const float4 *>(red + tok * R + qd * 4);
     const int n0 = row0 + qd * 4;
