@@ -65,7 +65,11 @@ def test_lut4_worked_example_on_gpu():
         np.testing.assert_array_equal(got, np.array([expected, expected]))
 
 
-@pytest.mark.parametrize("rows,cols,block", [(64, 128, 64), (3, 5, 4), (33, 70, 6)])
+# (64, 128, 64), (129, 512, 32) and (4096, 4096, 64) take the vectorised kernel; (33, 70, 64)
+# too, with a tail of 6 elements past the last whole 32; (3, 5, 4) and (33, 70, 6) the
+# element kernel.
+@pytest.mark.parametrize("rows,cols,block", [(64, 128, 64), (3, 5, 4), (33, 70, 6), (33, 70, 64),
+                                             (129, 512, 32), (4096, 4096, 64)])
 def test_lut4_dequant_bit_exact(rows, cols, block):
     packed, scales, book = synth.lut4_weights(80, rows, cols, block)
     ref = oracle.lut4_dequant(packed, scales, book, rows, cols, block)

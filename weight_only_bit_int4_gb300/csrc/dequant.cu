@@ -13,43 +13,57 @@
 namespace q4mm {
 namespace {
 
+// A thread decodes one 32-bit word (8 elements of one group) per step, so consecutive lanes
+// read consecutive 4-byte words and write consecutive 16-byte (bf16 / f16) or 32-byte (f32)
+// pieces: every load and store of a warp is one contiguous run.  The code becomes a float
+// exactly through the exponent trick (0x4B000000 | q is 2^23 + q), and one fmaf per element
+// forms q * s + b.
 template <int OUT>   // 0 = f32, 1 = bf16, 2 = f16
-__global__ void __launch_bounds__(256) q4_dequant_kernel(const uint4 *__restrict__ w,
+__global__ void __launch_bounds__(256) q4_dequant_kernel(const uint32_t *__restrict__ w,
                                                          const uint16_t *__restrict__ scales,
                                                          const uint16_t *__restrict__ biases,
-                                                         int64_t groups, void *__restrict__ out) {
-  for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
-       g += (int64_t)gridDim.x * blockDim.x) {
-    const uint4 q = ldg_stream_v4(w + g);
-    const float s = bf16_bits_to_float(ldg_u16(scales + g));
-    const float b = bf16_bits_to_float(ldg_u16(biases + g));
-    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-    float v[32];
+                                                         int64_t words, void *__restrict__ out) {
+  constexpr int kU = 4;   // words per thread per step, a warp-width apart
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x * kU;
+  const int64_t lane0 = (int64_t)blockIdx.x * blockDim.x * kU + (threadIdx.x / 32) * 32 * kU + threadIdx.x % 32;
+  for (int64_t base = lane0; base < words; base += stride) {
+    uint32_t q[kU];
+    float s[kU], b[kU];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int u = 0; u < kU; ++u) {
+      const int64_t i = base + 32 * u;
+      if (i < words) {
+        q[u] = __ldg(w + i);
+        s[u] = bf16_bits_to_float(ldg_u16(scales + i / 4));
+        b[u] = bf16_bits_to_float(ldg_u16(biases + i / 4));
+      }
+    }
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        v[i * 8 + j] = __fmaf_rn(static_cast<float>((words[i] >> (4 * j)) & 0xFu), s, b);
-    if constexpr (OUT == 0) {
-      float4 *o = reinterpret_cast<float4 *>(out) + g * 8;
+    for (int u = 0; u < kU; ++u) {
+      const int64_t i = base + 32 * u;
+      if (i >= words) break;
+      float v[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-    } else {
-      uint4 *o = reinterpret_cast<uint4 *>(out) + g * 4;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t p[4];
+      for (int j = 0; j < 8; ++j) {
+        const float qf = __uint_as_float(0x4B000000u | ((q[u] >> (4 * j)) & 0xFu)) - 8388608.0f;   // exact
+        v[j] = __fmaf_rn(qf, s[u], b[u]);
+      }
+      if constexpr (OUT == 0) {
+        float4 *o = reinterpret_cast<float4 *>(out) + i * 2;
+        o[0] = make_float4(v[0], v[1], v[2], v[3]);
+        o[1] = make_float4(v[4], v[5], v[6], v[7]);
+      } else {
+        uint32_t pk[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float lo = v[8 * i + 2 * j], hi = v[8 * i + 2 * j + 1];
           if constexpr (OUT == 1) {
-            p[j] = pack_bf16x2(lo, hi);
+            pk[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
           } else {
-            __half2 h = __floats2half2_rn(lo, hi);
-            p[j] = *reinterpret_cast<uint32_t *>(&h);
+            __half2 h = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
+            pk[j] = *reinterpret_cast<uint32_t *>(&h);
           }
         }
-        o[i] = make_uint4(p[0], p[1], p[2], p[3]);
+        reinterpret_cast<uint4 *>(out)[i] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
     }
   }
@@ -59,15 +73,14 @@ __global__ void __launch_bounds__(256) q4_dequant_kernel(const uint4 *__restrict
 
 cudaError_t launch_q4_dequant(const uint32_t *w, const uint16_t *scales, const uint16_t *biases,
                               int64_t N, int64_t K, void *out, int out_dtype, cudaStream_t s) {
-  const int64_t groups = N * (K / 32);
+  const int64_t words = N * (K / 8);
   const int threads = 256;
-  int64_t blocks = (groups + threads - 1) / threads;
+  int64_t blocks = (words + threads * 4 - 1) / (threads * 4);
   if (blocks > 152 * 16) blocks = 152 * 16;
-  const uint4 *w4 = reinterpret_cast<const uint4 *>(w);
   switch (out_dtype) {
-    case Q4MM_F32: q4_dequant_kernel<0><<<(unsigned)blocks, threads, 0, s>>>(w4, scales, biases, groups, out); break;
-    case Q4MM_BF16: q4_dequant_kernel<1><<<(unsigned)blocks, threads, 0, s>>>(w4, scales, biases, groups, out); break;
-    default: q4_dequant_kernel<2><<<(unsigned)blocks, threads, 0, s>>>(w4, scales, biases, groups, out); break;
+    case Q4MM_F32: q4_dequant_kernel<0><<<(unsigned)blocks, threads, 0, s>>>(w, scales, biases, words, out); break;
+    case Q4MM_BF16: q4_dequant_kernel<1><<<(unsigned)blocks, threads, 0, s>>>(w, scales, biases, words, out); break;
+    default: q4_dequant_kernel<2><<<(unsigned)blocks, threads, 0, s>>>(w, scales, biases, words, out); break;
   }
   return cudaGetLastError();
 }

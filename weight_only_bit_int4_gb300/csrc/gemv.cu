@@ -1193,16 +1193,17 @@ __global__ void __launch_bounds__(KS * 32) gemv_lks_kernel(const __grid_constant
     }
   };
 
-  // Pair table: entry (byte, copy) at ltab[byte * 16 + copy].
-  for (int i = threadIdx.x; i < 256 * kLutCopies; i += KS * 32) {
-    const int byte = i / kLutCopies;
-    ltab[i] = pack_bf16x2(p.book[byte >> 4], p.book[byte & 15]);
-  }
   // Chunks go through the loop in pairs; DEPTH - 2 chunks are in flight ahead of a pair.
+  // They are issued first, so the weight stream is under way while the table is built.
 #pragma unroll
   for (int i = 0; i < DEPTH - 2; ++i) {
     if (i < nch) issue(i);
     cp_async_commit();
+  }
+  // Pair table: entry (byte, copy) at ltab[byte * 16 + copy].
+  for (int i = threadIdx.x; i < 256 * kLutCopies; i += KS * 32) {
+    const int byte = i / kLutCopies;
+    ltab[i] = pack_bf16x2(p.book[byte >> 4], p.book[byte & 15]);
   }
   // Weights are in flight; x may be the previous kernel's output, and y may still be read by it.
   griddep_launch_dependents();

@@ -169,6 +169,93 @@ __global__ void __launch_bounds__(256) lut4_dequant_kernel(const uint8_t *__rest
   }
 }
 
+// Vectorised decode for block % 32 == 0 and 16-byte aligned codes and output: a thread takes
+// 8 consecutive elements (4 code bytes, one 4-byte load; they share one scale) per step, so
+// consecutive lanes read consecutive words and write consecutive 16-byte (bf16 / f16) or
+// 32-byte (f32) pieces.  Each byte's two codebook values come as one pair from a 256-entry
+// table in shared memory; fl32(book * scale) is formed in fp32.  Elements past the last whole
+// 32 run through the element kernel.
+template <int OUT>   // 0 = f32, 1 = bf16, 2 = f16
+__global__ void __launch_bounds__(256) lut4_dequant_vec_kernel(const uint8_t *__restrict__ packed,
+                                                               const float *__restrict__ scales,
+                                                               const __grid_constant__ Book16 bk,
+                                                               int64_t n32, int64_t block,
+                                                               void *__restrict__ out) {
+  __shared__ float2 pairs[256];   // byte b -> (book[b >> 4], book[b & 15]): (even, odd) element
+  pairs[threadIdx.x] = make_float2(bk.v[threadIdx.x >> 4], bk.v[threadIdx.x & 15]);
+  __syncthreads();
+  constexpr int kU = 4;   // words per thread per step, a warp-width apart
+  const int64_t words = n32 * 4;
+  const int64_t per_scale = block / 8;   // words per scale
+  const uint32_t *w32 = reinterpret_cast<const uint32_t *>(packed);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x * kU;
+  const int64_t lane0 = (int64_t)blockIdx.x * blockDim.x * kU + (threadIdx.x / 32) * 32 * kU + threadIdx.x % 32;
+  for (int64_t base = lane0; base < words; base += stride) {
+    uint32_t c[kU];
+    float sc[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t i = base + 32 * u;
+      if (i < words) {
+        c[u] = __ldg(w32 + i);
+        sc[u] = __ldg(scales + i / per_scale);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t i = base + 32 * u;
+      if (i >= words) break;
+      float v[8];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const float2 pr = pairs[(c[u] >> (8 * b)) & 0xFFu];
+        v[2 * b] = pr.x * sc[u];
+        v[2 * b + 1] = pr.y * sc[u];
+      }
+      if constexpr (OUT == 0) {
+        float4 *o = static_cast<float4 *>(out) + i * 2;
+        o[0] = make_float4(v[0], v[1], v[2], v[3]);
+        o[1] = make_float4(v[4], v[5], v[6], v[7]);
+      } else {
+        uint32_t h[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if constexpr (OUT == 1) {
+            h[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+          } else {
+            __half2 hh = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
+            h[j] = *reinterpret_cast<uint32_t *>(&hh);
+          }
+        }
+        static_cast<uint4 *>(out)[i] = make_uint4(h[0], h[1], h[2], h[3]);
+      }
+    }
+  }
+}
+
+template <int OUT>
+__global__ void __launch_bounds__(256) lut4_dequant_tail_kernel(const uint8_t *__restrict__ packed,
+                                                                const float *__restrict__ scales,
+                                                                const __grid_constant__ Book16 bk,
+                                                                int64_t f0, int64_t total, int64_t block,
+                                                                void *__restrict__ out) {
+  __shared__ float book[16];
+  if (threadIdx.x < 16) book[threadIdx.x] = bk.v[threadIdx.x];
+  __syncthreads();
+  const int64_t f = f0 + threadIdx.x;
+  if (f >= total) return;
+  const float v = lut4_value(packed, scales, book, f, block);
+  if constexpr (OUT == 0) {
+    static_cast<float *>(out)[f] = v;
+  } else if constexpr (OUT == 1) {
+    __nv_bfloat16 b = __float2bfloat16_rn(v);
+    static_cast<uint16_t *>(out)[f] = *reinterpret_cast<uint16_t *>(&b);
+  } else {
+    __half h = __float2half_rn(v);
+    static_cast<uint16_t *>(out)[f] = *reinterpret_cast<uint16_t *>(&h);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_lut4_general(const uint16_t *x, const uint8_t *packed, const float *scales,
@@ -211,6 +298,28 @@ cudaError_t launch_lut4_dequant(const uint8_t *packed, const float *scales, cons
   Book16 bk;
   for (int i = 0; i < 16; ++i) bk.v[i] = book[i];
   const int64_t total = rows * cols;
+  const bool vec = block % 32 == 0 && (reinterpret_cast<uintptr_t>(packed) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(out) & 15) == 0 && total >= 32;
+  if (vec) {
+    const int64_t n32 = total / 32, rest = total - n32 * 32;
+    int64_t blocks = (n32 * 4 + 1023) / 1024;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    switch (out_dtype) {
+      case Q4MM_F32:
+        lut4_dequant_vec_kernel<0><<<(unsigned)blocks, 256, 0, s>>>(packed, scales, bk, n32, block, out);
+        if (rest) lut4_dequant_tail_kernel<0><<<1, 256, 0, s>>>(packed, scales, bk, n32 * 32, total, block, out);
+        break;
+      case Q4MM_BF16:
+        lut4_dequant_vec_kernel<1><<<(unsigned)blocks, 256, 0, s>>>(packed, scales, bk, n32, block, out);
+        if (rest) lut4_dequant_tail_kernel<1><<<1, 256, 0, s>>>(packed, scales, bk, n32 * 32, total, block, out);
+        break;
+      default:
+        lut4_dequant_vec_kernel<2><<<(unsigned)blocks, 256, 0, s>>>(packed, scales, bk, n32, block, out);
+        if (rest) lut4_dequant_tail_kernel<2><<<1, 256, 0, s>>>(packed, scales, bk, n32 * 32, total, block, out);
+        break;
+    }
+    return cudaGetLastError();
+  }
   int64_t blocks = (total + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
   switch (out_dtype) {
