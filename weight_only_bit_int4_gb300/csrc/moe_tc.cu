@@ -6,14 +6,15 @@
 //
 //  1. routing (moe.cu): per-expert counts, ascending row lists, and a list of token blocks
 //     of <= 128 rows, each inside one expert;
-//  2. gather: xs[p] = fp16(2^e_p * x[hids[p] / top_k]) -- the rows of x in routed order, each
-//     scaled by a power of two that brings its largest magnitude into [2^14, 2^15);
+//  2. gather: xs[p] = fp16(2^e_t * x[t]), t = hids[p] / top_k -- the rows of x in routed
+//     order, each token scaled by a power of two that brings its largest magnitude into
+//     [2^14, 2^15) (found once per token by token_scale_kernel);
 //  3. this kernel, persistent over work items (token block, 128-row weight tile):
 //       A = the expert's Q4_0 weight rows, decoded to fp16 by four producer warps from
 //           144-byte TMA boxes (8 blocks of 18 bytes = 256 k per box);
 //       B = the block's gathered x rows (TMA, 64-row boxes, 128-byte swizzle);
 //       D = 128 weight rows x (rows rounded up to 16) fp32 in tensor memory;
-//     epilogue warps scatter 2^-e_p * D column j to out[hids[p0 + j]][n0 .. n0+127] (fp32).
+//     epilogue warps scatter 2^-e_t * D column j to out[hids[p0 + j]][n0 .. n0+127] (fp32).
 //     Each expert's weights stream once from HBM per token block.
 //
 // Operands are fp16 (fp32 accumulation): Q4_0's d is already fp16, so (q - 8) * d is formed
@@ -338,60 +339,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// xs[p] = fp16(2^e_p * x[hids[p] / top_k]) for p < number of valid routed rows, each 32-element
-// block laid out in the chunk order of q4_0_chunk, and xun[p] = 2^-e_p.  e_p is chosen so
-// that the row's largest magnitude m lands in [2^14, 2^15) (e_p = 15 - frexp exponent of m,
-// clamped to [-126, 127] so that both powers of two are f32 values; m == 0 or a non-finite m
-// keeps e_p = 0).  Multiplying by a power of two is exact, so the only rounding is the one to
-// fp16, relative to the row's own range.  A CTA takes four rows at a time: one pass finds the
-// four maxima (item = (row, block, chunk m): two float4 loads, elements 4m.. and 16+4m..), a
-// second pass reloads the rows (L1-resident) and stores one 16-byte chunk per item.
+// Per token t: the power of two 2^e_t that brings the row's largest magnitude m into
+// [2^14, 2^15) (e_t = 15 - frexp exponent of m, clamped to [-126, 127] so that both 2^e_t and
+// 2^-e_t are f32 values; m == 0 or a non-finite m keeps e_t = 0).  One CTA per token.
+__global__ void __launch_bounds__(256) token_scale_kernel(const float *__restrict__ x, int K,
+                                                          float *__restrict__ tsc) {
+  __shared__ float red[8];
+  const float4 *row = reinterpret_cast<const float4 *>(x + (size_t)blockIdx.x * K);
+  float m = 0.f;
+  for (int i = threadIdx.x; i < K / 4; i += blockDim.x) {
+    const float4 v = __ldg(row + i);
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x / 32); ++w) m = fmaxf(m, red[w]);
+    int e = 0;
+    if (m > 0.f && m <= 3.402823466e38f) {
+      int ex = 0;
+      frexpf(m, &ex);          // m in [2^(ex-1), 2^ex)
+      e = min(max(15 - ex, -126), 127);
+    }
+    tsc[blockIdx.x] = ldexpf(1.f, e);
+  }
+}
+
+// xs[p] = fp16(2^e_t * x[t]) with t = hids[p] / top_k for p < number of valid routed rows,
+// each 32-element block laid out in the chunk order of q4_0_chunk, and xun[p] = 2^-e_t.
+// Multiplying by a power of two is exact, so the only rounding is the one to fp16, relative
+// to the token row's own range.  Item = (row, block, chunk m): two float4 loads (elements
+// 4m.. and 16+4m..) and one 16-byte store; a CTA takes four rows at a time, so each thread
+// has four items' loads in flight.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const float *__restrict__ x, const int32_t *__restrict__ hids,
                                                           const uint32_t *__restrict__ n_valid, int top_k, int K,
-                                                          uint16_t *__restrict__ xs, float *__restrict__ xun,
-                                                          int n_rows) {
-  __shared__ float red[8][4];
-  __shared__ float fac[4];
+                                                          const float *__restrict__ tsc, uint16_t *__restrict__ xs,
+                                                          float *__restrict__ xun, int n_rows) {
   const int nv = min((int)*n_valid, n_rows);
   const int per_row = K / 8;   // items per row: K / 32 blocks x 4 chunks
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   for (int pos0 = blockIdx.x * 4; pos0 < nv; pos0 += gridDim.x * 4) {
     const float *src[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) src[u] = pos0 + u < nv ? x + (size_t)(hids[pos0 + u] / top_k) * K : nullptr;
-    float mx[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int i = threadIdx.x; i < per_row; i += blockDim.x) {
-      const int off = (i >> 2) * 32 + 4 * (i & 3);
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (src[u] != nullptr) {
-          const float4 a = __ldg(reinterpret_cast<const float4 *>(src[u] + off));
-          const float4 b = __ldg(reinterpret_cast<const float4 *>(src[u] + off + 16));
-          mx[u] = fmaxf(mx[u], fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
-                                     fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w)))));
-        }
-    }
+    float f[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx[u] = fmaxf(mx[u], __shfl_xor_sync(0xFFFFFFFFu, mx[u], o));
-      if (lane == 0) red[warp][u] = mx[u];
+      const int tok = pos0 + u < nv ? hids[pos0 + u] / top_k : 0;
+      src[u] = pos0 + u < nv ? x + (size_t)tok * K : nullptr;
+      f[u] = pos0 + u < nv ? __ldg(tsc + tok) : 1.f;
+      if (threadIdx.x == 0 && pos0 + u < nv) xun[pos0 + u] = 1.0f / f[u];   // exact: a power of two
     }
-    __syncthreads();
-    if (threadIdx.x < 4) {
-      const int u = threadIdx.x;
-      float m = 0.f;
-      for (int wv = 0; wv < (int)(blockDim.x / 32); ++wv) m = fmaxf(m, red[wv][u]);
-      int e = 0;
-      if (m > 0.f && m <= 3.402823466e38f) {
-        int ex = 0;
-        frexpf(m, &ex);          // m in [2^(ex-1), 2^ex)
-        e = min(max(15 - ex, -126), 127);
-      }
-      fac[u] = ldexpf(1.f, e);
-      if (pos0 + u < nv) xun[pos0 + u] = ldexpf(1.f, -e);
-    }
-    __syncthreads();
     for (int i = threadIdx.x; i < per_row; i += blockDim.x) {
       const int off = (i >> 2) * 32 + 4 * (i & 3);
       float4 lo[4], hi[4];
@@ -404,16 +401,15 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const float *__restric
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         if (src[u] != nullptr) {
-          const float f = fac[u];
+          const float s = f[u];
           const float4 a = lo[u], b = hi[u];
-          __half2 h0 = __floats2half2_rn(a.x * f, a.z * f), h1 = __floats2half2_rn(a.y * f, a.w * f);
-          __half2 h2 = __floats2half2_rn(b.x * f, b.z * f), h3 = __floats2half2_rn(b.y * f, b.w * f);
+          __half2 h0 = __floats2half2_rn(a.x * s, a.z * s), h1 = __floats2half2_rn(a.y * s, a.w * s);
+          __half2 h2 = __floats2half2_rn(b.x * s, b.z * s), h3 = __floats2half2_rn(b.y * s, b.w * s);
           *reinterpret_cast<uint4 *>(xs + (size_t)(pos0 + u) * K + (size_t)i * 8) =
               make_uint4(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
                          *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
         }
     }
-    __syncthreads();   // red and fac are reused by the next four rows
   }
 }
 
@@ -443,10 +439,12 @@ cudaError_t launch_q4_0_mm_tc(const float *x, const uint8_t *w, float *out, int 
   const uint32_t *offs = reinterpret_cast<const uint32_t *>(ws + L.offs);
   uint16_t *xs = reinterpret_cast<uint16_t *>(ws + L.xs);
   float *xun = reinterpret_cast<float *>(ws + L.xun);
+  float *tsc = reinterpret_cast<float *>(ws + L.tsc);
   int sms = 148, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
 
-  gather_rows_kernel<<<(unsigned)(4 * sms), 256, 0, s>>>(x, hids, offs + n_experts, top_k, K, xs, xun, n_rows);
+  token_scale_kernel<<<(unsigned)n_tokens, 256, 0, s>>>(x, K, tsc);
+  gather_rows_kernel<<<(unsigned)(4 * sms), 256, 0, s>>>(x, hids, offs + n_experts, top_k, K, tsc, xs, xun, n_rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

@@ -292,9 +292,10 @@ size_t q4_0_mm_workspace_bytes(int64_t n_tokens, int64_t top_k, int64_t N, int64
 //   xs      fp16 [R, K]    x rows gathered in hids order, each scaled by a power of two
 //                          (the mm operand)
 //   xun     f32 [R]        per gathered row, the power of two that undoes its scaling
+//   tsc     f32 [R]        per token (first n_tokens entries), the power of two that scales it
 constexpr int kMoeTokBlock = 128;
 struct MoeWorkspace {
-  size_t htpe, offs, hids, invalid, blk, n_blk, xs, xun, total;
+  size_t htpe, offs, hids, invalid, blk, n_blk, xs, xun, tsc, total;
 };
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 inline MoeWorkspace moe_workspace_layout(int64_t n_rows, int64_t K, int64_t E) {
@@ -309,6 +310,7 @@ inline MoeWorkspace moe_workspace_layout(int64_t n_rows, int64_t K, int64_t E) {
   w.n_blk = o; o = align256(o + 4);
   w.xs = o; o = align256(o + 2 * (size_t)n_rows * (size_t)K);
   w.xun = o; o = align256(o + 4 * (size_t)n_rows);
+  w.tsc = o; o = align256(o + 4 * (size_t)n_rows);
   w.total = o;
   return w;
 }
