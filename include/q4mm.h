@@ -59,9 +59,13 @@ typedef enum q4mm_dtype { Q4MM_F32 = 0, Q4MM_BF16 = 1, Q4MM_F16 = 2 } q4mm_dtype
 /* Bits of the device error word. */
 #define Q4MM_DEVERR_WAIT_TIMEOUT 0x1u  /* a pipeline wait gave up; that output is invalid */
 #define Q4MM_DEVERR_BAD_EXPERT 0x2u    /* an id >= n_experts was routed (its row is zero) */
-#define Q4MM_DEVERR_F16_RANGE 0x4u     /* reserved, never raised: the Q4_0 mat-mat form scales
-                                          each gathered x row by a power of two and serves
-                                          every finite f32 x */
+#define Q4MM_DEVERR_F16_RANGE 0x4u     /* a tensor-core mat-mat form (Q4_0, Q8_0) met a weight
+                                          whose dequantised value (q-8)*d or q*d is beyond
+                                          fp16's range (|value| >= 65520, only possible for
+                                          |d| >= 8192 in Q4_0, >= 512 in Q8_0); the outputs
+                                          that weight feeds are not finite.  x itself is
+                                          never out of range: each gathered row is scaled
+                                          by a power of two. */
 
 /* Static string for a status code (never NULL). */
 const char *q4mm_status_string(int status);
@@ -209,6 +213,9 @@ size_t q4_0_matmul_id_workspace_size(int64_t n_tokens, int64_t top_k, int64_t N,
  *       1 = mat-vec (each routed row reads its expert's rows; no workspace),
  *       2 = mat-mat (route, gather each expert's rows, stream each expert's weights once
  *           per 128-row tile through the tensor cores; needs the workspace).
+ * The mat-mat form runs on the tensor cores when K % 256 == 0 and w and expert_stride are
+ * 16-byte aligned (fp16 operands: each weight (q-8)*d rounded once to fp16, each x row scaled
+ * by a power of two and rounded once to fp16; fp32 accumulation), else on the fp32 FMA pipes.
  * Requirements: n_tokens, top_k, N, K, n_experts >= 1; K % 32 == 0; expert_stride >=
  * N*(K/32)*18; x, out 16-byte aligned; workspace (mat-mat) 256-byte aligned and at least
  * q4_0_matmul_id_workspace_size(...) bytes. */
@@ -247,10 +254,13 @@ q4mm_status q4_0_matmul_id_swiglu(const float *gate, const float *up, const void
  *   out[r][n] = sum_k x[r / top_k][k] * W[ids[r]][n][k]   (f32, fp32 accumulation);
  *   an id >= n_experts gives a zero row and sets Q4MM_DEVERR_BAD_EXPERT.
  * Mode 0 (automatic: mat-mat when n_tokens > Q4MM_MM_ID_THRESHOLD), 1 (mat-vec: each routed
- * row in order) or 2 (mat-mat: route, then visit the routed rows expert by expert).  The
- * mat-mat form needs q8_0_matmul_id_workspace_size(...) bytes of 256-byte aligned workspace
- * (the routing lists).  Requirements: K % 32 == 0, expert_stride >= N*(K/32)*34, x and out
- * 16-byte aligned, ids 4-byte aligned. */
+ * row in order, fp32 FMA) or 2 (mat-mat: route, then the tensor-core kernel of q4_0_matmul_id
+ * with the Q8_0 decode when K % 256 == 0 and w and expert_stride are 16-byte aligned --
+ * weights q*d rounded once to fp16, see Q4MM_DEVERR_F16_RANGE -- else the routed rows expert by
+ * expert on the fp32 FMA pipes).  The mat-mat form needs q8_0_matmul_id_workspace_size(...)
+ * bytes of 256-byte aligned workspace (the routing lists and the gathered x rows).
+ * Requirements: K % 32 == 0, expert_stride >= N*(K/32)*34, x and out 16-byte aligned, ids
+ * 4-byte aligned. */
 size_t q8_0_matmul_id_workspace_size(int64_t n_tokens, int64_t top_k, int64_t N, int64_t K,
                                      int64_t n_experts);
 q4mm_status q8_0_matmul_id(const float *x, const void *w, const uint32_t *ids, float *out,

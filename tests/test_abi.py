@@ -109,7 +109,7 @@ def test_q8_0_argument_checks(L):
     # mat-mat without (enough) workspace -> WORKSPACE; misaligned x -> UNSUPPORTED
     assert L.q8_0_matmul_id(FAKE, FAKE, FAKE, FAKE, 64, 8, 64, 64, 16, stride, 2, None, 0, None) == 3
     need = L.q8_0_matmul_id_workspace_size(64, 8, 64, 64, 16)
-    assert 0 < need < L.q4_0_matmul_id_workspace_size(64, 8, 64, 64, 16)   # no gathered rows
+    assert need == L.q4_0_matmul_id_workspace_size(64, 8, 64, 64, 16)   # the same routing and gathered rows
     assert L.q8_0_matmul_id(FAKE, FAKE, FAKE, FAKE, 64, 8, 64, 64, 16, stride, 2, FAKE, need - 1, None) == 3
     assert L.q8_0_matmul_id(FAKE + 4, FAKE, FAKE, FAKE, 2, 8, 64, 64, 16, stride, 1, None, 0, None) == 2
     # n_tokens == 0 is a no-op

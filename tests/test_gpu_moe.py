@@ -78,11 +78,13 @@ def test_moe_parity(mode, n_tokens, top_k, E, N, K, pad):
 
 # Invalid ids in one 32-row chunk, in chunks zeroed by different CTAs, and in an id count
 # large enough for the single-CTA routing form.
+# K = 128 runs the CUDA-core kernels, K = 256 the tensor-core mat-mat kernel.
+@pytest.mark.parametrize("K", [128, 256])
 @pytest.mark.parametrize("mode", [1, 2])
 @pytest.mark.parametrize("n_tokens,top_k,E,bad_rows", [(6, 2, 4, [5]), (300, 4, 8, [5, 100, 101, 700, 1199]),
                                                        (1600, 8, 8, [0, 4000, 12799])])
-def test_moe_invalid_id_gives_zero_row(mode, n_tokens, top_k, E, bad_rows):
-    N, K = 64, 128
+def test_moe_invalid_id_gives_zero_row(mode, n_tokens, top_k, E, bad_rows, K):
+    N = 64
     x, w, stride, ids = _moe_case(7, n_tokens, top_k, E, N, K)
     ids = ids.copy()
     ids[bad_rows] = 99
@@ -254,10 +256,14 @@ def _run_q8(x, w, ids, top_k, N, K, E, stride, mode):
     return out.cpu().numpy().astype(np.float64)
 
 
+# Mode 2 with K % 256 == 0 and 16-byte aligned expert slabs runs the tensor-core kernel
+# (fp16 operands); the padded stride of 2 bytes and K = 96 or 32 keep the CUDA-core kernel.
+# (300, 4, 4, ...) gives every expert about 300 routed rows, three token blocks.
 @pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("n_tokens,top_k,E,N,K,pad", [(1, 8, 64, 96, 256, 0), (5, 2, 6, 64, 2048, 2),
                                                       (40, 8, 16, 130, 512, 16), (33, 1, 3, 256, 96, 0),
-                                                      (3, 4, 9, 70, 4096, 0), (2, 2, 3, 20, 32, 0)])
+                                                      (3, 4, 9, 70, 4096, 0), (2, 2, 3, 20, 32, 0),
+                                                      (300, 4, 4, 160, 768, 0)])
 def test_q8_0_parity(mode, n_tokens, top_k, E, N, K, pad):
     x, w, stride, ids = _q8_case(200 + n_tokens, n_tokens, top_k, E, N, K, pad)
     ref = oracle.q8_0_matmul_id(x, w, ids, n_tokens, top_k, N, K, E, stride)
@@ -265,9 +271,10 @@ def test_q8_0_parity(mode, n_tokens, top_k, E, N, K, pad):
     assert_within_tolerance(got, ref, f"q8_0_matmul_id mode={mode}")
 
 
+@pytest.mark.parametrize("K", [128, 256])
 @pytest.mark.parametrize("mode", [1, 2])
-def test_q8_0_invalid_id_gives_zero_row(mode):
-    n_tokens, top_k, E, N, K = 300, 4, 8, 64, 128
+def test_q8_0_invalid_id_gives_zero_row(mode, K):
+    n_tokens, top_k, E, N = 300, 4, 8, 64
     x, w, stride, ids = _q8_case(17, n_tokens, top_k, E, N, K)
     ids = ids.copy()
     bad_rows = [5, 100, 101, 700, 1199]
@@ -289,3 +296,76 @@ def test_q8_0_full_size_sampled(n_tokens, mode):
                                      np.random.default_rng(n_tokens + 7).integers(0, n_tokens * top_k, 24)]))
     ref = oracle.q8_0_matmul_id_rows(x, w, ids, top_k, N, K, E, stride, rows)
     assert_within_tolerance(got[rows], ref, f"q8_0 full n_tokens={n_tokens} mode={mode}")
+
+
+# The tensor-core mat-mat form of Q8_0 scales each gathered x row by a power of two, as the
+# Q4_0 form does: rows far outside fp16's range are served, each held to its own rms.
+def test_q8_0_mm_any_f32_row_range():
+    n_tokens, top_k, E, N, K = 48, 4, 8, 192, 512
+    x, w, stride, ids = _q8_case(4300, n_tokens, top_k, E, N, K)
+    x = x.copy()
+    gains = np.array([1e6, 1e-6, 1.0, 3e4, 2e-5, 7e7, 1e-30, 5e30], np.float32)
+    x *= gains[np.arange(n_tokens) % gains.size][:, None]
+    x[5, 17] = 1e9
+    assert np.all(np.isfinite(x))
+    q.device_errors()
+    got = _run_q8(x, w, ids, top_k, N, K, E, stride, 2)
+    ref = oracle.q8_0_matmul_id(x, w, ids, n_tokens, top_k, N, K, E, stride)
+    assert np.all(np.isfinite(got))
+    for r in range(n_tokens * top_k):
+        assert_within_tolerance(got[r], ref[r], f"q8_0 routed row {r} (token {r // top_k})")
+    assert q.device_errors() == 0
+
+
+# ---------------------------------------------------------------------------------------
+# Weights near the end of fp16's range in the tensor-core mat-mat forms, which form each
+# dequantised weight as one fp16 product.  A large d whose products all stay finite is served
+# without a flag; a block with a product beyond fp16 (|value| >= 65520) raises
+# Q4MM_DEVERR_F16_RANGE, and only the outputs that block feeds are affected.
+# ---------------------------------------------------------------------------------------
+
+def _set_block(w, stride, K, bbytes, e, n, b, d, qs):
+    off = e * stride + (n * (K // 32) + b) * bbytes
+    w[off:off + 2] = np.array([d], np.float16).view(np.uint8)
+    w[off + 2:off + bbytes] = qs
+
+
+@pytest.mark.parametrize("bt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("overflow", [False, True])
+def test_mm_weight_range(bt, overflow):
+    n_tokens, top_k, E, N, K = 64, 2, 4, 128, 512
+    rng = np.random.default_rng(91)
+    if bt == "q4_0":
+        x, w, stride, ids = _moe_case(4400, n_tokens, top_k, E, N, K)
+        d = 9000.0                                        # 7 d = 63000 is finite, 8 d is not
+        nib = rng.integers(1, 16, 32).astype(np.uint8)    # q - 8 in [-7, 7]
+        if overflow:
+            nib[0] = 0                                    # q - 8 = -8: -72000
+        qs = (nib[:16] | (nib[16:] << 4)).astype(np.uint8)
+        bbytes, run, ref_fn = 18, _run, oracle.q4_0_matmul_id
+    else:
+        x, w, stride, ids = _q8_case(4500, n_tokens, top_k, E, N, K)
+        d = 600.0                                         # 100 d = 60000 is finite, 127 d is not
+        qv = rng.integers(-100, 101, 32)
+        if overflow:
+            qv[7] = 127                                   # 76200
+        qs = qv.astype(np.int8).view(np.uint8)
+        bbytes, run, ref_fn = 34, _run_q8, oracle.q8_0_matmul_id
+    w = w.copy()
+    e_big, n_big, b_big = 2, 9, 3
+    _set_block(w, stride, K, bbytes, e_big, n_big, b_big, d, qs)
+    q.device_errors()
+    got = run(x, w, ids, top_k, N, K, E, stride, 2)
+    err = q.device_errors()
+    ref = ref_fn(x, w, ids, n_tokens, top_k, N, K, E, stride)
+    fed = np.zeros(got.shape, bool)
+    fed[np.nonzero(ids == e_big)[0], n_big] = True
+    assert fed.any()
+    if overflow:
+        assert err & 0x4
+        assert not np.any(np.isfinite(got[fed]))
+        assert_within_tolerance(got[~fed], ref[~fed], f"{bt} outputs the block does not feed")
+    else:
+        assert err == 0
+        assert_within_tolerance(got[fed], ref[fed], f"{bt} outputs of the large finite weights")
+        assert_within_tolerance(got[~fed], ref[~fed], f"{bt} other outputs")

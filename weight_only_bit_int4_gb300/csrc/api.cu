@@ -297,7 +297,7 @@ size_t q8_0_matmul_id_workspace_size(int64_t n_tokens, int64_t top_k, int64_t N,
   if (n_tokens < 1 || !routed_rows_ok(n_tokens, top_k) || N < 1 || K < 32 || N > kMaxDim || K > kMaxDim ||
       n_experts < 1 || n_experts > 1024)
     return 0;
-  return q8_0_mm_workspace_bytes(n_tokens, top_k, n_experts);
+  return q8_0_mm_workspace_bytes(n_tokens, top_k, K, n_experts);
 }
 
 q4mm_status q8_0_matmul_id(const float *x, const void *w, const uint32_t *ids, float *out,
@@ -316,7 +316,7 @@ q4mm_status q8_0_matmul_id(const float *x, const void *w, const uint32_t *ids, f
   if (!aligned(x, 16) || !aligned(out, 16) || !aligned(ids, 4)) return Q4MM_ERR_UNSUPPORTED;
   const bool mm = mode == 2 || (mode == 0 && n_tokens > Q4MM_MM_ID_THRESHOLD);
   if (mm) {
-    const size_t need = q8_0_mm_workspace_bytes(n_tokens, top_k, n_experts);
+    const size_t need = q8_0_mm_workspace_bytes(n_tokens, top_k, K, n_experts);
     if (!workspace || workspace_bytes < need) return Q4MM_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return Q4MM_ERR_UNSUPPORTED;
   }

@@ -189,7 +189,6 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const uint32_t *__
 constexpr int kMvWarps = 4;
 constexpr int kMvRowsPerWarp = 8;
 constexpr int kMvSegBlocks = 64;   // K segment: 64 blocks = 2048 values
-constexpr int kQ4_0 = 0, kQ8_0 = 1;
 __host__ __device__ constexpr int block_bytes(int bt) { return bt == kQ8_0 ? 34 : 18; }
 
 struct MvParams {
@@ -784,9 +783,8 @@ cudaError_t launch_q4_0_mm(const float *x, const uint8_t *w, const uint32_t *ids
   if (e != cudaSuccess) return e;
   // Tensor-core form: K a multiple of 256 (whole 144-byte TMA boxes of Q4_0 blocks) and
   // 16-byte aligned expert slabs.
-  const bool tc_ok = K % 256 == 0 && expert_stride % 16 == 0 && (reinterpret_cast<uintptr_t>(w) & 15) == 0;
-  if (tc_ok)
-    return launch_q4_0_mm_tc(x, w, out, n_tokens, top_k, N, K, n_experts, expert_stride, workspace, s);
+  if (routed_mm_tc_ok(K, expert_stride, w))
+    return launch_routed_mm_tc(kQ4_0, x, w, out, n_tokens, top_k, N, K, n_experts, expert_stride, workspace, s);
   MvParams p{};
   p.x = x; p.up = nullptr; p.w = w; p.ids = ids; p.order = hids; p.n_order = offs + n_experts; p.out = out;
   p.n_rows = n_rows; p.top_k = top_k; p.N = N; p.K = K; p.E = n_experts;
@@ -798,9 +796,11 @@ cudaError_t launch_q4_0_mm(const float *x, const uint8_t *w, const uint32_t *ids
 }
 
 // GGML Q8_0 routed matmul (the type is among the routed kernels of quantized_matmul_id_ggml.rs):
-// mat-vec visits routed rows in order; mat-mat routes first (per-expert lists in the
-// workspace) and visits the rows expert by expert, so that the CTAs running at one time
-// share an expert's weights through L2.  Both run the fp32 FMA kernel.
+// mat-vec visits routed rows in order on the fp32 FMA kernel.  Mat-mat routes first
+// (per-expert lists and token blocks in the workspace); with K % 256 == 0 and 16-byte aligned
+// expert slabs it runs the tensor-core kernel of the Q4_0 form with the Q8_0 decode, else it
+// visits the rows expert by expert on the FMA kernel, so that the CTAs running at one time
+// share an expert's weights through L2.
 cudaError_t launch_q8_0_matmul_id(const float *x, const uint8_t *w, const uint32_t *ids, float *out,
                                   int n_tokens, int top_k, int N, int K, int n_experts, uint64_t expert_stride,
                                   bool mm, void *workspace, cudaStream_t s) {
@@ -810,7 +810,7 @@ cudaError_t launch_q8_0_matmul_id(const float *x, const uint8_t *w, const uint32
   p.n_rows = n_rows; p.top_k = top_k; p.N = N; p.K = K; p.E = n_experts;
   p.expert_stride = expert_stride;
   if (mm) {
-    const MoeWorkspace L = moe_workspace_layout(n_rows, 0, n_experts);
+    const MoeWorkspace L = moe_workspace_layout(n_rows, K, n_experts);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     uint32_t *offs = reinterpret_cast<uint32_t *>(ws + L.offs);
     int32_t *hids = reinterpret_cast<int32_t *>(ws + L.hids);
@@ -819,6 +819,8 @@ cudaError_t launch_q8_0_matmul_id(const float *x, const uint8_t *w, const uint32
                                           reinterpret_cast<int4 *>(ws + L.blk),
                                           reinterpret_cast<uint32_t *>(ws + L.n_blk), out, N);
     if (e != cudaSuccess) return e;
+    if (routed_mm_tc_ok(K, expert_stride, w))
+      return launch_routed_mm_tc(kQ8_0, x, w, out, n_tokens, top_k, N, K, n_experts, expert_stride, workspace, s);
     p.order = hids;
     p.n_order = offs + n_experts;
   }
@@ -828,8 +830,8 @@ cudaError_t launch_q8_0_matmul_id(const float *x, const uint8_t *w, const uint32
   return cudaGetLastError();
 }
 
-size_t q8_0_mm_workspace_bytes(int64_t n_tokens, int64_t top_k, int64_t n_experts) {
-  return moe_workspace_layout(n_tokens * top_k, 0, n_experts).total;
+size_t q8_0_mm_workspace_bytes(int64_t n_tokens, int64_t top_k, int64_t K, int64_t n_experts) {
+  return moe_workspace_layout(n_tokens * top_k, K, n_experts).total;
 }
 
 // Dispatch records for the routed mat-vec (quantized_matmul_id_ggml.rs pre-bakes its decode

@@ -1,4 +1,4 @@
-// moe_tc.cu -- GGML Q4_0 expert-routed matmul, mat-mat form, on the tensor cores.
+// moe_tc.cu -- GGML Q4_0 and Q8_0 expert-routed matmul, mat-mat form, on the tensor cores.
 //
 // quantized_matmul_id_ggml.rs (mlx-native 0.9.0): `dispatch_id_mm_for_test` regroups the
 // routed rows per expert (map0) so that a matmul tile reads a single expert's weights and
@@ -9,20 +9,24 @@
 //  2. gather: xs[p] = fp16(2^e_t * x[t]), t = hids[p] / top_k -- the rows of x in routed
 //     order, each token scaled by a power of two that brings its largest magnitude into
 //     [2^14, 2^15) (found once per token by token_scale_kernel);
-//  3. this kernel, persistent over work items (token block, 128-row weight tile):
-//       A = the expert's Q4_0 weight rows, decoded to fp16 by four producer warps from
-//           144-byte TMA boxes (8 blocks of 18 bytes = 256 k per box);
+//  3. routed_mm_tc_kernel<BT>, persistent over work items (token block, 128-row weight tile):
+//       A = the expert's weight rows, decoded to fp16 by four producer warps from TMA boxes of
+//           8 blocks per row (256 k): 144 bytes for Q4_0 (18-byte blocks), 272 for Q8_0
+//           (34-byte blocks);
 //       B = the block's gathered x rows (TMA, 64-row boxes, 128-byte swizzle);
 //       D = 128 weight rows x (rows rounded up to 16) fp32 in tensor memory;
 //     epilogue warps scatter 2^-e_t * D column j to out[hids[p0 + j]][n0 .. n0+127] (fp32).
 //     Each expert's weights stream once from HBM per token block.
 //
-// Operands are fp16 (fp32 accumulation): Q4_0's d is already fp16, so (q - 8) * d is formed
-// with one fp16 multiply (a single rounding of the exact product), and x is rounded from fp32
-// to fp16 once in the gather.  The power-of-two row scaling is exact in both directions, so
-// any finite f32 row is served: its largest element lands near 2^14 (no fp16 overflow, and no
-// fp16 subnormals unless an element is 2^-28 below the row's largest), and the rounding to
-// fp16 is relative to the row's own range.  The mat-vec form rounds x to bf16 instead.
+// Operands are fp16 (fp32 accumulation): the blocks' d is already fp16, so (q - 8) * d (Q4_0)
+// or q * d (Q8_0) is formed with one fp16 multiply (a single rounding of the exact product),
+// and x is rounded from fp32 to fp16 once in the gather.  The power-of-two row scaling is
+// exact in both directions, so any finite f32 row is served: its largest element lands near
+// 2^14 (no fp16 overflow, and no fp16 subnormals unless an element is 2^-28 below the row's
+// largest), and the rounding to fp16 is relative to the row's own range.  A weight whose
+// product leaves fp16's range (|value| >= 65520, possible only for |d| >= 8192 in Q4_0 or
+// >= 512 in Q8_0) is reported as Q4MM_DEVERR_F16_RANGE.  The mat-vec form rounds x to bf16
+// instead.
 #include "tc_common.cuh"
 
 #include <cudaTypedefs.h>
@@ -42,20 +46,32 @@ constexpr uint32_t kTmemCols = 256; // two 128-column accumulators
 constexpr uint32_t kABytes = kTW * kBK * 2;               // 16 KB
 constexpr uint32_t kBBytes = kMoeTokBlock * kBK * 2;      // 16 KB
 constexpr uint32_t kBoxTok = 64;                          // x rows per TMA box
-constexpr uint32_t kRawRow = 144;                         // 8 Q4_0 blocks = 4 K blocks
-constexpr uint32_t kRawBytes = kTW * kRawRow;             // 18 KB
-constexpr int kRawSlots = 4;                              // weight boxes in flight
 
+// Weight boxes: one row of a box is 8 blocks (256 k = 4 K blocks) of one weight row.
+//   Q4_0: 8 x 18 = 144 bytes, copied as 144 uint8 elements; 4 boxes in flight (18 KB each);
+//   Q8_0: 8 x 34 = 272 bytes, copied as 136 uint16 elements (a box row holds at most 256
+//         elements); 2 boxes in flight (34 KB each).
+template <int BT>
+struct RawCfg {
+  static constexpr uint32_t kRow = BT == kQ8_0 ? 272 : 144;
+  static constexpr uint32_t kBoxX = BT == kQ8_0 ? 136 : 144;   // box row in TMA elements
+  static constexpr int kSlots = BT == kQ8_0 ? 2 : 4;
+  static constexpr uint32_t kBytes = kTW * kRow;
+};
+
+template <int BT>
 struct SmemL {
   static constexpr uint32_t a = 0;
   static constexpr uint32_t b = a + kStages * kABytes;
-  static constexpr uint32_t raw = b + kStages * kBBytes;   // [kRawSlots]
-  // full_a, full_b, empty, acc_full[2], acc_empty[2], raw_full[kRawSlots], raw_empty[kRawSlots]
-  static constexpr uint32_t bars = raw + kRawSlots * kRawBytes;
-  static constexpr uint32_t misc = bars + (3 * kStages + 4 + 2 * kRawSlots) * 8;
+  static constexpr uint32_t raw = b + kStages * kBBytes;   // [kSlots]
+  // full_a, full_b, empty, acc_full[2], acc_empty[2], raw_full[kSlots], raw_empty[kSlots]
+  static constexpr uint32_t bars = raw + RawCfg<BT>::kSlots * RawCfg<BT>::kBytes;
+  static constexpr uint32_t misc = bars + (3 * kStages + 4 + 2 * RawCfg<BT>::kSlots) * 8;
   static constexpr uint32_t total = misc + 16;
 };
-constexpr size_t kSmem = SmemL::total + 1024;
+template <int BT>
+constexpr size_t mm_smem_bytes() { return SmemL<BT>::total + 1024; }
+static_assert(mm_smem_bytes<kQ4_0>() <= 227 * 1024 && mm_smem_bytes<kQ8_0>() <= 227 * 1024, "shared memory");
 
 struct MmParams {
   float *out;
@@ -103,22 +119,72 @@ __device__ __forceinline__ uint4 q4_0_chunk(uint32_t word, uint32_t d2) {
   return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
+// Q8_0 qs words m (elements 4m..4m+3) and m + 4 (elements 4m+16..) as one 16-byte chunk of
+// q * d in fp16, in the chunk order above.  (byte ^ 0x80) | 0x6400 is the fp16 value
+// 1024 + (q + 128) for the signed byte q; subtracting 1152 gives q exactly, and the product
+// with d is rounded once.  The mask keeps bytes 0 and 2 (or 1 and 3 after the shift), the
+// pairs (4m, 4m+2) and (4m+1, 4m+3).
+__device__ __forceinline__ uint4 q8_0_chunk(uint32_t lo, uint32_t hi, uint32_t d2) {
+  constexpr uint32_t kMask = 0x00FF00FFu, kFlip = 0x64806480u;   // 0x80 on each byte, exponent bits of 1024
+  const uint32_t c[4] = {(lo & kMask) ^ kFlip, ((lo >> 8) & kMask) ^ kFlip, (hi & kMask) ^ kFlip,
+                         ((hi >> 8) & kMask) ^ kFlip};
+  uint32_t r[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t q;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(q) : "r"(c[i]), "r"(kFlip));   // 0x6480 is 1152
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r[i]) : "r"(q), "r"(d2));
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// Either half of an f16x2 word is infinite or NaN.
+__device__ __forceinline__ bool f16x2_nonfinite(uint32_t v) {
+  return (v & 0x7C00u) == 0x7C00u || (v & 0x7C000000u) == 0x7C000000u;
+}
+__device__ __forceinline__ bool chunk_nonfinite(uint4 c) {
+  return f16x2_nonfinite(c.x) || f16x2_nonfinite(c.y) || f16x2_nonfinite(c.z) || f16x2_nonfinite(c.w);
+}
+
+// The nine 32-bit words of Q8_0 block 2 kk + H of every K block kk from a 272-byte box row:
+// block 2kk + H starts at byte 68 kk + 34 H, so H = 0 takes words 17kk .. 17kk + 8 (d in the
+// low half of the first) and H = 1 words 17kk + 8 .. 17kk + 16 (d in the high half of the
+// first).  Only the 16-byte pieces that hold them are read.
+template <int H>
+__device__ __forceinline__ void q8_0_box_words(const uint4 *row, uint32_t (&u)[4][9]) {
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+      const int w = 17 * kk + 8 * H + i;
+      const uint4 c = row[w >> 2];
+      const int j = w & 3;
+      u[kk][i] = j == 0 ? c.x : j == 1 ? c.y : j == 2 ? c.z : c.w;
+    }
+  }
+}
+
+template <int BT>
 __global__ void __launch_bounds__(kThreads, 1)
-    q4_0_mm_tc_kernel(const __grid_constant__ MmMaps maps, const __grid_constant__ MmParams p) {
+    routed_mm_tc_kernel(const __grid_constant__ MmMaps maps, const __grid_constant__ MmParams p) {
+  using L = SmemL<BT>;
+  constexpr int kRawSlots = RawCfg<BT>::kSlots;
+  constexpr uint32_t kRawBytes = RawCfg<BT>::kBytes;
+  constexpr uint32_t kRawRow = RawCfg<BT>::kRow;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
   uint8_t *smem = smem_raw + (base - raw_base);
-  const uint32_t sA = base + SmemL::a, sB = base + SmemL::b, sR = base + SmemL::raw;
-  const uint32_t bar_full_a = base + SmemL::bars;
+  const uint32_t sA = base + L::a, sB = base + L::b, sR = base + L::raw;
+  const uint32_t bar_full_a = base + L::bars;
   const uint32_t bar_full_b = bar_full_a + kStages * 8;
   const uint32_t bar_empty = bar_full_b + kStages * 8;
   const uint32_t bar_acc_full = bar_empty + kStages * 8;
   const uint32_t bar_acc_empty = bar_acc_full + 16;
   const uint32_t bar_raw_full = bar_acc_empty + 16;
   const uint32_t bar_raw_empty = bar_raw_full + 8 * kRawSlots;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SmemL::misc);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SmemL::misc + 4);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::misc + 4);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int KB = p.K / kBK;                 // multiple of 4
@@ -157,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 14) {
-    // ---------------- weight TMA: one 144-byte x 128-row box per 4 K blocks ----------------
+    // ---------------- weight TMA: one 128-row box per 4 K blocks ----------------
     // Runs ahead of the MMA by up to kRawSlots boxes, independently of the x stages.
     if (lane == 0) {
       int raw_issued = 0;
@@ -180,7 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slot = q % kRawSlots;
         if (!tc::mbar_wait(bar_raw_empty + 8 * slot, ((q / kRawSlots) & 1) ^ 1, abort_flag)) break;
         tc::mbar_arrive_expect_tx(bar_raw_full + 8 * slot, kRawBytes);
-        tma_load_3d(sR + slot * kRawBytes, &maps.w, bq * (int)kRawRow, n0, e, bar_raw_full + 8 * slot);
+        tma_load_3d(sR + slot * kRawBytes, &maps.w, bq * (int)RawCfg<BT>::kBoxX, n0, e,
+                    bar_raw_full + 8 * slot);
         ++raw_issued;
         ++bq;
       }
@@ -253,25 +320,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < 10) {
-    // ---------------- Q4_0 decode producers: thread (row, half) ----------------
-    // A row's 144-byte box (4 K blocks = 8 Q4_0 blocks) is read once with nine 16-byte loads
-    // (the 144-byte row stride puts 8 consecutive rows on distinct bank quads); thread half h
-    // then decodes block 2*kk + h of K block kk into chunks 4h .. 4h+3 of the bf16 row.
+    // ---------------- decode producers: thread (row, half) ----------------
+    // A row of a weight box (4 K blocks = 8 blocks) is read once into registers (Q4_0: nine
+    // 16-byte loads; the 144- and 272-byte row strides put 8 consecutive rows on distinct bank
+    // quads); thread half h then decodes block 2*kk + h of K block kk into chunks 4h .. 4h+3 of
+    // the fp16 row.  half is uniform within a warp (warps 2-5: 0, warps 6-9: 1).
+    // A block whose d is large enough for a product to leave fp16's range (|d| >= 8192 for
+    // Q4_0, >= 512 for Q8_0) has its products checked; an infinite one is reported.
+    constexpr uint32_t kBigD = BT == kQ8_0 ? 0x6000u : 0x7000u;   // fp16 bits of 512 / 8192
     const int pt = threadIdx.x - 64;          // 0..255
     const int tp = pt & (kTW - 1), half = pt >> 7;
     const int boxes_per_item = KB / 4;
-    bool ok = true;
+    bool ok = true, range = false;
     for (int q = 0; q < my_items * boxes_per_item && ok; ++q) {
       const int slot = q % kRawSlots;
       if (!tc::mbar_wait(bar_raw_full + 8 * slot, (q / kRawSlots) & 1, abort_flag, 100)) break;
+      const uint4 *row = reinterpret_cast<const uint4 *>(smem + L::raw + slot * kRawBytes + tp * kRawRow);
+      // v: Q4_0, the whole 144-byte row; Q8_0, the nine words of this thread's block per K block
       uint32_t v[36];
-      {
-        const uint4 *row = reinterpret_cast<const uint4 *>(smem + SmemL::raw + slot * kRawBytes + tp * kRawRow);
+      if constexpr (BT == kQ4_0) {
 #pragma unroll
         for (int m = 0; m < 9; ++m) {
           const uint4 r4 = row[m];
           v[4 * m] = r4.x; v[4 * m + 1] = r4.y; v[4 * m + 2] = r4.z; v[4 * m + 3] = r4.w;
         }
+      } else {
+        uint32_t u[4][9];
+        if (half == 0) q8_0_box_words<0>(row, u);
+        else q8_0_box_words<1>(row, u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+          for (int i = 0; i < 9; ++i) v[9 * kk + i] = u[kk][i];
       }
       tc::mbar_arrive(bar_raw_empty + 8 * slot);   // registers hold the box now
 #pragma unroll
@@ -279,29 +359,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = q * 4 + kk;                 // pipeline step (K block)
         const int s = j % kStages;
         const uint32_t ph = (j / kStages) & 1;
-        // block 2kk+half: 18 bytes at byte 36kk + 18 half
-        uint32_t qs[4], d2;
-        if (half == 0) {
-          const uint32_t *u = v + 9 * kk;
+        constexpr int kQsWords = BT == kQ8_0 ? 8 : 4;
+        uint32_t qs[kQsWords], d2;
+        if constexpr (BT == kQ4_0) {
+          // block 2kk+half: 18 bytes at byte 36kk + 18 half
+          if (half == 0) {
+            const uint32_t *u = v + 9 * kk;
 #pragma unroll
-          for (int m = 0; m < 4; ++m) qs[m] = prmt(u[m], u[m + 1], 0x5432u);
-          d2 = (u[0] & 0xFFFFu) | (u[0] << 16);
+            for (int m = 0; m < 4; ++m) qs[m] = prmt(u[m], u[m + 1], 0x5432u);
+            d2 = (u[0] & 0xFFFFu) | (u[0] << 16);
+          } else {
+            const uint32_t *u = v + 9 * kk + 4;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) qs[m] = u[1 + m];
+            d2 = (u[0] >> 16) | (u[0] & 0xFFFF0000u);
+          }
         } else {
-          const uint32_t *u = v + 9 * kk + 4;
+          // block 2kk+half: 34 bytes at byte 68kk + 34 half; v + 9kk holds its words
+          const uint32_t *u = v + 9 * kk;
+          if (half == 0) {
 #pragma unroll
-          for (int m = 0; m < 4; ++m) qs[m] = u[1 + m];
-          d2 = (u[0] >> 16) | (u[0] & 0xFFFF0000u);
+            for (int m = 0; m < 8; ++m) qs[m] = prmt(u[m], u[m + 1], 0x5432u);
+            d2 = (u[0] & 0xFFFFu) | (u[0] << 16);
+          } else {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) qs[m] = u[1 + m];
+            d2 = (u[0] >> 16) | (u[0] & 0xFFFF0000u);
+          }
         }
+        const bool big = (d2 & 0x7FFFu) >= kBigD;
         if (!tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, 100)) { ok = false; break; }
-        uint8_t *a_tile = smem + SmemL::a + s * kABytes;
+        uint8_t *a_tile = smem + L::a + s * kABytes;
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
-          *reinterpret_cast<uint4 *>(a_tile + tc::sw128_offset((uint32_t)tp, (uint32_t)(4 * half + m))) =
-              q4_0_chunk(qs[m], d2);
+        for (int m = 0; m < 4; ++m) {
+          uint4 c;
+          if constexpr (BT == kQ4_0) c = q4_0_chunk(qs[m], d2);
+          else c = q8_0_chunk(qs[m], qs[m + 4], d2);
+          if (big) range |= chunk_nonfinite(c);
+          *reinterpret_cast<uint4 *>(a_tile + tc::sw128_offset((uint32_t)tp, (uint32_t)(4 * half + m))) = c;
+        }
         tc::fence_proxy_async_smem();
         tc::mbar_arrive(bar_full_a + 8 * s);
       }
     }
+    if (range) raise_device_error(Q4MM_DEVERR_F16_RANGE);
   } else {
     // ---------------- epilogue: TMEM -> out rows (fp32) ----------------
     const int quarter = warp & 3;
@@ -428,8 +529,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-cudaError_t launch_q4_0_mm_tc(const float *x, const uint8_t *w, float *out, int n_tokens, int top_k, int N,
-                              int K, int n_experts, uint64_t expert_stride, void *workspace, cudaStream_t s) {
+cudaError_t launch_routed_mm_tc(int bt, const float *x, const uint8_t *w, float *out, int n_tokens, int top_k,
+                                int N, int K, int n_experts, uint64_t expert_stride, void *workspace, cudaStream_t s) {
+  if (bt != kQ4_0 && bt != kQ8_0) return cudaErrorInvalidValue;
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const int n_rows = n_tokens * top_k;
@@ -449,14 +551,20 @@ cudaError_t launch_q4_0_mm_tc(const float *x, const uint8_t *w, float *out, int 
   if (e != cudaSuccess) return e;
 
   MmMaps maps;
-  const uint64_t row_bytes = (uint64_t)(K / 32) * 18;
+  const bool q8 = bt == kQ8_0;
+  const uint64_t row_bytes = (uint64_t)(K / 32) * (q8 ? 34 : 18);
   {
-    cuuint64_t dims[3] = {(cuuint64_t)row_bytes, (cuuint64_t)N, (cuuint64_t)n_experts};
+    // Q4_0 rows as uint8 elements (144-element box rows), Q8_0 rows as uint16 elements
+    // (136-element box rows: 272 uint8 elements would exceed the 256-element limit of a box
+    // dimension)
+    const uint64_t esz = q8 ? 2 : 1;
+    cuuint64_t dims[3] = {(cuuint64_t)(row_bytes / esz), (cuuint64_t)N, (cuuint64_t)n_experts};
     cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)expert_stride};
-    cuuint32_t box[3] = {kRawRow, (cuuint32_t)kTW, 1};
+    cuuint32_t box[3] = {q8 ? RawCfg<kQ8_0>::kBoxX : RawCfg<kQ4_0>::kBoxX, (cuuint32_t)kTW, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    if (enc(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(w), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    if (enc(&maps.w, q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+            const_cast<uint8_t *>(w), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -478,9 +586,15 @@ cudaError_t launch_q4_0_mm_tc(const float *x, const uint8_t *w, float *out, int 
   p.n_blk = reinterpret_cast<const uint32_t *>(ws + L.n_blk);
   p.N = N;
   p.K = K;
-  e = cudaFuncSetAttribute(q4_0_mm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
-  if (e != cudaSuccess) return e;
-  q4_0_mm_tc_kernel<<<(unsigned)sms, kThreads, kSmem, s>>>(maps, p);
+  if (q8) {
+    e = ensure_dynamic_smem(reinterpret_cast<const void *>(routed_mm_tc_kernel<kQ8_0>), (int)mm_smem_bytes<kQ8_0>());
+    if (e != cudaSuccess) return e;
+    routed_mm_tc_kernel<kQ8_0><<<(unsigned)sms, kThreads, mm_smem_bytes<kQ8_0>(), s>>>(maps, p);
+  } else {
+    e = ensure_dynamic_smem(reinterpret_cast<const void *>(routed_mm_tc_kernel<kQ4_0>), (int)mm_smem_bytes<kQ4_0>());
+    if (e != cudaSuccess) return e;
+    routed_mm_tc_kernel<kQ4_0><<<(unsigned)sms, kThreads, mm_smem_bytes<kQ4_0>(), s>>>(maps, p);
+  }
   return cudaGetLastError();
 }
 

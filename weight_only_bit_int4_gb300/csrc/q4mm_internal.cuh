@@ -270,7 +270,11 @@ cudaError_t ensure_dynamic_smem(const void *fn, int bytes);
 cudaError_t launch_q8_0_matmul_id(const float *x, const uint8_t *w, const uint32_t *ids, float *out,
                                   int n_tokens, int top_k, int N, int K, int n_experts, uint64_t expert_stride,
                                   bool mm, void *workspace, cudaStream_t s);
-size_t q8_0_mm_workspace_bytes(int64_t n_tokens, int64_t top_k, int64_t n_experts);
+size_t q8_0_mm_workspace_bytes(int64_t n_tokens, int64_t top_k, int64_t K, int64_t n_experts);
+
+// Block types of the routed kernels: GGML Q4_0 (18 bytes: fp16 d, 16 bytes of nibbles) and
+// Q8_0 (34 bytes: fp16 d, 32 signed bytes).
+constexpr int kQ4_0 = 0, kQ8_0 = 1;
 
 // Routed-row count check: n_tokens and top_k are each bounded before their product is
 // formed, so a huge top_k cannot overflow int64 and wrap past the 2^24 limit.
@@ -317,8 +321,14 @@ inline MoeWorkspace moe_workspace_layout(int64_t n_rows, int64_t K, int64_t E) {
 
 cudaError_t launch_q4_0_route_blocks(const uint32_t *ids, int n_rows, int n_experts, void *workspace,
                                      cudaStream_t s);
-cudaError_t launch_q4_0_mm_tc(const float *x, const uint8_t *w, float *out, int n_tokens, int top_k,
-                              int N, int K, int n_experts, uint64_t expert_stride, void *workspace,
-                              cudaStream_t s);
+// The tensor-core mat-mat form (after routing) takes whole 256-element TMA boxes of blocks
+// (K % 256 == 0) from 16-byte aligned expert slabs.
+inline bool routed_mm_tc_ok(int K, uint64_t expert_stride, const void *w) {
+  return K % 256 == 0 && expert_stride % 16 == 0 && (reinterpret_cast<uintptr_t>(w) & 15) == 0;
+}
+// bt: kQ4_0 or kQ8_0.  The workspace must already hold the routing (launch_route_internal).
+cudaError_t launch_routed_mm_tc(int bt, const float *x, const uint8_t *w, float *out, int n_tokens, int top_k,
+                                int N, int K, int n_experts, uint64_t expert_stride, void *workspace,
+                                cudaStream_t s);
 
 }  // namespace q4mm
