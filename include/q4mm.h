@@ -59,13 +59,14 @@ typedef enum q4mm_dtype { Q4MM_F32 = 0, Q4MM_BF16 = 1, Q4MM_F16 = 2 } q4mm_dtype
 /* Bits of the device error word. */
 #define Q4MM_DEVERR_WAIT_TIMEOUT 0x1u  /* a pipeline wait gave up; that output is invalid */
 #define Q4MM_DEVERR_BAD_EXPERT 0x2u    /* an id >= n_experts was routed (its row is zero) */
-#define Q4MM_DEVERR_F16_RANGE 0x4u     /* a tensor-core mat-mat form (Q4_0, Q8_0) met a weight
-                                          whose dequantised value (q-8)*d or q*d is beyond
-                                          fp16's range (|value| >= 65520, only possible for
-                                          |d| >= 8192 in Q4_0, >= 512 in Q8_0); the outputs
-                                          that weight feeds are not finite.  x itself is
-                                          never out of range: each gathered row is scaled
-                                          by a power of two. */
+#define Q4MM_DEVERR_F16_RANGE 0x4u     /* a tensor-core mat-mat form (Q4_0, Q8_0), which
+                                          forms each weight (q-8)*d or q*d in fp16, met a
+                                          block whose |d| could take a weight beyond fp16's
+                                          range (|d| >= 8192 for Q4_0, >= 512 for Q8_0).  The
+                                          outputs that block feeds are correct if all of its
+                                          weights stay below 65520 in magnitude, else not
+                                          finite.  x itself is never out of range: each
+                                          gathered row is scaled by a power of two. */
 
 /* Static string for a status code (never NULL). */
 const char *q4mm_status_string(int status);

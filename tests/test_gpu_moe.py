@@ -319,9 +319,12 @@ def test_q8_0_mm_any_f32_row_range():
 
 # ---------------------------------------------------------------------------------------
 # Weights near the end of fp16's range in the tensor-core mat-mat forms, which form each
-# dequantised weight as one fp16 product.  A large d whose products all stay finite is served
-# without a flag; a block with a product beyond fp16 (|value| >= 65520) raises
-# Q4MM_DEVERR_F16_RANGE, and only the outputs that block feeds are affected.
+# dequantised weight as one fp16 product.  Q4MM_DEVERR_F16_RANGE is raised for every block
+# whose d could give a product beyond fp16 (|d| >= 8192 for Q4_0, >= 512 for Q8_0):
+#   "edge":     the largest d below that bound with the extreme code: finite, no flag;
+#   "flagged":  a d above the bound whose codes all stay finite: flagged, outputs correct;
+#   "overflow": a d above the bound with a code beyond fp16: flagged, and only the outputs
+#               that block feeds are not finite.
 # ---------------------------------------------------------------------------------------
 
 def _set_block(w, stride, K, bbytes, e, n, b, d, qs):
@@ -331,24 +334,28 @@ def _set_block(w, stride, K, bbytes, e, n, b, d, qs):
 
 
 @pytest.mark.parametrize("bt", ["q4_0", "q8_0"])
-@pytest.mark.parametrize("overflow", [False, True])
-def test_mm_weight_range(bt, overflow):
+@pytest.mark.parametrize("case", ["edge", "flagged", "overflow"])
+def test_mm_weight_range(bt, case):
     n_tokens, top_k, E, N, K = 64, 2, 4, 128, 512
     rng = np.random.default_rng(91)
     if bt == "q4_0":
         x, w, stride, ids = _moe_case(4400, n_tokens, top_k, E, N, K)
-        d = 9000.0                                        # 7 d = 63000 is finite, 8 d is not
+        # 8 * 8188 = 65504 is fp16's largest finite value; 7 * 9000 = 63000 is finite, 8 * 9000 is not
+        d = 8188.0 if case == "edge" else 9000.0
         nib = rng.integers(1, 16, 32).astype(np.uint8)    # q - 8 in [-7, 7]
-        if overflow:
-            nib[0] = 0                                    # q - 8 = -8: -72000
+        if case != "flagged":
+            nib[0] = 0                                    # q - 8 = -8
         qs = (nib[:16] | (nib[16:] << 4)).astype(np.uint8)
         bbytes, run, ref_fn = 18, _run, oracle.q4_0_matmul_id
     else:
         x, w, stride, ids = _q8_case(4500, n_tokens, top_k, E, N, K)
-        d = 600.0                                         # 100 d = 60000 is finite, 127 d is not
+        # 128 * 511.75 = 65504; 100 * 600 = 60000 is finite, 127 * 600 is not
+        d = 511.75 if case == "edge" else 600.0
         qv = rng.integers(-100, 101, 32)
-        if overflow:
-            qv[7] = 127                                   # 76200
+        if case == "edge":
+            qv[7] = -128
+        elif case == "overflow":
+            qv[7] = 127
         qs = qv.astype(np.int8).view(np.uint8)
         bbytes, run, ref_fn = 34, _run_q8, oracle.q8_0_matmul_id
     w = w.copy()
@@ -361,11 +368,9 @@ def test_mm_weight_range(bt, overflow):
     fed = np.zeros(got.shape, bool)
     fed[np.nonzero(ids == e_big)[0], n_big] = True
     assert fed.any()
-    if overflow:
-        assert err & 0x4
+    assert bool(err & 0x4) == (case != "edge")
+    if case == "overflow":
         assert not np.any(np.isfinite(got[fed]))
-        assert_within_tolerance(got[~fed], ref[~fed], f"{bt} outputs the block does not feed")
     else:
-        assert err == 0
-        assert_within_tolerance(got[fed], ref[fed], f"{bt} outputs of the large finite weights")
-        assert_within_tolerance(got[~fed], ref[~fed], f"{bt} other outputs")
+        assert_within_tolerance(got[fed], ref[fed], f"{bt} outputs of the large weights ({case})")
+    assert_within_tolerance(got[~fed], ref[~fed], f"{bt} other outputs ({case})")

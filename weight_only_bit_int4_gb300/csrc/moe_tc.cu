@@ -23,10 +23,14 @@
 // and x is rounded from fp32 to fp16 once in the gather.  The power-of-two row scaling is
 // exact in both directions, so any finite f32 row is served: its largest element lands near
 // 2^14 (no fp16 overflow, and no fp16 subnormals unless an element is 2^-28 below the row's
-// largest), and the rounding to fp16 is relative to the row's own range.  A weight whose
-// product leaves fp16's range (|value| >= 65520, possible only for |d| >= 8192 in Q4_0 or
-// >= 512 in Q8_0) is reported as Q4MM_DEVERR_F16_RANGE.  The mat-vec form rounds x to bf16
-// instead.
+// largest), and the rounding to fp16 is relative to the row's own range.  A block whose d
+// could take a weight beyond fp16's range (|value| >= 65520: |d| >= 8192 in Q4_0, >= 512 in
+// Q8_0) is reported as Q4MM_DEVERR_F16_RANGE.  The mat-vec form rounds x to bf16 instead.
+//
+// Pipeline: two stages of two 64-k tiles each (A and B).  The producers publish a stage on
+// full_a once their A tiles are written and the stage's B tiles (TMA) have landed, so the
+// single MMA thread waits on one barrier and commits once per 128 k: its per-stage waits,
+// fences and commits, not the tensor core, had set the pace at one barrier pair per 64 k.
 #include "tc_common.cuh"
 
 #include <cudaTypedefs.h>
@@ -38,8 +42,10 @@ Q4MM_DEFINE_ERROR_READER(read_errors_moe_tc)
 namespace {
 
 constexpr int kTW = 128;            // weight rows per tile (MMA M)
-constexpr int kBK = 64;             // K per pipeline stage
-constexpr int kStages = 4;
+constexpr int kBK = 64;             // K per tile (one 128-byte swizzle atom of fp16)
+constexpr int kKps = 2;             // K tiles per pipeline stage (one barrier phase)
+constexpr int kStages = 2;          // pipeline stages
+constexpr int kTiles = kKps * kStages;
 constexpr int kThreads = 480;       // warp 0 x TMA, 1 MMA, 2-9 producers, 10-13 epilogue, 14 weight TMA
 constexpr int kProducers = 256;     // two threads per weight row, one Q4_0 block each per K block
 constexpr uint32_t kTmemCols = 256; // two 128-column accumulators
@@ -62,8 +68,8 @@ struct RawCfg {
 template <int BT>
 struct SmemL {
   static constexpr uint32_t a = 0;
-  static constexpr uint32_t b = a + kStages * kABytes;
-  static constexpr uint32_t raw = b + kStages * kBBytes;   // [kSlots]
+  static constexpr uint32_t b = a + kTiles * kABytes;
+  static constexpr uint32_t raw = b + kTiles * kBBytes;    // [kSlots]
   // full_a, full_b, empty, acc_full[2], acc_empty[2], raw_full[kSlots], raw_empty[kSlots]
   static constexpr uint32_t bars = raw + RawCfg<BT>::kSlots * RawCfg<BT>::kBytes;
   static constexpr uint32_t misc = bars + (3 * kStages + 4 + 2 * RawCfg<BT>::kSlots) * 8;
@@ -138,14 +144,6 @@ __device__ __forceinline__ uint4 q8_0_chunk(uint32_t lo, uint32_t hi, uint32_t d
   return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-// Either half of an f16x2 word is infinite or NaN.
-__device__ __forceinline__ bool f16x2_nonfinite(uint32_t v) {
-  return (v & 0x7C00u) == 0x7C00u || (v & 0x7C000000u) == 0x7C000000u;
-}
-__device__ __forceinline__ bool chunk_nonfinite(uint4 c) {
-  return f16x2_nonfinite(c.x) || f16x2_nonfinite(c.y) || f16x2_nonfinite(c.z) || f16x2_nonfinite(c.w);
-}
-
 // The nine 32-bit words of Q8_0 block 2 kk + H of every K block kk from a 272-byte box row:
 // block 2kk + H starts at byte 68 kk + 34 H, so H = 0 takes words 17kk .. 17kk + 8 (d in the
 // low half of the first) and H = 1 words 17kk + 8 .. 17kk + 16 (d in the high half of the
@@ -188,10 +186,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int KB = p.K / kBK;                 // multiple of 4
+  const int KJ = KB / kKps;                 // stages per item
   const int n_tiles = (p.N + kTW - 1) / kTW;
   const int items = (int)*p.n_blk * n_tiles;
   const int my_items = (int)blockIdx.x < items ? (items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  const int steps = my_items * KB;
+  const int steps = my_items * KJ;          // stages of this CTA
   auto item_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
 
   if (threadIdx.x == 0) {
@@ -262,12 +261,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- x TMA: the block's gathered rows, every K block ----------------
     if (lane == 0) {
       int issued = 0;
-      int i = 0, kb = 0;
+      int i = 0, jb = 0;
       int4 bi = my_items > 0 ? p.blk[item_of(0) / n_tiles] : make_int4(0, 0, 0, 0);
       int4 bnext = my_items > 1 ? p.blk[item_of(1) / n_tiles] : bi;   // one item ahead
-      for (int j = 0; j < steps; ++j, ++kb) {
-        if (kb == KB) {
-          kb = 0;
+      for (int j = 0; j < steps; ++j, ++jb) {
+        if (jb == KJ) {
+          jb = 0;
           ++i;
           bi = bnext;
           if (i + 1 < my_items) bnext = p.blk[item_of(i + 1) / n_tiles];
@@ -276,10 +275,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = (j / kStages) & 1;
         if (!tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag)) break;
         const int boxes = (bi.z + (int)kBoxTok - 1) / (int)kBoxTok;
-        tc::mbar_arrive_expect_tx(bar_full_b + 8 * s, (uint32_t)boxes * kBoxTok * kBK * 2);
-        for (int bx = 0; bx < boxes; ++bx)
-          tc::tma_load_2d(sB + s * kBBytes + bx * kBoxTok * kBK * 2, &maps.xs, kb * kBK, bi.y + bx * (int)kBoxTok,
-                          bar_full_b + 8 * s);
+        tc::mbar_arrive_expect_tx(bar_full_b + 8 * s, (uint32_t)(kKps * boxes) * kBoxTok * kBK * 2);
+        for (int h = 0; h < kKps; ++h)
+          for (int bx = 0; bx < boxes; ++bx)
+            tc::tma_load_2d(sB + (s * kKps + h) * kBBytes + bx * kBoxTok * kBK * 2, &maps.xs, (jb * kKps + h) * kBK,
+                            bi.y + bx * (int)kBoxTok, bar_full_b + 8 * s);
         ++issued;
       }
       if (*abort_flag) {
@@ -303,17 +303,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc::tc_fence_after();
         const uint32_t dtm = tmem + (uint32_t)(ab * kMoeTokBlock);
-        for (int kb = 0; kb < KB; ++kb) {
-          const int j = i * KB + kb, s = j % kStages;
+        for (int jb = 0; jb < KJ; ++jb) {
+          const int j = i * KJ + jb, s = j % kStages;
           const uint32_t ph = (j / kStages) & 1;
-          ok = tc::mbar_wait(bar_full_a + 8 * s, ph, abort_flag, 100) &&
-               tc::mbar_wait(bar_full_b + 8 * s, ph, abort_flag, 100);
+          ok = tc::mbar_wait(bar_full_a + 8 * s, ph, abort_flag, 100);
           if (!ok) break;
           tc::tc_fence_after();
-          const uint64_t ad = tc::smem_desc_sw128(sA + s * kABytes);
-          const uint64_t bd = tc::smem_desc_sw128(sB + s * kBBytes);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) tc::mma_bf16(dtm, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+          for (int h = 0; h < kKps; ++h) {
+            const uint64_t ad = tc::smem_desc_sw128(sA + (s * kKps + h) * kABytes);
+            const uint64_t bd = tc::smem_desc_sw128(sB + (s * kKps + h) * kBBytes);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              tc::mma_bf16(dtm, ad + 2 * k, bd + 2 * k, idesc, (jb | h | k) != 0);
+          }
           tc::mma_commit(bar_empty + 8 * s);
         }
         if (ok) tc::mma_commit(bar_acc_full + 8 * ab);
@@ -325,13 +328,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 16-byte loads; the 144- and 272-byte row strides put 8 consecutive rows on distinct bank
     // quads); thread half h then decodes block 2*kk + h of K block kk into chunks 4h .. 4h+3 of
     // the fp16 row.  half is uniform within a warp (warps 2-5: 0, warps 6-9: 1).
-    // A block whose d is large enough for a product to leave fp16's range (|d| >= 8192 for
-    // Q4_0, >= 512 for Q8_0) has its products checked; an infinite one is reported.
+    // The largest |d| a thread decodes is tracked (fp16 bit patterns of non-negative values
+    // order like the values); one at or above 8192 (Q4_0) or 512 (Q8_0), where a code can give
+    // a product beyond fp16's range, is reported once at the end.
     constexpr uint32_t kBigD = BT == kQ8_0 ? 0x6000u : 0x7000u;   // fp16 bits of 512 / 8192
     const int pt = threadIdx.x - 64;          // 0..255
     const int tp = pt & (kTW - 1), half = pt >> 7;
     const int boxes_per_item = KB / 4;
-    bool ok = true, range = false;
+    bool ok = true;
+    uint32_t dmax = 0;
     for (int q = 0; q < my_items * boxes_per_item && ok; ++q) {
       const int slot = q % kRawSlots;
       if (!tc::mbar_wait(bar_raw_full + 8 * slot, (q / kRawSlots) & 1, abort_flag, 100)) break;
@@ -356,7 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_arrive(bar_raw_empty + 8 * slot);   // registers hold the box now
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        const int j = q * 4 + kk;                 // pipeline step (K block)
+        const int kbt = q * 4 + kk;               // K tile of this CTA's sequence
+        const int j = kbt / kKps, h = kbt % kKps;  // pipeline stage, tile within it
         const int s = j % kStages;
         const uint32_t ph = (j / kStages) & 1;
         constexpr int kQsWords = BT == kQ8_0 ? 8 : 4;
@@ -387,22 +393,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             d2 = (u[0] >> 16) | (u[0] & 0xFFFF0000u);
           }
         }
-        const bool big = (d2 & 0x7FFFu) >= kBigD;
-        if (!tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, 100)) { ok = false; break; }
-        uint8_t *a_tile = smem + L::a + s * kABytes;
+        dmax = max(dmax, d2 & 0x7FFFu);
+        if (h == 0 && !tc::mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, 100)) { ok = false; break; }
+        uint8_t *a_tile = smem + L::a + (s * kKps + h) * kABytes;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
           uint4 c;
           if constexpr (BT == kQ4_0) c = q4_0_chunk(qs[m], d2);
           else c = q8_0_chunk(qs[m], qs[m + 4], d2);
-          if (big) range |= chunk_nonfinite(c);
           *reinterpret_cast<uint4 *>(a_tile + tc::sw128_offset((uint32_t)tp, (uint32_t)(4 * half + m))) = c;
         }
-        tc::fence_proxy_async_smem();
-        tc::mbar_arrive(bar_full_a + 8 * s);
+        if (h == kKps - 1) {
+          // The stage's B tiles have landed too once full_a completes: every producer waits
+          // for them before its arrival, so the MMA issuer waits on one barrier per stage.
+          tc::fence_proxy_async_smem();
+          if (!tc::mbar_wait(bar_full_b + 8 * s, ph, abort_flag, 100)) { ok = false; break; }
+          tc::mbar_arrive(bar_full_a + 8 * s);
+        }
       }
     }
-    if (range) raise_device_error(Q4MM_DEVERR_F16_RANGE);
+    if (dmax >= kBigD) raise_device_error(Q4MM_DEVERR_F16_RANGE);
   } else {
     // ---------------- epilogue: TMEM -> out rows (fp32) ----------------
     const int quarter = warp & 3;
