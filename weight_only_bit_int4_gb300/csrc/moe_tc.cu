@@ -5,7 +5,7 @@
 // reuses them across that expert's routed rows instead of re-reading them per row.  Here:
 //
 //  1. routing (moe.cu): per-expert counts, ascending row lists, and a list of token blocks
-//     of <= 128 rows, each inside one expert;
+//     of <= kMoeTokBlock (112) rows, each inside one expert;
 //  2. gather: xs[p] = fp16(2^e_t * x[t]), t = hids[p] / top_k -- the rows of x in routed
 //     order, each token scaled by a power of two that brings its largest magnitude into
 //     [2^14, 2^15) (found once per token by token_scale_kernel);
@@ -44,35 +44,38 @@ namespace {
 constexpr int kTW = 128;            // weight rows per tile (MMA M)
 constexpr int kBK = 64;             // K per tile (one 128-byte swizzle atom of fp16)
 constexpr int kKps = 2;             // K tiles per pipeline stage (one barrier phase)
-constexpr int kStages = 2;          // pipeline stages
-constexpr int kTiles = kKps * kStages;
 constexpr int kThreads = 480;       // warp 0 x TMA, 1 MMA, 2-9 producers, 10-13 epilogue, 14 weight TMA
 constexpr int kProducers = 256;     // two threads per weight row, one Q4_0 block each per K block
-constexpr uint32_t kTmemCols = 256; // two 128-column accumulators
+constexpr uint32_t kTmemCols = 256; // two accumulators of kAccCols columns
 constexpr uint32_t kABytes = kTW * kBK * 2;               // 16 KB
-constexpr uint32_t kBBytes = kMoeTokBlock * kBK * 2;      // 16 KB
-constexpr uint32_t kBoxTok = 64;                          // x rows per TMA box
+constexpr uint32_t kBBytes = kMoeTokBlock * kBK * 2;      // 14 KB (112 token rows)
+constexpr uint32_t kBoxTok = kMoeTokBlock / 2;            // x rows per TMA box (56: whole 8-row swizzle atoms)
+constexpr uint32_t kAccCols = 128;                        // TMEM columns per accumulator (>= kMoeTokBlock)
+static_assert(kBBytes % 1024 == 0 && kBoxTok % 8 == 0 && kMoeTokBlock <= (int)kAccCols, "B tile layout");
 
 // Weight boxes: one row of a box is 8 blocks (256 k = 4 K blocks) of one weight row.
-//   Q4_0: 8 x 18 = 144 bytes, copied as 144 uint8 elements; 4 boxes in flight (18 KB each);
+//   Q4_0: 8 x 18 = 144 bytes, copied as 144 uint8 elements; 2 boxes in flight (18 KB each);
 //   Q8_0: 8 x 34 = 272 bytes, copied as 136 uint16 elements (a box row holds at most 256
 //         elements); 2 boxes in flight (34 KB each).
+// Pipeline stages (kKps A and B tiles each): 3 for Q4_0, 2 for Q8_0 (its boxes take the room).
 template <int BT>
 struct RawCfg {
   static constexpr uint32_t kRow = BT == kQ8_0 ? 272 : 144;
   static constexpr uint32_t kBoxX = BT == kQ8_0 ? 136 : 144;   // box row in TMA elements
-  static constexpr int kSlots = BT == kQ8_0 ? 2 : 4;
+  static constexpr int kSlots = 2;
   static constexpr uint32_t kBytes = kTW * kRow;
+  static constexpr int kStages = BT == kQ8_0 ? 2 : 3;
 };
 
 template <int BT>
 struct SmemL {
   static constexpr uint32_t a = 0;
+  static constexpr int kTiles = kKps * RawCfg<BT>::kStages;
   static constexpr uint32_t b = a + kTiles * kABytes;
   static constexpr uint32_t raw = b + kTiles * kBBytes;    // [kSlots]
   // full_a, full_b, empty, acc_full[2], acc_empty[2], raw_full[kSlots], raw_empty[kSlots]
   static constexpr uint32_t bars = raw + RawCfg<BT>::kSlots * RawCfg<BT>::kBytes;
-  static constexpr uint32_t misc = bars + (3 * kStages + 4 + 2 * RawCfg<BT>::kSlots) * 8;
+  static constexpr uint32_t misc = bars + (3 * RawCfg<BT>::kStages + 4 + 2 * RawCfg<BT>::kSlots) * 8;
   static constexpr uint32_t total = misc + 16;
 };
 template <int BT>
@@ -166,6 +169,7 @@ template <int BT>
 __global__ void __launch_bounds__(kThreads, 1)
     routed_mm_tc_kernel(const __grid_constant__ MmMaps maps, const __grid_constant__ MmParams p) {
   using L = SmemL<BT>;
+  constexpr int kStages = RawCfg<BT>::kStages;
   constexpr int kRawSlots = RawCfg<BT>::kSlots;
   constexpr uint32_t kRawBytes = RawCfg<BT>::kBytes;
   constexpr uint32_t kRawRow = RawCfg<BT>::kRow;
@@ -302,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = tc::mbar_wait(bar_acc_empty + 8 * ab, ((i >> 1) & 1) ^ 1, abort_flag);
         if (!ok) break;
         tc::tc_fence_after();
-        const uint32_t dtm = tmem + (uint32_t)(ab * kMoeTokBlock);
+        const uint32_t dtm = tmem + (uint32_t)ab * kAccCols;
         for (int jb = 0; jb < KJ; ++jb) {
           const int j = i * KJ + jb, s = j % kStages;
           const uint32_t ph = (j / kStages) & 1;
@@ -425,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = (w % n_tiles) * kTW + quarter * 32 + lane;
       for (int c0 = 0; c0 < bi.z; c0 += 32) {
         uint32_t v[32];
-        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * kMoeTokBlock + c0), v);
+        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)ab * kAccCols + (uint32_t)c0, v);
         tc::tmem_ld_wait();
         const int r_lane = c0 + lane < bi.z ? p.hids[bi.y + c0 + lane] : 0;
         const float un_lane = c0 + lane < bi.z ? p.xun[bi.y + c0 + lane] : 1.f;

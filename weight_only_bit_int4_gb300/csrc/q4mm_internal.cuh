@@ -291,13 +291,13 @@ size_t q4_0_mm_workspace_bytes(int64_t n_tokens, int64_t top_k, int64_t N, int64
 //   offs    u32 [E + 1]    exclusive prefix of htpe (offs[E] = number of valid rows)
 //   hids    i32 [R]        routed rows grouped by expert, ascending within an expert
 //   invalid u32 [1]        rows whose id is >= E
-//   blk     int4 [B]       token blocks (expert, first position in hids, count <= 128, 0)
+//   blk     int4 [B]       token blocks (expert, first position in hids, count <= kMoeTokBlock, 0)
 //   n_blk   u32 [1]        number of token blocks
 //   xs      fp16 [R, K]    x rows gathered in hids order, each scaled by a power of two
 //                          (the mm operand)
 //   xun     f32 [R]        per gathered row, the power of two that undoes its scaling
 //   tsc     f32 [R]        per token (first n_tokens entries), the power of two that scales it
-constexpr int kMoeTokBlock = 128;
+constexpr int kMoeTokBlock = 112;
 struct MoeWorkspace {
   size_t htpe, offs, hids, invalid, blk, n_blk, xs, xun, tsc, total;
 };
