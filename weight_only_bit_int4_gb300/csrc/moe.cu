@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const uint32_t *__
   uint32_t *pos = sm + n_warps * E;         // [n_warps][E]
   uint32_t *scan = pos + n_warps * E;       // [E + 1]
   __shared__ uint32_t bad_count;
+  griddep_launch_dependents();   // a mat-mat call's next kernel may start its independent work
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int active_warps = min(n_warps, (int)(blockDim.x / 32));
   for (int i = threadIdx.x; i < n_warps * E; i += blockDim.x) cnt[i] = 0;
@@ -346,6 +347,7 @@ __global__ void __launch_bounds__(kRouteParThreads) route_par_kernel(
   extern __shared__ uint32_t hist[];                 // [E] counts, then the ids [n_rows]
   __shared__ uint32_t warp_cnt[kRouteParThreads / 32];
   __shared__ uint32_t s_less, s_blkbase, s_total, s_total_blk;
+  griddep_launch_dependents();   // a mat-mat call's next kernel may start its independent work
   const int e = blockIdx.x;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const unsigned lt = (1u << lane) - 1u;

@@ -35,6 +35,8 @@
 
 #include <cudaTypedefs.h>
 
+#include <utility>
+
 namespace q4mm {
 
 Q4MM_DEFINE_ERROR_READER(read_errors_moe_tc)
@@ -192,9 +194,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int KB = p.K / kBK;                 // multiple of 4
   const int KJ = KB / kKps;                 // stages per item
   const int n_tiles = (p.N + kTW - 1) / kTW;
-  const int items = (int)*p.n_blk * n_tiles;
-  const int my_items = (int)blockIdx.x < items ? (items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  const int steps = my_items * KJ;          // stages of this CTA
   auto item_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
 
   if (threadIdx.x == 0) {
@@ -224,6 +223,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched as a programmatic dependent of the gather: everything above overlapped its
+  // tail; the routing lists and gathered rows are read only after it has completed.
+  griddep_wait();
+  const int items = (int)*p.n_blk * n_tiles;
+  const int my_items = (int)blockIdx.x < items ? (items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int steps = my_items * KJ;          // stages of this CTA
 
   if (warp == 14) {
     // ---------------- weight TMA: one 128-row box per 4 K blocks ----------------
@@ -460,6 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(256) token_scale_kernel(const float *__restrict__ x, int K,
                                                           float *__restrict__ tsc) {
   __shared__ float red[8];
+  griddep_launch_dependents();
   const float4 *row = reinterpret_cast<const float4 *>(x + (size_t)blockIdx.x * K);
   float m = 0.f;
   for (int i = threadIdx.x; i < K / 4; i += blockDim.x) {
@@ -480,6 +486,9 @@ __global__ void __launch_bounds__(256) token_scale_kernel(const float *__restric
     }
     tsc[blockIdx.x] = ldexpf(1.f, e);
   }
+  // Launched as a programmatic dependent of the routing, which it does not read: it runs
+  // alongside and completes only after the routing has, so the chain stays ordered.
+  griddep_wait();
 }
 
 // xs[p] = fp16(2^e_t * x[t]) with t = hids[p] / top_k for p < number of valid routed rows,
@@ -492,6 +501,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const float *__restric
                                                           const uint32_t *__restrict__ n_valid, int top_k, int K,
                                                           const float *__restrict__ tsc, uint16_t *__restrict__ xs,
                                                           float *__restrict__ xun, int n_rows) {
+  griddep_launch_dependents();
+  griddep_wait();   // the routing lists and token scales come from the two kernels before
   const int nv = min((int)*n_valid, n_rows);
   const int per_row = K / 8;   // items per row: K / 32 blocks x 4 chunks
   for (int pos0 = blockIdx.x * 4; pos0 < nv; pos0 += gridDim.x * 4) {
@@ -528,6 +539,25 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const float *__restric
   }
 }
 
+// Launch with programmatic stream serialization: the kernel may start while the previous
+// kernel in the stream finishes, and must call griddep_wait() before it reads that kernel's
+// output.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -559,9 +589,13 @@ cudaError_t launch_routed_mm_tc(int bt, const float *x, const uint8_t *w, float 
   int sms = 148, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
 
-  token_scale_kernel<<<(unsigned)n_tokens, 256, 0, s>>>(x, K, tsc);
-  gather_rows_kernel<<<(unsigned)(4 * sms), 256, 0, s>>>(x, hids, offs + n_experts, top_k, K, tsc, xs, xun, n_rows);
-  cudaError_t e = cudaGetLastError();
+  // token scale, gather and mat-mat are programmatic dependents of the kernel before each
+  // (every one waits for its predecessor before it reads what that wrote)
+  cudaError_t e = launch_dependent(token_scale_kernel, dim3((unsigned)n_tokens), dim3(256), 0, s, x, K, tsc);
+  if (e != cudaSuccess) return e;
+  e = launch_dependent(gather_rows_kernel, dim3((unsigned)(4 * sms)), dim3(256), 0, s, x,
+                       static_cast<const int32_t *>(hids), offs + n_experts, top_k, K,
+                       static_cast<const float *>(tsc), xs, xun, n_rows);
   if (e != cudaSuccess) return e;
 
   MmMaps maps;
@@ -603,13 +637,15 @@ cudaError_t launch_routed_mm_tc(int bt, const float *x, const uint8_t *w, float 
   if (q8) {
     e = ensure_dynamic_smem(reinterpret_cast<const void *>(routed_mm_tc_kernel<kQ8_0>), (int)mm_smem_bytes<kQ8_0>());
     if (e != cudaSuccess) return e;
-    routed_mm_tc_kernel<kQ8_0><<<(unsigned)sms, kThreads, mm_smem_bytes<kQ8_0>(), s>>>(maps, p);
+    e = launch_dependent(routed_mm_tc_kernel<kQ8_0>, dim3((unsigned)sms), dim3(kThreads), mm_smem_bytes<kQ8_0>(), s,
+                         maps, p);
   } else {
     e = ensure_dynamic_smem(reinterpret_cast<const void *>(routed_mm_tc_kernel<kQ4_0>), (int)mm_smem_bytes<kQ4_0>());
     if (e != cudaSuccess) return e;
-    routed_mm_tc_kernel<kQ4_0><<<(unsigned)sms, kThreads, mm_smem_bytes<kQ4_0>(), s>>>(maps, p);
+    e = launch_dependent(routed_mm_tc_kernel<kQ4_0>, dim3((unsigned)sms), dim3(kThreads), mm_smem_bytes<kQ4_0>(), s,
+                         maps, p);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace q4mm
