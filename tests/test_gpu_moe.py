@@ -256,14 +256,17 @@ def _run_q8(x, w, ids, top_k, N, K, E, stride, mode):
     return out.cpu().numpy().astype(np.float64)
 
 
-# Mode 2 with K % 256 == 0 and 16-byte aligned expert slabs runs the tensor-core kernel
-# (fp16 operands); the padded stride of 2 bytes and K = 96 or 32 keep the CUDA-core kernel.
-# (300, 4, 4, ...) gives every expert about 300 routed rows, three token blocks.
+# Mode 2 with K % 256 == 0 and 16-byte aligned expert slabs runs the tensor-core mat-mat
+# kernel (fp16 operands); mode 1 with K % 128 == 0 and 8-byte aligned slabs the tensor-core
+# mat-vec (16-byte copies when K % 256 == 0 and the slabs allow, else 8-byte copies and, for
+# K % 256 != 0, a 4-block tail piece).  The padded stride of 2 bytes and K = 96 or 32 keep the
+# CUDA-core kernel.  (300, 4, 4, ...) gives every expert about 300 routed rows.
 @pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("n_tokens,top_k,E,N,K,pad", [(1, 8, 64, 96, 256, 0), (5, 2, 6, 64, 2048, 2),
                                                       (40, 8, 16, 130, 512, 16), (33, 1, 3, 256, 96, 0),
                                                       (3, 4, 9, 70, 4096, 0), (2, 2, 3, 20, 32, 0),
-                                                      (300, 4, 4, 160, 768, 0)])
+                                                      (300, 4, 4, 160, 768, 0), (3, 2, 5, 40, 384, 0),
+                                                      (2, 4, 7, 48, 1408, 8), (1, 3, 4, 33, 128, 8)])
 def test_q8_0_parity(mode, n_tokens, top_k, E, N, K, pad):
     x, w, stride, ids = _q8_case(200 + n_tokens, n_tokens, top_k, E, N, K, pad)
     ref = oracle.q8_0_matmul_id(x, w, ids, n_tokens, top_k, N, K, E, stride)

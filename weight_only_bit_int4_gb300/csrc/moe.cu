@@ -514,18 +514,48 @@ __device__ __forceinline__ void cp_async_piece(uint32_t dst, const void *src, ui
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 
-// One chunk of 16 weight rows into a ring stage: PIECES copies of PIECE bytes per row
-// (compile-time counts, so the row/piece split of an item index is a multiply, not a divide).
-template <int PIECES, int PIECE>
+// One chunk of 16 weight rows into a ring stage of ROW bytes per row: PIECES copies of PIECE
+// bytes per row (compile-time counts, so the row/piece split of an item index is a multiply,
+// not a divide).
+template <int PIECES, int PIECE, int ROW = kMvcRow>
 __device__ __forceinline__ void mv_copy_rows(uint32_t slot, const uint8_t *src, size_t row_bytes, int row0,
                                              int N, int lane) {
 #pragma unroll 1
   for (int i = lane; i < 16 * PIECES; i += 32) {
     const int rr = i / PIECES, pc = i - rr * PIECES;
     const bool ok = row0 + rr < N;
-    cp_async_piece<PIECE>(slot + (uint32_t)(rr * kMvcRow + pc * PIECE),
+    cp_async_piece<PIECE>(slot + (uint32_t)(rr * ROW + pc * PIECE),
                           ok ? src + (size_t)(row0 + rr) * row_bytes + pc * PIECE : src, ok ? (uint32_t)PIECE : 0u);
   }
+}
+
+// A warp's x slice of nblk_w 32-element blocks in the decode's k order: item (block, m) is 16
+// bytes of bf16 pairs (x[4m], x[4m+2]), (x[4m+16], x[4m+18]), (x[4m+1], x[4m+3]),
+// (x[4m+17], x[4m+19]); xsum[block] = the sum of the block's bf16 values in fp32.  The
+// SwiGLU form stages silu(gate) * up.
+template <bool SWIGLU>
+__device__ __forceinline__ void mv_stage_x(uint8_t *xs, float *xsum, const float *xr, const float *ur, int nblk_w,
+                                           int lane) {
+  for (int it = lane; it < ((nblk_w * 4 + 31) & ~31); it += 32) {   // 4 consecutive lanes share a block
+    const int blk = it >> 2, m = it & 3;
+    const bool in = blk < nblk_w;
+    float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+    if (in) {
+      lo = mv_input4<SWIGLU>(xr, ur, blk * 32 + 4 * m);
+      hi = mv_input4<SWIGLU>(xr, ur, blk * 32 + 16 + 4 * m);
+    }
+    const uint32_t p0 = pack_bf16x2(lo.x, lo.z), p1 = pack_bf16x2(hi.x, hi.z);
+    const uint32_t p2 = pack_bf16x2(lo.y, lo.w), p3 = pack_bf16x2(hi.y, hi.w);
+    if (in) *reinterpret_cast<uint4 *>(xs + (size_t)blk * 64 + m * 16) = make_uint4(p0, p1, p2, p3);
+    float sum = 0.f;
+    const uint32_t pv[4] = {p0, p2, p1, p3};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sum += __uint_as_float(pv[i] << 16) + __uint_as_float(pv[i] & 0xFFFF0000u);
+    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+    if (in && m == 0) xsum[blk] = sum;
+  }
+  __syncwarp();
 }
 
 template <int KS, bool SWIGLU, int PIECE>
@@ -577,26 +607,7 @@ __global__ void __launch_bounds__(KS * 32) q4_0_mv_mma_kernel(const __grid_const
     const size_t xrow = SWIGLU ? (size_t)r : (size_t)(r / p.top_k);
     const float *xr = p.x + xrow * p.K + (size_t)c_begin * 256;
     const float *ur = SWIGLU ? p.up + xrow * p.K + (size_t)c_begin * 256 : nullptr;
-    for (int it = lane; it < ((nblk_w * 4 + 31) & ~31); it += 32) {   // 4 consecutive lanes share a block
-      const int blk = it >> 2, m = it & 3;
-      const bool in = blk < nblk_w;
-      float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
-      if (in) {
-        lo = mv_input4<SWIGLU>(xr, ur, blk * 32 + 4 * m);
-        hi = mv_input4<SWIGLU>(xr, ur, blk * 32 + 16 + 4 * m);
-      }
-      const uint32_t p0 = pack_bf16x2(lo.x, lo.z), p1 = pack_bf16x2(hi.x, hi.z);
-      const uint32_t p2 = pack_bf16x2(lo.y, lo.w), p3 = pack_bf16x2(hi.y, hi.w);
-      if (in) *reinterpret_cast<uint4 *>(xs + (size_t)blk * 64 + m * 16) = make_uint4(p0, p1, p2, p3);
-      float sum = 0.f;
-      const uint32_t pv[4] = {p0, p2, p1, p3};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sum += __uint_as_float(pv[i] << 16) + __uint_as_float(pv[i] & 0xFFFF0000u);
-      sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-      sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-      if (in && m == 0) xsum[blk] = sum;
-    }
-    __syncwarp();
+    mv_stage_x<SWIGLU>(xs, xsum, xr, ur, nblk_w, lane);
 
     const bool bl = g == t;   // B column g = block g of the sub-chunk (one token: g < 4)
     float acc[2] = {0.f, 0.f};
@@ -651,6 +662,156 @@ __global__ void __launch_bounds__(KS * 32) q4_0_mv_mma_kernel(const __grid_const
           a = __fmaf_rn(-136.f * da, X.x, a);
           a = __fmaf_rn(db, D[2 * h + 1], a);
           a = __fmaf_rn(-136.f * db, X.y, a);
+          acc[h] = t < 2 ? a : 0.f;
+        }
+      }
+      __syncwarp();
+    }
+    cp_async_wait<0>();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float v = acc[h] + __shfl_xor_sync(0xFFFFFFFFu, acc[h], 1);
+      if (t == 0) red[warp * 16 + g + 8 * h] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < 16) {
+      float v = red[threadIdx.x];
+#pragma unroll
+      for (int w = 1; w < KS; ++w) v += red[w * 16 + threadIdx.x];
+      if (row0 + (int)threadIdx.x < p.N) p.out[(size_t)r * p.N + row0 + threadIdx.x] = v;
+    }
+    __syncthreads();   // ring, x and red are reused by the next routed row
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Q8_0 mat-vec on the tensor cores (K % 128 == 0, 8-byte aligned rows): the layout of
+// q4_0_mv_mma_kernel with 272-byte row pieces (8 Q8_0 blocks; 136 bytes for a 4-block tail).
+//
+// A signed byte q is split into two nibble planes that enter the MMA exactly as bf16:
+// lo = q & 15 as 128 + lo, and hi = q >> 4 (arithmetic, -8..7) as 136 + hi (the high nibble
+// with its top bit flipped).  q = 16 hi + lo, so per (row, block)
+//     sum_k q x = 16 D_hi + D_lo - 2304 X,   D_lo = sum (128 + lo) x,  D_hi = sum (136 + hi) x,
+// with X the sum of the block's bf16 x; both D are exact sums of exact products in fp32.
+// Qs word m of a block holds elements 4m..4m+3, word m + 4 elements 4m+16..4m+19, so each
+// plane's MMA k-slots take the pairs (4m, 4m+2), (4m+16, 4m+18), (4m+1, 4m+3),
+// (4m+17, 4m+19): the x order the Q4_0 kernel stages.
+// ---------------------------------------------------------------------------------------
+constexpr int kMv8Row = 272;                   // bytes per weight row per chunk (8 Q8_0 blocks)
+constexpr int kMv8Chunk = 16 * kMv8Row;        // 4352 bytes per chunk stage
+
+__host__ __device__ inline size_t mv8_warp_bytes(int maxc) {
+  return (size_t)mvc_depth(maxc) * kMv8Chunk + (size_t)maxc * 8 * 64 + (size_t)maxc * 8 * 4;
+}
+
+template <int KS, int PIECE>
+__global__ void __launch_bounds__(KS * 32) q8_0_mv_mma_kernel(const __grid_constant__ MvParams p, int maxc) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int kPiecesFull = kMv8Row / PIECE;   // copies per row of an 8-block chunk
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int g = lane / 4, t = lane % 4;
+  const int depth = mvc_depth(maxc);
+  const size_t wb = mv8_warp_bytes(maxc);
+  uint8_t *ring = smem + (size_t)warp * wb;
+  uint8_t *xs = ring + (size_t)depth * kMv8Chunk;                      // [maxc * 8 blocks][4][16 B]
+  float *xsum = reinterpret_cast<float *>(xs + (size_t)maxc * 8 * 64);  // [maxc * 8]
+  float *red = reinterpret_cast<float *>(smem + (size_t)KS * wb);       // [KS][16]
+  const uint32_t ring_s = smem_u32(ring);
+  const int S4 = p.K / 128;                       // 4-block sub-chunks per row
+  const int C = (S4 + 1) / 2;                     // chunks of (up to) 8 blocks
+  const int c_begin = (int)(((long long)warp * C) / KS);
+  const int c_end = (int)(((long long)(warp + 1) * C) / KS);
+  const int nch = c_end - c_begin;
+  const int nblk_w = min(8 * nch, p.K / 32 - 8 * c_begin);   // blocks in this warp's slice
+  const int row0 = blockIdx.x * 16;
+  const size_t row_bytes = (size_t)(p.K / 32) * 34;
+
+  for (int r = blockIdx.y; r < p.n_rows; r += gridDim.y) {
+    const uint32_t e = __ldg(p.ids + r);
+    if (e >= (uint32_t)p.E) {   // routed to no expert: zero row, and record it
+      if (threadIdx.x < 16 && row0 + (int)threadIdx.x < p.N) p.out[(size_t)r * p.N + row0 + threadIdx.x] = 0.f;
+      if (threadIdx.x == 0 && blockIdx.x == 0) raise_device_error(Q4MM_DEVERR_BAD_EXPERT);
+      continue;
+    }
+    const uint8_t *wexp = p.w + (size_t)e * p.expert_stride;
+    auto issue = [&](int c) {
+      const uint32_t slot = ring_s + (uint32_t)((c % kMvcDepth) * kMv8Chunk);
+      const int a = c_begin + c;
+      const uint8_t *src = wexp + (size_t)a * kMv8Row;
+      if (2 * a + 1 < S4)
+        mv_copy_rows<kPiecesFull, PIECE, kMv8Row>(slot, src, row_bytes, row0, p.N, lane);
+      else   // 4-block tail chunk
+        mv_copy_rows<kPiecesFull / 2, PIECE, kMv8Row>(slot, src, row_bytes, row0, p.N, lane);
+    };
+#pragma unroll
+    for (int i = 0; i < kMvcDepth - 1; ++i) {
+      if (i < nch) issue(i);
+      cp_async_commit();
+    }
+
+    const float *xr = p.x + (size_t)(r / p.top_k) * p.K + (size_t)c_begin * 256;
+    mv_stage_x<false>(xs, xsum, xr, nullptr, nblk_w, lane);
+
+    const bool bl = g == t;   // B column g = block g of the sub-chunk (one token: g < 4)
+    float acc[2] = {0.f, 0.f};
+    for (int c = 0; c < nch; ++c) {
+      if (c + kMvcDepth - 1 < nch) issue(c + kMvcDepth - 1);
+      cp_async_commit();
+      cp_async_wait<kMvcDepth - 1>();
+      __syncwarp();
+      const uint8_t *slot = ring + (c % kMvcDepth) * kMv8Chunk;
+      const int nsub = 2 * (c_begin + c) + 1 < S4 ? 2 : 1;
+      for (int sc = 0; sc < nsub; ++sc) {   // sub-chunks of 4 blocks; quad lane t decodes block 4 sc + t
+        const int bk = 4 * sc + t;
+        const int off = 34 * bk + 2;                    // qs of block bk within a row
+        const uint32_t sel = (off & 2) ? 0x5432u : 0x3210u;
+        uint32_t qs[2][8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t *u = reinterpret_cast<const uint32_t *>(slot + (g + 8 * h) * kMv8Row + (off & ~3));
+          uint32_t v[9];
+#pragma unroll
+          for (int i = 0; i < 9; ++i) v[i] = u[i];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) qs[h][i] = prmt(v[i], v[i + 1], sel);
+        }
+        uint4 xb[4];
+        const uint8_t *xl = xs + (size_t)(c * 8 + bk) * 64;
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          xb[m] = bl ? *reinterpret_cast<const uint4 *>(xl + m * 16) : make_uint4(0, 0, 0, 0);
+        float Dl[4] = {0.f, 0.f, 0.f, 0.f}, Dh[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const uint32_t w0 = qs[0][m], w1 = qs[1][m], v0 = qs[0][m + 4], v1 = qs[1][m + 4];
+          constexpr uint32_t kMask = 0x000F000Fu, kMagic = 0x43004300u;   // bf16 128 + lo
+          constexpr uint32_t kFlip = 0x43084308u;                         // bf16 136 + hi
+          const uint32_t l0[4] = {and_or(w0, kMask, kMagic), and_or(w1, kMask, kMagic),
+                                  and_or(v0, kMask, kMagic), and_or(v1, kMask, kMagic)};
+          const uint32_t l1[4] = {and_or(w0 >> 8, kMask, kMagic), and_or(w1 >> 8, kMask, kMagic),
+                                  and_or(v0 >> 8, kMask, kMagic), and_or(v1 >> 8, kMask, kMagic)};
+          const uint32_t h0[4] = {((w0 >> 4) & kMask) ^ kFlip, ((w1 >> 4) & kMask) ^ kFlip,
+                                  ((v0 >> 4) & kMask) ^ kFlip, ((v1 >> 4) & kMask) ^ kFlip};
+          const uint32_t h1[4] = {((w0 >> 12) & kMask) ^ kFlip, ((w1 >> 12) & kMask) ^ kFlip,
+                                  ((v0 >> 12) & kMask) ^ kFlip, ((v1 >> 12) & kMask) ^ kFlip};
+          mma_bf16_16816(Dl, l0, xb[m].x, xb[m].y);
+          mma_bf16_16816(Dl, l1, xb[m].z, xb[m].w);
+          mma_bf16_16816(Dh, h0, xb[m].x, xb[m].y);
+          mma_bf16_16816(Dh, h1, xb[m].z, xb[m].w);
+        }
+        // columns 2t, 2t+1 = blocks 4 sc + 2t, +1 for t < 2; zero columns for t >= 2
+        const int ba = 4 * sc + 2 * (t & 1);
+        const float2 X = *reinterpret_cast<const float2 *>(xsum + c * 8 + ba);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint8_t *rowp = slot + (g + 8 * h) * kMv8Row;
+          const float da = f16_bits_to_float(*reinterpret_cast<const uint16_t *>(rowp + 34 * ba));
+          const float db = f16_bits_to_float(*reinterpret_cast<const uint16_t *>(rowp + 34 * (ba + 1)));
+          float a = acc[h];
+          a = __fmaf_rn(da, __fmaf_rn(16.f, Dh[2 * h], Dl[2 * h]), a);
+          a = __fmaf_rn(-2304.f * da, X.x, a);
+          a = __fmaf_rn(db, __fmaf_rn(16.f, Dh[2 * h + 1], Dl[2 * h + 1]), a);
+          a = __fmaf_rn(-2304.f * db, X.y, a);
           acc[h] = t < 2 ? a : 0.f;
         }
       }
@@ -797,8 +958,31 @@ cudaError_t launch_q4_0_mm(const float *x, const uint8_t *w, const uint32_t *ids
   return cudaGetLastError();
 }
 
+// Q8_0 mat-vec on the tensor cores: kernel instance for (warps, copy size).
+cudaError_t launch_q8_0_mv_mma(const MvParams &p, int ks, int maxc, size_t smem, bool a16, cudaStream_t s) {
+  const void *fn;
+  if (a16)
+    fn = ks == 4 ? reinterpret_cast<const void *>(q8_0_mv_mma_kernel<4, 16>)
+       : ks == 2 ? reinterpret_cast<const void *>(q8_0_mv_mma_kernel<2, 16>)
+                 : reinterpret_cast<const void *>(q8_0_mv_mma_kernel<1, 16>);
+  else
+    fn = ks == 4 ? reinterpret_cast<const void *>(q8_0_mv_mma_kernel<4, 8>)
+       : ks == 2 ? reinterpret_cast<const void *>(q8_0_mv_mma_kernel<2, 8>)
+                 : reinterpret_cast<const void *>(q8_0_mv_mma_kernel<1, 8>);
+  cudaError_t e = ensure_dynamic_smem(fn, (int)smem);
+  if (e != cudaSuccess) return e;
+  MvParams pp = p;
+  int mc = maxc;
+  void *args[] = {&pp, &mc};
+  const dim3 grid((unsigned)((p.N + 15) / 16), (unsigned)(p.n_rows < 65535 ? p.n_rows : 65535), 1);
+  e = cudaLaunchKernel(fn, grid, dim3(ks * 32), args, smem, s);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // GGML Q8_0 routed matmul (the type is among the routed kernels of quantized_matmul_id_ggml.rs):
-// mat-vec visits routed rows in order on the fp32 FMA kernel.  Mat-mat routes first
+// mat-vec visits routed rows in order, on the tensor cores when the rows allow it (K % 128
+// == 0; 16-byte copies need K % 256 == 0 and 16-byte aligned slabs, 8-byte copies 8-byte
+// aligned ones), else on the fp32 FMA kernel.  Mat-mat routes first
 // (per-expert lists and token blocks in the workspace); with K % 256 == 0 and 16-byte aligned
 // expert slabs it runs the tensor-core kernel of the Q4_0 form with the Q8_0 decode, else it
 // visits the rows expert by expert on the FMA kernel, so that the CTAs running at one time
@@ -811,6 +995,18 @@ cudaError_t launch_q8_0_matmul_id(const float *x, const uint8_t *w, const uint32
   p.x = x; p.up = nullptr; p.w = w; p.ids = ids; p.order = nullptr; p.n_order = nullptr; p.out = out;
   p.n_rows = n_rows; p.top_k = top_k; p.N = N; p.K = K; p.E = n_experts;
   p.expert_stride = expert_stride;
+  if (!mm) {
+    const uintptr_t wa = reinterpret_cast<uintptr_t>(w);
+    const bool a16 = K % 256 == 0 && expert_stride % 16 == 0 && (wa & 15) == 0;
+    const bool a8 = K % 128 == 0 && expert_stride % 8 == 0 && (wa & 7) == 0;
+    if (a16 || a8) {
+      const int C = (K / 128 + 1) / 2;
+      const int ks = C >= 4 ? 4 : (C >= 2 ? 2 : 1);
+      const int maxc = (C + ks - 1) / ks;
+      const size_t smem = (size_t)ks * mv8_warp_bytes(maxc) + (size_t)ks * 16 * 4;
+      if (smem <= 227 * 1024) return launch_q8_0_mv_mma(p, ks, maxc, smem, a16, s);
+    }
+  }
   if (mm) {
     const MoeWorkspace L = moe_workspace_layout(n_rows, K, n_experts);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
