@@ -317,18 +317,18 @@ void q4mm_record_free(q4mm_record *rec);
 /* ======================================================================================
  * Allocation-free variant of the mat-mat form (the source pages have no counterpart).
  *
- * For callers that cannot obtain device memory at the moment of the call -- code running
- * inside a stream capture they do not control, serving loops that must never wait on or fail
- * in the device allocator, hosts that own all device buffers.  Computes exactly what
+ * For callers that cannot obtain device memory at the moment of the call -- serving loops
+ * that must never wait on or fail in the device allocator, hosts that own all device
+ * buffers.  Computes exactly what
  * q4_0_matmul_id computes in mode 2 (mat-mat), with the same argument rules, but takes no
  * workspace: its scratch is a fixed Q4MM_NOALLOC_SCRATCH_BYTES array built into the library,
  * held on every device that loads the library until process exit.
  *   - Returns Q4MM_ERR_WORKSPACE, launching nothing, when
  *     q4_0_matmul_id_workspace_size(n_tokens, top_k, N, K, n_experts) exceeds the array.
  *   - The first call on a device (made with that device current) looks up the array's device
- *     address; make that first call before any stream capture that includes this call.
- *     Later calls on a stream that is not capturing look it up again, so after a device reset
- *     (cudaDeviceReset) the next such call picks up the new address; make one before capturing.
+ *     address (cudaGetSymbolAddress; no allocation) and keeps it.  Later calls look it up
+ *     again unless their stream reports that it is capturing, so after a device reset
+ *     (cudaDeviceReset) the next call picks up the new address.
  *   - All calls on a device share the array.  Calls that overlap on the GPU race on it and
  *     give wrong results: order them (for instance on one stream).
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.

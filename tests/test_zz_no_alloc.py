@@ -1,9 +1,9 @@
 """The allocation-free Q4_0 mat-mat entry point (q4_0_matmul_id_noalloc), called through the
 C ABI, against the workspace entry point (q4_0_matmul_id, mode 2) on the same inputs.
 
-It exists for callers that cannot allocate device memory when they call the library (inside
-someone else's stream capture, in allocator-free serving loops, in hosts that own all device
-buffers); it uses the library's fixed scratch array instead of a caller workspace.  Two calls
+It exists for callers that cannot allocate device memory when they call the library
+(allocator-free serving loops, hosts that own all device buffers); it uses the library's
+fixed scratch array instead of a caller workspace.  Two calls
 in a row with different sizes check that nothing depends on what the previous call left in
 the shared array."""
 import ctypes

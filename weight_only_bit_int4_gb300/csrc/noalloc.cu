@@ -2,21 +2,18 @@
 // callers that cannot allocate device memory when they call it.
 //
 // q4_0_matmul_id needs a caller-provided workspace for its routing lists and gathered rows.
-// Some callers have no way to get one at the moment of the call: code that runs while a
-// stream is being captured by someone else (a cudaMalloc there is illegal or breaks the
-// capture), serving loops that must never block on the device allocator or fail under
-// memory pressure, and hosts (plugins, runtimes) that own every device buffer and hand
-// out none.  This entry point needs no workspace from them: its scratch is one fixed
+// Some callers have no way to get one at the moment of the call: serving loops that must
+// never block on the device allocator or fail under memory pressure, and hosts (plugins,
+// runtimes) that own every device buffer and hand out none.  This entry point needs no workspace from them: its scratch is one fixed
 // array compiled into the library, below.
 //
 // The array is a file-scope __device__ variable, so every GPU that loads this library holds
 // Q4MM_NOALLOC_SCRATCH_BYTES of it until the process exits.  Host code cannot use the
 // array's name as a device address; on the first call on a device (with that device
-// current) the address is fetched with cudaGetSymbolAddress and kept per device.  That first
-// call should therefore happen before any stream capture that includes this call.  Every
-// later call whose stream is not capturing fetches the address again, so a device reset
-// (which reloads the library's module in a new context) leaves no stale address behind;
-// calls made while their stream is capturing use the kept one.
+// current) the address is fetched with cudaGetSymbolAddress and kept per device.  Every
+// later call fetches it again unless its stream reports that it is capturing (then the kept
+// one is used), so a device reset (which reloads the library's module in a new context)
+// leaves no stale address behind.
 //
 // All calls on a device share the one array, which keeps whatever the previous call left.
 // Nothing in it has to start at zero: each call's routing pass rewrites every routing field
