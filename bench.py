@@ -607,8 +607,8 @@ def bench_moe(args, q, synth, to_dev, ring_of, time_graph, dev, pk):
                                                       Nd, Kd, E, stride_d) for l in range(L)], L, replays=5) / L
     swiglu = {"n_tokens": n_tokens, "N": Nd, "K": Kd, "us": round(t * 1e6, 2), "GB_s": round(by / t / 1e9, 1),
               "frac_hbm": round(by / t / 1e9 / pk["hbm_gbs"], 3)}
-    # GGML Q8_0 routed matmul on the same MoE shape (34-byte blocks): mat-vec at one token,
-    # mat-mat (route, then the routed rows expert by expert) at 512 tokens.
+    # GGML Q8_0 routed matmul on the same MoE shape (34-byte blocks): mat-vec at one token
+    # (tensor cores, two nibble planes), mat-mat (route, scale, gather, tcgen05) at 512 tokens.
     w8, stride8 = synth.q8_0_experts(4700, E, N, K)
     ring8 = ring_of((to_dev(w8),), w8.nbytes)
     q8 = []
