@@ -10,7 +10,7 @@
 //     order, each token scaled by a power of two that brings its largest magnitude into
 //     [2^14, 2^15) (found once per token by token_scale_kernel);
 //  3. routed_mm_tc_kernel<BT>, persistent over work items (token block, 128-row weight tile):
-//       A = the expert's weight rows, decoded to fp16 by four producer warps from TMA boxes of
+//       A = the expert's weight rows, decoded to fp16 by eight producer warps from TMA boxes of
 //           8 blocks per row (256 k): 144 bytes for Q4_0 (18-byte blocks), 272 for Q8_0
 //           (34-byte blocks);
 //       B = the block's gathered x rows (TMA, 64-row boxes, 128-byte swizzle);
@@ -27,10 +27,12 @@
 // could take a weight beyond fp16's range (|value| >= 65520: |d| >= 8192 in Q4_0, >= 512 in
 // Q8_0) is reported as Q4MM_DEVERR_F16_RANGE.  The mat-vec form rounds x to bf16 instead.
 //
-// Pipeline: two stages of two 64-k tiles each (A and B).  The producers publish a stage on
+// Pipeline: stages of two 64-k tiles each (A and B), three for Q4_0 and two for Q8_0.  The
+// producers publish a stage on
 // full_a once their A tiles are written and the stage's B tiles (TMA) have landed, so the
-// single MMA thread waits on one barrier and commits once per 128 k: its per-stage waits,
-// fences and commits, not the tensor core, had set the pace at one barrier pair per 64 k.
+// single MMA thread waits on one barrier and commits once per 128 k.  That thread sets the
+// pace: each tcgen05.mma costs it 50-100 cycles to issue, more than the tensor core needs
+// for a 128 x 64 x 16 product.
 #include "tc_common.cuh"
 
 #include <cudaTypedefs.h>
