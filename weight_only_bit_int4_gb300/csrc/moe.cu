@@ -692,7 +692,7 @@ __global__ void __launch_bounds__(KS * 32) q4_0_mv_mma_kernel(const __grid_const
 // lo = q & 15 as 128 + lo, and hi = q >> 4 (arithmetic, -8..7) as 136 + hi (the high nibble
 // with its top bit flipped).  q = 16 hi + lo, so per (row, block)
 //     sum_k q x = 16 D_hi + D_lo - 2304 X,   D_lo = sum (128 + lo) x,  D_hi = sum (136 + hi) x,
-// with X the sum of the block's bf16 x; both D are exact sums of exact products in fp32.
+// with X the sum of the block's bf16 x; both D are fp32 sums of exact products.
 // Qs word m of a block holds elements 4m..4m+3, word m + 4 elements 4m+16..4m+19, so each
 // plane's MMA k-slots take the pairs (4m, 4m+2), (4m+16, 4m+18), (4m+1, 4m+3),
 // (4m+17, 4m+19): the x order the Q4_0 kernel stages.
