@@ -818,6 +818,7 @@ CASES = {
     "lut4_f16_m1": "lut4_matmul M=1 K=N=4096, weights rounded to f16 (CUDA-core row kernel)",
     "moe_n1": "q4_0_matmul_id n_tokens=1 (mat-vec)",
     "moe_n512": "q4_0_matmul_id n_tokens=512 (mat-mat)",
+    "moe_q8_n1": "q8_0_matmul_id n_tokens=1 (mat-vec)",
     "moe_q8_n512": "q8_0_matmul_id n_tokens=512 (mat-mat)",
     "swiglu_n1": "q4_0_matmul_id_swiglu n_tokens=1, K=1408 -> N=2048 (fused SwiGLU mat-vec)",
 }
@@ -863,8 +864,9 @@ def run_case(name: str, launches: int = 3):
         Wd, idd = to_dev(w), to_dev(ids.view(np.int32))
         out = torch.empty((top_k, N), dtype=torch.float32, device=dev)
         fn = lambda: q.q4_0_matmul_id_swiglu(gate, up, Wd, idd, out, top_k, N, K, E, stride)
-    elif name == "moe_q8_n512":
-        n_tokens, E, top_k, N, K = 512, 64, 8, 1408, 2048
+    elif name in ("moe_q8_n1", "moe_q8_n512"):
+        n_tokens = 1 if name == "moe_q8_n1" else 512
+        E, top_k, N, K = 64, 8, 1408, 2048
         w, stride = synth.q8_0_experts(4000, E, N, K)
         ids = synth.routing_ids(4100 + n_tokens, n_tokens, top_k, E)
         x = to_dev(synth.activations_f32(4200 + n_tokens, n_tokens, K))
@@ -872,7 +874,8 @@ def run_case(name: str, launches: int = 3):
         out = torch.empty((n_tokens * top_k, N), dtype=torch.float32, device=dev)
         ws = torch.empty(q.q8_0_matmul_id_workspace_size(n_tokens, top_k, N, K, E), dtype=torch.uint8,
                          device=dev)
-        fn = lambda: q.q8_0_matmul_id(x, Wd, idd, out, top_k, N, K, E, stride, mode=2, workspace=ws)
+        mode = 1 if n_tokens == 1 else 2
+        fn = lambda: q.q8_0_matmul_id(x, Wd, idd, out, top_k, N, K, E, stride, mode=mode, workspace=ws)
     else:
         n_tokens = 1 if name == "moe_n1" else 512
         E, top_k, N, K = 64, 8, 1408, 2048
