@@ -40,6 +40,8 @@
 //  CTA; tensor memory is always released).
 #include "tc_common.cuh"
 
+#include <cstdlib>
+
 #include <cudaTypedefs.h>
 
 namespace q4mm {
@@ -758,7 +760,13 @@ TilePlan pick_tile_plan(const TcGemmParams &p) {
       if (S > 1 && cost < bestS) { bestS = cost; planS = TilePlan{tt, S}; }
     }
   }
-  return bestS < 0.9 * best1 ? planS : best;
+  TilePlan chosen = bestS < 0.9 * best1 ? planS : best;
+#ifdef Q4MM_TUNING
+  // Tuning builds only: environment overrides of the tile plan, for plan sweeps.
+  if (const char *v = getenv("Q4MM_GEMM_TT")) chosen.tt = atoi(v);
+  if (const char *v = getenv("Q4MM_GEMM_S")) chosen.S = atoi(v);
+#endif
+  return chosen;
 }
 
 template <bool LUT, int TT>
