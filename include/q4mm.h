@@ -255,10 +255,12 @@ q4mm_status q4_0_matmul_id_swiglu(const float *gate, const float *up, const void
  *   out[r][n] = sum_k x[r / top_k][k] * W[ids[r]][n][k]   (f32, fp32 accumulation);
  *   an id >= n_experts gives a zero row and sets Q4MM_DEVERR_BAD_EXPERT.
  * Mode 0 (automatic: mat-mat when n_tokens > Q4MM_MM_ID_THRESHOLD), 1 (mat-vec: each routed
- * row in order, fp32 FMA) or 2 (mat-mat: route, then the tensor-core kernel of q4_0_matmul_id
- * with the Q8_0 decode when K % 256 == 0 and w and expert_stride are 16-byte aligned --
- * weights q*d rounded once to fp16, see Q4MM_DEVERR_F16_RANGE -- else the routed rows expert by
- * expert on the fp32 FMA pipes).  The mat-mat form needs q8_0_matmul_id_workspace_size(...)
+ * row in order; on the tensor cores when K % 128 == 0 and w and expert_stride are 8-byte
+ * aligned -- x rounded to bf16, the byte products exact, fp32 sums -- else fp32 FMA) or 2
+ * (mat-mat: route, then the tensor-core kernel of q4_0_matmul_id with the Q8_0 decode when
+ * K % 256 == 0 and w and expert_stride are 16-byte aligned -- weights q*d rounded once to
+ * fp16, see Q4MM_DEVERR_F16_RANGE -- else the routed rows expert by expert on the fp32 FMA
+ * pipes).  The mat-mat form needs q8_0_matmul_id_workspace_size(...)
  * bytes of 256-byte aligned workspace (the routing lists and the gathered x rows).
  * Requirements: K % 32 == 0, expert_stride >= N*(K/32)*34, x and out 16-byte aligned, ids
  * 4-byte aligned. */
