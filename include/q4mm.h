@@ -299,6 +299,17 @@ q4mm_status q4_gemv_record_launch(const q4mm_record *rec, const uint16_t *x, con
                                   const uint16_t *scales, const uint16_t *biases, uint16_t *y,
                                   q4mm_stream_t stream);
 
+/* Replay n gemv records in order on one stream, in one host call (a decode step's sequence
+ * of planned calls): record i on x[i], w[i], scales[i], biases[i], y[i] (host arrays of n
+ * device pointers, each as q4_gemv_record_launch requires).  Every record and pointer is
+ * checked before anything is launched; on a check failure nothing is launched.  A launch
+ * error stops the sequence (the launches before it stay enqueued).  0 <= n <= 65536;
+ * n = 0 is a no-op. */
+q4mm_status q4_gemv_record_launch_n(const q4mm_record *const *recs, const uint16_t *const *x,
+                                    const uint32_t *const *w, const uint16_t *const *scales,
+                                    const uint16_t *const *biases, uint16_t *const *y, int64_t n,
+                                    q4mm_stream_t stream);
+
 /* Record the routed Q4_0 mat-vec: q4_0_matmul_id in mode 1 (swiglu = 0) or
  * q4_0_matmul_id_swiglu (swiglu = 1), with the argument rules of those calls.  The plan
  * assumes the weight pointer of every replay is 16-byte aligned when K % 256 == 0 and

@@ -128,5 +128,11 @@ def test_record_argument_checks(L):
     assert L.q4_0_matmul_id_mv_record(1, 8, 64, 64, 16, 1 << 20, 2, ctypes.byref(out)) == 1
     # launching without a record, and freeing NULL
     assert L.q4_gemv_record_launch(None, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 1
+    # the batched replay: n = 0 is a no-op, missing arrays, records or pointers are refused
+    arr = (ctypes.c_void_p * 1)
+    assert L.q4_gemv_record_launch_n(None, None, None, None, None, None, 0, None) == 0
+    assert L.q4_gemv_record_launch_n(None, None, None, None, None, None, 1, None) == 1
+    assert L.q4_gemv_record_launch_n(arr(None), arr(FAKE), arr(FAKE), arr(FAKE), arr(FAKE), arr(FAKE), 1, None) == 1
+    assert L.q4_gemv_record_launch_n(arr(None), arr(FAKE), arr(FAKE), arr(FAKE), arr(FAKE), arr(FAKE), -1, None) == 1
     assert L.q4_0_matmul_id_mv_record_launch(None, FAKE, None, FAKE, FAKE, FAKE, None) == 1
     L.q4mm_record_free(None)

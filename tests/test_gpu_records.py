@@ -32,6 +32,42 @@ def test_gemv_record_matches_direct_call(M, N, K, static_weights):
     rec.close()
 
 
+def test_gemv_record_launch_n_matches_single_replays():
+    """The batched replay launches each record's kernel in order on one stream: outputs
+    bit-identical to one replay per record, including a chain where a later call reads an
+    earlier call's y as its x."""
+    shapes = [(1, 4096, 4096), (4, 1000, 384), (16, 256, 512), (3, 1000, 2080), (16, 512, 1000 // 32 * 32)]
+    recs, args_b, args_1, outs_b, outs_1 = [], [], [], [], []
+    for i, (M, N, K) in enumerate(shapes):
+        w, s, b = synth.int4_weights(90 + i, N, K)
+        x = dev(synth.activations_bf16(91 + i, M, K))
+        W = (dev(w), dev(s), dev(b))
+        recs.append(q.q4_gemv_record(M, N, K, static_weights=(i % 2 == 0)))
+        yb, y1 = poisoned_bf16(M, N), poisoned_bf16(M, N)
+        args_b.append((x, *W, yb))
+        args_1.append((x, *W, y1))
+        outs_b.append(yb)
+        outs_1.append(y1)
+    # chain: the last shape's x is the previous shape's y (M = 16, K = 512 -> N = 256 ... ) where
+    # the shapes allow it: shape 2 has M = 16, N = 256; feed its y to a record of K = 256
+    w, s, b = synth.int4_weights(99, 128, 256)
+    W = (dev(w), dev(s), dev(b))
+    recs.append(q.q4_gemv_record(16, 128, 256, static_weights=True))
+    yb, y1 = poisoned_bf16(16, 128), poisoned_bf16(16, 128)
+    args_b.append((outs_b[2], *W, yb))
+    args_1.append((outs_1[2], *W, y1))
+    outs_b.append(yb)
+    outs_1.append(y1)
+    q.q4_gemv_record_launch_n(recs, *[list(a) for a in zip(*args_b)])
+    for r, a in zip(recs, args_1):
+        r.gemv(*a)
+    torch.cuda.synchronize()
+    for yb, y1 in zip(outs_b, outs_1):
+        np.testing.assert_array_equal(host_u16(yb), host_u16(y1))
+    for r in recs:
+        r.close()
+
+
 def test_gemv_record_survives_smaller_plans_of_the_same_kernel():
     """Several shapes share one decode kernel with different shared-memory sizes.  A record
     planned for the largest must still launch after smaller shapes of the same kernel were

@@ -206,6 +206,32 @@ def q4_gemv_record(M: int, N: int, K: int, static_weights: bool = False) -> Reco
     return Record("gemv", h.value)
 
 
+class RecordBatch:
+    """A prepared q4_gemv_record_launch_n call: records[i] on xs[i], ws[i], scales[i],
+    biases[i], ys[i].  The host pointer arrays are built once (the tensors are kept alive);
+    launch() replays all the records in order in one library call."""
+
+    def __init__(self, records, xs, ws, scales, biases, ys):
+        n = len(records)
+        if not all(len(v) == n for v in (xs, ws, scales, biases, ys)):
+            raise ValueError("RecordBatch: every list needs one entry per record")
+        arr = ctypes.c_void_p * n
+        self._keep = (list(records), list(xs), list(ws), list(scales), list(biases), list(ys))
+        self._arrays = (arr(*[r._h for r in records]), arr(*[_ptr(t) for t in xs]), arr(*[_ptr(t) for t in ws]),
+                        arr(*[_ptr(t) for t in scales]), arr(*[_ptr(t) for t in biases]),
+                        arr(*[_ptr(t) for t in ys]))
+        self._n = n
+
+    def launch(self, stream=None) -> None:
+        _check("q4_gemv_record_launch_n", lib().q4_gemv_record_launch_n(*self._arrays, self._n, _stream(stream)))
+
+
+def q4_gemv_record_launch_n(records, xs, ws, scales, biases, ys, stream=None) -> None:
+    """Replay gemv records in order in one library call: records[i] on xs[i], ws[i],
+    scales[i], biases[i], ys[i] (q4_gemv_record_launch_n)."""
+    RecordBatch(records, xs, ws, scales, biases, ys).launch(stream)
+
+
 def q4_0_matmul_id_mv_record(n_tokens: int, top_k: int, N: int, K: int, n_experts: int,
                              expert_stride: int, swiglu: bool = False) -> Record:
     h = ctypes.c_void_p()

@@ -33,6 +33,7 @@ SIGNATURES = {
     "q8_0_matmul_id": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_uint64, _S, _P, ctypes.c_size_t, _P], _S),
     "q4_gemv_record": ([_I, _I, _I, ctypes.c_uint32, ctypes.POINTER(_P)], _S),
     "q4_gemv_record_launch": ([_P, _P, _P, _P, _P, _P, _P], _S),
+    "q4_gemv_record_launch_n": ([ctypes.POINTER(_P)] * 6 + [_I, _P], _S),
     "q4_0_matmul_id_mv_record": ([_I, _I, _I, _I, _I, ctypes.c_uint64, _S, ctypes.POINTER(_P)], _S),
     "q4_0_matmul_id_mv_record_launch": ([_P, _P, _P, _P, _P, _P, _P], _S),
     "q4mm_record_free": ([_P], None),

@@ -401,6 +401,31 @@ q4mm_status q4_gemv_record_launch(const q4mm_record *rec, const uint16_t *x, con
   return from_cuda(replay_q4_gemv(rec->impl, x, w, scales, biases, y, (cudaStream_t)stream));
 }
 
+q4mm_status q4_gemv_record_launch_n(const q4mm_record *const *recs, const uint16_t *const *x,
+                                    const uint32_t *const *w, const uint16_t *const *scales,
+                                    const uint16_t *const *biases, uint16_t *const *y, int64_t n,
+                                    q4mm_stream_t stream) {
+  if (n == 0) return Q4MM_OK;
+  if (n < 0 || n > 65536 || !recs || !x || !w || !scales || !biases || !y) return Q4MM_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < n; ++i) {
+    if (!recs[i] || recs[i]->kind != kRecGemv) return Q4MM_ERR_INVALID_ARG;
+    if (!x[i] || !w[i] || !scales[i] || !biases[i] || !y[i]) return Q4MM_ERR_INVALID_ARG;
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return Q4MM_ERR_CUDA;
+  for (int64_t i = 0; i < n; ++i) {
+    if (recs[i]->device != dev) return Q4MM_ERR_DEVICE;
+    if (!aligned(x[i], 16) || !aligned(w[i], 16) || !aligned(scales[i], 16) || !aligned(biases[i], 16) ||
+        !aligned(y[i], 16))
+      return Q4MM_ERR_UNSUPPORTED;
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    const cudaError_t e = replay_q4_gemv(recs[i]->impl, x[i], w[i], scales[i], biases[i], y[i], (cudaStream_t)stream);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return Q4MM_OK;
+}
+
 q4mm_status q4_0_matmul_id_mv_record(int64_t n_tokens, int64_t top_k, int64_t N, int64_t K,
                                      int64_t n_experts, uint64_t expert_stride, int swiglu,
                                      q4mm_record **out) {
