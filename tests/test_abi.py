@@ -136,3 +136,10 @@ def test_record_argument_checks(L):
     assert L.q4_gemv_record_launch_n(arr(None), arr(FAKE), arr(FAKE), arr(FAKE), arr(FAKE), arr(FAKE), -1, None) == 1
     assert L.q4_0_matmul_id_mv_record_launch(None, FAKE, None, FAKE, FAKE, FAKE, None) == 1
     L.q4mm_record_free(None)
+
+
+def test_record_batch_checks_its_lists():
+    # the Python side refuses lists of different lengths before any library call
+    import weight_only_bit_int4_gb300 as q
+    with pytest.raises(ValueError):
+        q.RecordBatch([], [1], [], [], [], [])
